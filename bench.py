@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV attention step on GB300.
+
+A step is the whole hot path over one batch: pkv_write of the step's new K/V
+rows, then pkv_attention (plan, decode and prefill kernels) over the paged
+cache.  The default workload is the pure MHA decode batch (256 requests, cached
+lengths uniform in [512, 4096], Hq = Hkv = 32, head size 128, block size 16),
+reported as KV GB/s: the K and V bytes every request's attention reads once
+per KV head, divided by the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...   # the float64 CPU oracle, same workload
+
+With N > 1 (launched by torchrun, one process per GPU) every rank runs its own
+replica of the batch (the step shards by request with no exchange), and the
+value is the total over ranks divided by the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from paged_kv_attention_05_gb300 import workloads as W  # noqa: E402
+
+DECODE_CONFIGS = {"mha_decode", "gqa_decode", "mqa_long_decode"}
+
+
+def metric_of(spec):
+    if spec.name in DECODE_CONFIGS:
+        return "paged-attn decode KV GB/s", "GB/s"
+    if spec.name == "large_prefill":
+        return "paged-attn prefill TFLOP/s", "TFLOP/s"
+    return "mixed-batch query tokens/s", "tokens/s"
+
+
+def causal_flops(spec):
+    """4 * head_size flops per (visible key, query row, query head)."""
+    tot = 0
+    for c, n in zip(spec.ctx, spec.q_len):
+        tot += n * c + n * (n + 1) // 2
+    return 4 * spec.head_size * spec.hq * tot
+
+
+def metric_work(spec):
+    """Units of the metric one step processes."""
+    name, unit = metric_of(spec)
+    if unit == "GB/s":
+        return spec.kv_bytes() / 1e9
+    if unit == "TFLOP/s":
+        return causal_flops(spec) / 1e12
+    return float(spec.num_tokens)
+
+
+def decode_algorithmic_bytes(spec):
+    """Algorithmic bytes of one decode-kernel launch: every decode request's
+    K and V rows once per KV head, its query rows read and output rows
+    written (bf16)."""
+    b = 0
+    for c, n in zip(spec.ctx, spec.q_len):
+        if n == 1:
+            b += (c + 1) * spec.hkv * spec.head_size * 2 * 2
+            b += 2 * spec.hq * spec.head_size * 2
+    return b
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, sources):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.json" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != source_hash(sources):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(step, sample_reqs=None):
+    """The float64 oracle on the host cores over (a sample of) the same step."""
+    import oracle
+    spec = step.spec
+    R = spec.num_reqs if sample_reqs is None else min(sample_reqs, spec.num_reqs)
+    kc, vc = step.key_cache, step.value_cache
+    t0 = time.perf_counter()
+    oracle.write(step.k, step.v, kc, vc, step.slot_mapping)
+    qsl = step.query_start_loc[:R + 1]
+    oracle.attention(step.q, kc, vc, qsl, step.seq_lens[:R], step.block_table[:R], R,
+                     step.scale)
+    dt = time.perf_counter() - t0
+    sub = W.StepSpec(spec.name, spec.ctx[:R], spec.q_len[:R], spec.hq, spec.hkv,
+                     spec.num_blocks, spec.seed)
+    work = metric_work(sub)
+    return {"value": work / dt, "unit": metric_of(spec)[1], "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d requests, one step (write + attention), %.1f s" %
+                      (R, spec.num_reqs, dt)}
+
+
+def run_reference(args, spec, rank):
+    """--impl reference: the float64 CPU oracle as it stands, same workload."""
+    if rank != 0:
+        return
+    import oracle
+    step = W.build(spec)
+    name, unit = metric_of(spec)
+    # size each step as a bounded sample of the workload (whole batch if cheap)
+    probe = cpu_baseline(step, sample_reqs=min(8, spec.num_reqs))
+    per_req = (metric_work(spec) / spec.num_reqs) / probe["value"]
+    sample = max(1, min(spec.num_reqs, int(8.0 / max(per_req, 1e-9))))
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_baseline(step, sample)
+    times, work = [], None
+    for _ in range(args.steps):
+        r = cpu_baseline(step, sample)
+        times.append(r)
+    vals = [t["value"] for t in times]
+    value = statistics.median(vals)
+    rec = {"metric": name, "value": value, "unit": unit, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": spec.name, "requests_per_step": sample},
+           "impl": "reference",
+           "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": times[-1]["sample"]},
+           "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(rec))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mha_decode", choices=W.CONFIG_NAMES)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    spec = W.spec(args.config)
+    if args.impl == "reference":
+        run_reference(args, spec, rank)
+        return
+
+    import torch
+    import paged_kv_attention_05_gb300 as pkv
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    step = W.build(spec)
+    s = spec
+    d = s.head_size
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    rows = step.qkv.shape[0]
+    qkv = dev(step.qkv)
+    q = qkv[:, :s.hq * d].view(rows, s.hq, d)
+    k = qkv[:, s.hq * d:(s.hq + s.hkv) * d].view(rows, s.hkv, d)
+    v = qkv[:, (s.hq + s.hkv) * d:].view(rows, s.hkv, d)
+    key_cache, value_cache = dev(step.key_cache), dev(step.value_cache)
+    slot_mapping = torch.from_numpy(step.slot_mapping).cuda()
+    qsl = torch.from_numpy(step.query_start_loc).cuda()
+    seq_lens = torch.from_numpy(step.seq_lens).cuda()
+    block_table = torch.from_numpy(step.block_table).cuda()
+    out = torch.empty((rows, s.hq, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    pkv.pkv_reserve_workspace(s.num_reqs, rows, step.block_table.shape[1], s.hq, s.hkv)
+
+    def one_step():
+        pkv.pkv_write(k, v, key_cache, value_cache, slot_mapping, stream=stream)
+        pkv.pkv_attention(q, key_cache, value_cache, qsl, seq_lens, block_table, s.num_reqs,
+                          s.scale, out, stream=stream)
+
+    for _ in range(max(args.warmup, 0)):
+        one_step()
+    torch.cuda.synchronize()
+    bits = pkv.pkv_get_error()
+    if bits:
+        raise SystemExit("device error word %d after warm-up" % bits)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    pkv.pkv_trace_read()
+    pkv.pkv_trace_enable(True)
+    launches0 = pkv.pkv_launch_count()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    barrier()
+    launches = pkv.pkv_launch_count() - launches0
+    pkv.pkv_trace_enable(False)
+    trace = pkv.pkv_trace_read()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    t_max = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms = float(t_max.item())
+    ms_per_step = ms / args.steps
+    name, unit = metric_of(spec)
+    work = metric_work(spec)
+    value = work * world / (ms_per_step / 1e3)
+
+    # end to end through the public API with host buffers: pinned host inputs
+    # copied in, the two calls, the output copied back, every step
+    e2e = None
+    if not args.no_e2e:
+        h_qkv = torch.from_numpy(step.qkv.view(np.int16)).pin_memory()
+        h_slots = torch.from_numpy(step.slot_mapping).pin_memory()
+        h_qsl = torch.from_numpy(step.query_start_loc).pin_memory()
+        h_sl = torch.from_numpy(step.seq_lens).pin_memory()
+        h_bt = torch.from_numpy(step.block_table).pin_memory()
+        h_out = torch.empty((rows, s.hq, d), dtype=torch.bfloat16).pin_memory()
+        d_qkv = qkv.view(torch.int16)
+        h2d = sum(t.numel() * t.element_size() for t in (h_qkv, h_slots, h_qsl, h_sl, h_bt))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            d_qkv.copy_(h_qkv, non_blocking=True)
+            slot_mapping.copy_(h_slots, non_blocking=True)
+            qsl.copy_(h_qsl, non_blocking=True)
+            seq_lens.copy_(h_sl, non_blocking=True)
+            block_table.copy_(h_bt, non_blocking=True)
+            one_step()
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        barrier()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        tt = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        if dist is not None:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e = {"value": work * world / float(tt.item()), "unit": unit,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": float(tt.item()) * 1e3}
+
+    # roofline of the dominant kernel, from its live CUDA-event durations
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    kinds = {k: v for k, v in trace.items() if v[1] > 0}
+    dominant = max(kinds, key=lambda k: kinds[k][0]) if kinds else "decode"
+    dom_ms, dom_n = trace.get(dominant, (0.0, 0))
+    avg_ms = dom_ms / max(dom_n, 1)
+    if dominant == "prefill":
+        algo = causal_flops(spec)
+        peak = peaks.get("bf16_tflops")
+        roof = {"bound": "tensor", "achieved": algo / (avg_ms / 1e3) / 1e12,
+                "peak": peak, "unit": "TFLOP/s", "peak_source": "measured" if peak else None}
+        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu"]
+    else:
+        algo = decode_algorithmic_bytes(spec) if dominant == "decode" else \
+            2 * s.num_tokens * s.hkv * d * 2 * 2
+        peak = peaks.get("hbm_gbs")
+        roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
+                "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
+        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % dominant,
+                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
+    if roof["peak"] is None:
+        roof["peak"] = 1900.0 if roof["unit"] == "TFLOP/s" else 6800.0
+        roof["peak_source"] = "fallback"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dominant
+    roof["avg_launch_ms"] = avg_ms
+    traffic = profiled_traffic(dominant, spec.name, srcs)
+    roof["traffic"] = traffic
+
+    rec = {"metric": name, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": spec.name, "requests": s.num_reqs, "query_tokens": s.num_tokens,
+                      "num_heads": s.hq, "num_kv_heads": s.hkv, "head_size": d,
+                      "block_size": s.block_size, "kv_bytes_per_step": s.kv_bytes(),
+                      "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB)" %
+                            (s.kv_bytes() / 1e9),
+                      "parallelism": "replica per GPU (dp%d)" % world},
+           "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
+           "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
+           "roofline": roof}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(step)
+    if rank == 0:
+        print(json.dumps(rec))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

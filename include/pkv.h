@@ -1,0 +1,188 @@
+/*
+ * pkv — the per-layer paged-KV attention step on NVIDIA GB300 (sm_103a).
+ *
+ * Two calls make one layer's step:
+ *   pkv_write      scatters the step's new K/V rows into the block-paged cache;
+ *   pkv_attention  runs causal varlen attention for a packed batch of prefill
+ *                  chunks and decodes over that cache.
+ * Call pkv_write before pkv_attention on the same stream: the step's own
+ * tokens must be in the cache when attention reads it.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device.
+ *   - bf16 tensors are passed as raw bit storage (2 bytes per element).
+ *   - Row strides are counted in elements, not bytes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on `stream` and returns; none
+ *     synchronises except pkv_get_error.
+ *   - The caller owns every buffer it passes; the library keeps no pointer to
+ *     any of them after the call returns.  The library owns one grow-only
+ *     device workspace per device (step plan, split-KV partial results and
+ *     the device error word).  It is allocated on first use, or beforehand by
+ *     pkv_reserve_workspace (needed before CUDA-graph capture, since no
+ *     allocation may happen while a stream is being captured).
+ *   - Errors found on the host (null pointers, sizes, geometry, alignment)
+ *     return a negative PKV_ERR_* code before anything is enqueued: no buffer
+ *     is touched.  pkv_last_error_string() describes the last such error of
+ *     the calling thread.
+ *   - Errors in the VALUES of device-resident metadata (a slot past the pool,
+ *     a block id outside the pool, seq_len < query_len, decreasing
+ *     query_start_loc, a block-table row too short) cannot be seen by the host
+ *     without a device-to-host copy.  The kernels skip the offending item,
+ *     never trap, and OR a PKV_DEV_ERR_* bit into a per-device error word that
+ *     pkv_get_error reads and clears.
+ *
+ * Geometry supported: head_size 128, block_size 16, num_heads a multiple of
+ * num_kv_heads (MHA: equal; GQA: num_kv_heads > 1; MQA: num_kv_heads = 1),
+ * num_heads / num_kv_heads <= 32.  Anything else returns PKV_ERR_UNSUPPORTED.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side status codes. */
+#define PKV_OK 0
+#define PKV_ERR_ARG (-1)         /* null pointer, negative size, bad stride   */
+#define PKV_ERR_UNSUPPORTED (-2) /* geometry outside the supported set        */
+#define PKV_ERR_ALIGN (-3)       /* pointer or row stride not 16-byte aligned */
+#define PKV_ERR_CUDA (-4)        /* a CUDA runtime call failed                */
+#define PKV_ERR_NO_DEVICE (-5)   /* no usable sm_103 device current           */
+
+/* Device error word bits (pkv_get_error). */
+#define PKV_DEV_ERR_SLOT_RANGE 1 /* pkv_write: slot >= num_blocks*block_size  */
+#define PKV_DEV_ERR_QSL 2        /* query_start_loc decreasing or > q_rows    */
+#define PKV_DEV_ERR_SEQ_LEN 4    /* seq_len < query_len (or negative)         */
+#define PKV_DEV_ERR_BT_WIDTH 8   /* ceil(seq_len/block_size) > row width      */
+#define PKV_DEV_ERR_BLOCK_ID 16  /* block id outside [0, num_blocks)          */
+#define PKV_DEV_ERR_TIMEOUT 32   /* an on-chip pipeline wait gave up          */
+
+/*
+ * pkv_write — the cache-write scatter.
+ *
+ * Defined by "vLLM 推理全流程深度解析" (vLLM inference deep dive),
+ * reshape_and_cache section, and "Tour: One forward pass", stop 4 (slot =
+ * block_number * block_size + offset; padding tokens at PAD_SLOT_ID = -1) and
+ * stop 10 (the separate cache-update op before attention).
+ *
+ * For t in [0, n_tokens): s = slot_mapping[t]; if s < 0 the token is padding
+ * and is skipped; otherwise the [num_kv_heads, head_size] rows k[t] and v[t]
+ * are copied bit for bit to key_cache[s / block_size][s % block_size] and
+ * value_cache[s / block_size][s % block_size].  No other cache byte changes.
+ *
+ *   k, v          bf16 [n_tokens, num_kv_heads, head_size]; token t starts at
+ *                 element t * k_row_stride (v_row_stride); each token's
+ *                 num_kv_heads * head_size elements are contiguous.  Strided
+ *                 rows let k and v be column slices of a fused qkv tensor.
+ *   key_cache,    bf16 [num_blocks, block_size, num_kv_heads, head_size],
+ *   value_cache   contiguous.  Written in place.
+ *   slot_mapping  int64 [n_tokens].  Non-negative slots within one call must
+ *                 be distinct (the result is otherwise unspecified).  A slot
+ *                 >= num_blocks * block_size is skipped and reported as
+ *                 PKV_DEV_ERR_SLOT_RANGE.
+ *   n_tokens      >= 0; 0 enqueues nothing.
+ * Alignment: k, v, both caches 16-byte aligned; row strides * 2 bytes a
+ * multiple of 16.
+ */
+int pkv_write(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+              void* key_cache, void* value_cache, int64_t num_blocks, int32_t block_size,
+              int32_t num_kv_heads, int32_t head_size, const int64_t* slot_mapping,
+              int64_t n_tokens, void* stream);
+
+/*
+ * pkv_attention — varlen causal attention over the paged cache for a packed
+ * batch that mixes prefill chunks and decodes.
+ *
+ * Defined by "Tour: One forward pass", stop 3 (query_start_loc, seq_lens =
+ * num_computed + query_len), stop 5 (the attention metadata) and stop 10
+ * (cu_seqlens_q = query_start_loc, seqused_k = seq_lens, block_table; causal;
+ * only the first query_start_loc[num_reqs] output rows are written); "vLLM
+ * MHA Code Path: From QKV to Paged KV Cache", sections "One Path Covers MHA,
+ * GQA, and MQA" and "Worked Trace: One Decode Token" (the current token
+ * attends to itself); "vLLM 推理全流程深度解析", paged_attention_v1 section
+ * (gather through block_tables, softmax, weighted sum of V).
+ *
+ * For request r: q0 = query_start_loc[r], n = query_start_loc[r+1] - q0,
+ * L = seq_lens[r], ctx = L - n.  Query row i (absolute position ctx + i) of
+ * head h reads KV head h / (num_heads / num_kv_heads) and keys 0 .. ctx + i,
+ * key j living at key_cache[block_table[r][j / 16]][j % 16]:
+ *   out[q0+i][h] = sum_j softmax_j(scale * q[q0+i][h] . K_j) * V_j,
+ * computed with bf16 inputs, fp32 accumulation and a bf16 result.
+ *
+ *   q               bf16 [q_rows, num_heads, head_size], row stride
+ *                   q_row_stride elements (>= num_heads * head_size).
+ *   key_cache,      bf16 [num_blocks, block_size, num_kv_heads, head_size],
+ *   value_cache     contiguous; read only.
+ *   query_start_loc int32 [num_reqs + 1], non-decreasing, last <= q_rows.
+ *   seq_lens        int32 [num_reqs].
+ *   block_table     int32 [num_reqs, block_table_width], rows contiguous.
+ *                   Entries past ceil(seq_len / 16) are never read.
+ *   num_reqs        >= 0.
+ *   scale           softmax scale (1/sqrt(head_size) for standard attention).
+ *   out             bf16 [q_rows, num_heads, head_size], row stride
+ *                   out_row_stride.  Rows >= query_start_loc[num_reqs], and
+ *                   rows of requests that fail a metadata check, are not
+ *                   written.  (A request with a block id outside the pool is
+ *                   reported as PKV_DEV_ERR_BLOCK_ID; its rows are then
+ *                   unspecified.)
+ * Alignment: q, out, caches 16-byte aligned; row strides * 2 bytes multiples
+ * of 16.
+ */
+int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
+                  const void* key_cache, const void* value_cache, int64_t num_blocks,
+                  int32_t block_size, int32_t num_kv_heads, int32_t head_size,
+                  const int32_t* query_start_loc, const int32_t* seq_lens,
+                  const int32_t* block_table, int64_t block_table_width, int32_t num_reqs,
+                  float scale, void* out, int64_t out_row_stride, void* stream);
+
+/*
+ * pkv_reserve_workspace — sizes the current device's workspace for
+ * pkv_attention calls with up to max_reqs requests, max_q_rows query rows,
+ * block-table rows of up to block_table_width entries and this head
+ * geometry, so that such calls allocate nothing (required before capturing
+ * them in a CUDA graph: no allocation may happen while a stream is being
+ * captured).  Also allocates the device error word.  Synchronous.  Returns
+ * PKV_OK or an error code.
+ */
+int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows, int64_t block_table_width,
+                          int32_t num_heads, int32_t num_kv_heads);
+
+/*
+ * pkv_get_error — synchronises `stream`, then returns the current device's
+ * error word (an OR of PKV_DEV_ERR_* bits accumulated since the last read)
+ * in *bits and clears it.  Returns PKV_OK or a host error code.
+ */
+int pkv_get_error(void* stream, int32_t* bits);
+
+/* Text of the calling thread's last host-side error ("" if none). */
+const char* pkv_last_error_string(void);
+
+/* Number of SMs the library sizes its persistent grids for (current device). */
+int pkv_num_sms(void);
+
+/*
+ * Tracing.  Not part of the step itself: a timing facility for benchmarks.
+ * While tracing is on, every kernel the library launches is bracketed by a
+ * pair of CUDA events recorded on the launch stream (do not capture traced
+ * calls in a CUDA graph).  pkv_trace_read waits for those events, adds each
+ * launch's duration to its kernel kind, copies up to n kinds of totals into
+ * ms[] and launches[] (either may be NULL), clears the record and returns the
+ * number of kinds (PKV_TRACE_KINDS).  Kinds: 0 cache write, 1 step plan,
+ * 2 decode attention, 3 prefill attention.
+ */
+#define PKV_TRACE_KINDS 4
+int pkv_trace_enable(int on);
+int pkv_trace_read(double* ms, int64_t* launches, int n);
+
+/* Total kernel launches issued by the library in this process. */
+int64_t pkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

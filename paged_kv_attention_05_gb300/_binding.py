@@ -1,0 +1,188 @@
+"""ctypes marshalling for libpkv.so (argument checks and pointers only)."""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "libpkv.so")
+_lib = None
+
+DEV_ERR_BITS = {
+    "SLOT_RANGE": 1,
+    "QSL": 2,
+    "SEQ_LEN": 4,
+    "BT_WIDTH": 8,
+    "BLOCK_ID": 16,
+    "TIMEOUT": 32,
+}
+
+EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
+           "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
+           "pkv_launch_count"]
+TRACE_KINDS = ["write", "plan", "decode", "prefill"]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("pkv error %d: %s" % (code, msg))
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Loads libpkv.so (built by ``build.py`` / ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise PkvError(-100, "libpkv.so is not built (%s); run __graft_entry__.build()" % _LIB_PATH)
+    L = ctypes.CDLL(_LIB_PATH)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    L.pkv_write.restype = ctypes.c_int
+    L.pkv_write.argtypes = [vp, i64, vp, i64, vp, vp, i64, i32, i32, i32, vp, i64, vp]
+    L.pkv_attention.restype = ctypes.c_int
+    L.pkv_attention.argtypes = [vp, i64, i64, i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64,
+                                i32, f32, vp, i64, vp]
+    L.pkv_reserve_workspace.restype = ctypes.c_int
+    L.pkv_reserve_workspace.argtypes = [i32, i64, i64, i32, i32]
+    L.pkv_get_error.restype = ctypes.c_int
+    L.pkv_get_error.argtypes = [vp, ctypes.POINTER(i32)]
+    L.pkv_last_error_string.restype = ctypes.c_char_p
+    L.pkv_last_error_string.argtypes = []
+    L.pkv_num_sms.restype = ctypes.c_int
+    L.pkv_num_sms.argtypes = []
+    L.pkv_trace_enable.restype = ctypes.c_int
+    L.pkv_trace_enable.argtypes = [ctypes.c_int]
+    L.pkv_trace_read.restype = ctypes.c_int
+    L.pkv_trace_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
+                                 ctypes.c_int]
+    L.pkv_launch_count.restype = i64
+    L.pkv_launch_count.argtypes = []
+    _lib = L
+    return L
+
+
+def _check(rc):
+    if rc != 0:
+        msg = load().pkv_last_error_string().decode(errors="replace")
+        raise PkvError(rc, msg)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _require(t, dtype, name, device=True):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if device and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def _rows3(t, name):
+    """Row stride of a [rows, heads, 128] tensor whose per-row block is contiguous."""
+    if t.dim() == 2:
+        if t.stride(1) != 1:
+            raise ValueError("%s: last dimension must be contiguous" % name)
+        return t.stride(0)
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("%s must be [rows, heads, head_size] with contiguous rows" % name)
+    return t.stride(0)
+
+
+def pkv_write(k, v, key_cache, value_cache, slot_mapping, n_tokens=None, stream=None):
+    """Scatters k/v ([n, Hkv, 128] bf16) into the caches at slot_mapping (int64)."""
+    import torch
+    for t, n in ((k, "k"), (v, "v"), (key_cache, "key_cache"), (value_cache, "value_cache")):
+        _require(t, torch.bfloat16, n)
+    _require(slot_mapping, torch.int64, "slot_mapping")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
+    if key_cache.shape != value_cache.shape:
+        raise ValueError("key_cache and value_cache shapes differ")
+    if not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous")
+    nb, bs, hkv, d = key_cache.shape
+    n = slot_mapping.shape[0] if n_tokens is None else int(n_tokens)
+    if n > slot_mapping.shape[0] or n > k.shape[0] or n > v.shape[0]:
+        raise ValueError("n_tokens exceeds the rows of k/v/slot_mapping")
+    _check(load().pkv_write(k.data_ptr(), _rows3(k, "k"), v.data_ptr(), _rows3(v, "v"),
+                            key_cache.data_ptr(), value_cache.data_ptr(), nb, bs, hkv, d,
+                            slot_mapping.data_ptr(), n, _stream(stream)))
+
+
+def pkv_attention(q, key_cache, value_cache, query_start_loc, seq_lens, block_table, num_reqs,
+                  scale, out, stream=None):
+    """Causal varlen attention of q ([T, Hq, 128] bf16) over the paged cache
+    into out ([T, Hq, 128] bf16); see include/pkv.h for the contract."""
+    import torch
+    for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"), (out, "out")):
+        _require(t, torch.bfloat16, n)
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_table, "block_table")):
+        _require(t, torch.int32, n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
+    if key_cache.shape != value_cache.shape:
+        raise ValueError("key_cache and value_cache shapes differ")
+    nb, bs, hkv, d = key_cache.shape
+    if q.dim() != 3:
+        raise ValueError("q must be [rows, num_heads, head_size]")
+    rows, hq, _ = q.shape
+    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+        raise ValueError("out must hold [rows, num_heads * head_size]")
+    bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
+    if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
+                              seq_lens.numel() < int(num_reqs) or
+                              (block_table.dim() == 2 and block_table.shape[0] < int(num_reqs))):
+        raise ValueError("metadata shorter than num_reqs")
+    _check(load().pkv_attention(q.data_ptr(), _rows3(q, "q"), rows, hq, key_cache.data_ptr(),
+                                value_cache.data_ptr(), nb, bs, hkv, d,
+                                query_start_loc.data_ptr(), seq_lens.data_ptr(),
+                                block_table.data_ptr(), bt_width, int(num_reqs), float(scale),
+                                out.data_ptr(), _rows3(out, "out"), _stream(stream)))
+
+
+def pkv_reserve_workspace(max_reqs, max_q_rows, block_table_width, num_heads, num_kv_heads):
+    _check(load().pkv_reserve_workspace(int(max_reqs), int(max_q_rows), int(block_table_width),
+                                        int(num_heads), int(num_kv_heads)))
+
+
+def pkv_get_error(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device error word."""
+    bits = ctypes.c_int32(0)
+    _check(load().pkv_get_error(_stream(stream), ctypes.byref(bits)))
+    return bits.value
+
+
+def pkv_num_sms() -> int:
+    return load().pkv_num_sms()
+
+
+def pkv_trace_enable(on: bool) -> None:
+    load().pkv_trace_enable(1 if on else 0)
+
+
+def pkv_trace_read():
+    """{kind: (total ms, launches)} of the traced launches since the last read."""
+    n = len(TRACE_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    rc = load().pkv_trace_read(ms, cnt, n)
+    if rc < 0:
+        _check(rc)
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(TRACE_KINDS)}
+
+
+def pkv_launch_count() -> int:
+    return load().pkv_launch_count()

@@ -1,0 +1,383 @@
+// Host side of the C ABI declared in include/pkv.h: argument checks, the
+// per-device workspace and error word, and the kernel launches.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;  // device error word
+  void* ws = nullptr;  // workspace
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+thread_local char g_msg[512] = "";
+
+// Tracing (guarded by g_mu): event pairs around each launch while enabled.
+struct TraceRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_ev_pool;
+int64_t g_launches = 0;
+
+cudaEvent_t take_event() {
+  if (!g_ev_pool.empty()) {
+    cudaEvent_t e = g_ev_pool.back();
+    g_ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+template <class F>
+cudaError_t traced(int kind, cudaStream_t st, F&& launch) {
+  ++g_launches;
+  if (!g_trace_on) return launch();
+  TraceRec r{kind, take_event(), take_event()};
+  cudaEventRecord(r.a, st);
+  cudaError_t e = launch();
+  cudaEventRecord(r.b, st);
+  g_trace.push_back(r);
+  return e;
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Device state of the current device, initialised on first use.
+int current_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_NO_DEVICE, "device %d out of range", dev);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(PKV_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, prop.major, prop.minor);
+    s.sms = prop.multiProcessorCount;
+    e = cudaMalloc(&s.err, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+    e = cudaMemset(s.err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    s.ready = true;
+  }
+  *out = &s;
+  return PKV_OK;
+}
+
+struct Sizes {
+  int64_t units, pre, pairs;
+  int group;
+};
+
+Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv) {
+  Sizes z;
+  const int64_t max_keys = bt_width * kBlockSize;
+  const int64_t splits = (max_keys + kMinChunk - 1) / kMinChunk;
+  z.units = reqs * hkv * (splits < 1 ? 1 : splits);
+  z.pre = (q_rows + kPreTileQ - 1) / kPreTileQ + reqs;
+  z.pairs = reqs * hkv;
+  z.group = hq / hkv;
+  return z;
+}
+
+// Makes sure the workspace holds at least `z`; allocation only outside capture.
+int ensure_workspace(DeviceState* s, const Sizes& z, cudaStream_t st, Workspace* ws) {
+  const size_t need = workspace_bytes(z.units, z.pre, z.pairs, z.group);
+  if (need > s->ws_bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (st != nullptr) cudaStreamIsCapturing(st, &cap);
+    if (cap != cudaStreamCaptureStatusNone)
+      return fail(PKV_ERR_ARG,
+                  "workspace of %zu bytes needed while the stream is being captured; call "
+                  "pkv_reserve_workspace before capture",
+                  need);
+    cudaError_t e = cudaDeviceSynchronize();  // the old workspace may still be in use
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if (s->ws) cudaFree(s->ws);
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+    const size_t grow = need + need / 4;
+    e = cudaMalloc(&s->ws, grow);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemset(s->ws, 0, grow);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+    s->ws_bytes = grow;
+  }
+  // carve for the capacity actually held, scaled from the request
+  *ws = carve_workspace(s->ws, z.units, z.pre, z.pairs, z.group, s->err);
+  return PKV_OK;
+}
+
+int check_geometry(int32_t block_size, int32_t hkv, int32_t head_size) {
+  if (block_size != kBlockSize)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (only %d)", block_size, kBlockSize);
+  if (head_size != kHeadSize)
+    return fail(PKV_ERR_UNSUPPORTED, "head_size %d (only %d)", head_size, kHeadSize);
+  if (hkv <= 0) return fail(PKV_ERR_ARG, "num_kv_heads %d", hkv);
+  return PKV_OK;
+}
+
+}  // namespace
+
+size_t workspace_bytes(int64_t max_units, int64_t max_pre, int64_t max_pairs, int group) {
+  size_t b = 256;                                      // header
+  b += (size_t)max_units * sizeof(DecUnit);
+  b += (size_t)max_pre * sizeof(PreEntry);
+  b += (size_t)max_pairs * sizeof(int);
+  b = (b + 255) & ~(size_t)255;
+  b += (size_t)max_units * group * 2 * sizeof(float);  // part_ml
+  b = (b + 255) & ~(size_t)255;
+  b += (size_t)max_units * group * kHeadSize * sizeof(float);  // part_o
+  return b + 256;
+}
+
+Workspace carve_workspace(void* base, int64_t max_units, int64_t max_pre, int64_t max_pairs,
+                          int group, int* err) {
+  Workspace w;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  w.hdr = reinterpret_cast<PlanHeader*>(p);
+  off += 256;
+  w.units = reinterpret_cast<DecUnit*>(p + off);
+  off += (size_t)max_units * sizeof(DecUnit);
+  w.pre = reinterpret_cast<PreEntry*>(p + off);
+  off += (size_t)max_pre * sizeof(PreEntry);
+  w.counters = reinterpret_cast<int*>(p + off);
+  off += (size_t)max_pairs * sizeof(int);
+  off = (off + 255) & ~(size_t)255;
+  w.part_ml = reinterpret_cast<float*>(p + off);
+  off += (size_t)max_units * group * 2 * sizeof(float);
+  off = (off + 255) & ~(size_t)255;
+  w.part_o = reinterpret_cast<float*>(p + off);
+  w.err = err;
+  w.max_units = max_units;
+  w.max_pre = max_pre;
+  w.max_pairs = max_pairs;
+  return w;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_write(const void* k, int64_t k_row_stride, const void* v,
+                         int64_t v_row_stride, void* key_cache, void* value_cache,
+                         int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_size, const int64_t* slot_mapping, int64_t n_tokens,
+                         void* stream) {
+  g_msg[0] = 0;
+  int rc = check_geometry(block_size, num_kv_heads, head_size);
+  if (rc) return rc;
+  if (n_tokens < 0) return fail(PKV_ERR_ARG, "n_tokens %lld < 0", (long long)n_tokens);
+  if (num_blocks < 1) return fail(PKV_ERR_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (n_tokens == 0) return PKV_OK;
+  if (!k || !v || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_ERR_ARG, "null pointer argument");
+  const int64_t row = (int64_t)num_kv_heads * kHeadSize;
+  if (k_row_stride < row || v_row_stride < row)
+    return fail(PKV_ERR_ARG, "row stride below num_kv_heads * head_size (%lld)", (long long)row);
+  if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      (k_row_stride % 8) || (v_row_stride % 8))
+    return fail(PKV_ERR_ALIGN, "k/v/caches must be 16-byte aligned with row strides * 2 a "
+                               "multiple of 16 bytes");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(0, st, [&] {
+    return launch_write(static_cast<const uint16_t*>(k), k_row_stride,
+                        static_cast<const uint16_t*>(v), v_row_stride,
+                        static_cast<uint16_t*>(key_cache), static_cast<uint16_t*>(value_cache),
+                        num_blocks, num_kv_heads, slot_mapping, n_tokens, s->err, s->sms, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_write launch");
+  return PKV_OK;
+}
+
+extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows,
+                             int32_t num_heads, const void* key_cache, const void* value_cache,
+                             int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_size, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, const int32_t* block_table,
+                             int64_t block_table_width, int32_t num_reqs, float scale, void* out,
+                             int64_t out_row_stride, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_geometry(block_size, num_kv_heads, head_size);
+  if (rc) return rc;
+  if (num_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_UNSUPPORTED, "num_heads %d is not a multiple of num_kv_heads %d",
+                num_heads, num_kv_heads);
+  if (num_heads / num_kv_heads > kMaxGroup)
+    return fail(PKV_ERR_UNSUPPORTED, "num_heads / num_kv_heads = %d > %d",
+                num_heads / num_kv_heads, kMaxGroup);
+  if (num_reqs < 0 || q_rows < 0 || block_table_width < 0)
+    return fail(PKV_ERR_ARG, "negative size");
+  if (num_blocks < 1) return fail(PKV_ERR_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (num_reqs == 0 || q_rows == 0) return PKV_OK;
+  if (!q || !key_cache || !value_cache || !query_start_loc || !seq_lens || !block_table || !out)
+    return fail(PKV_ERR_ARG, "null pointer argument");
+  if (block_table_width < 1) return fail(PKV_ERR_ARG, "block_table_width < 1");
+  const int64_t row = (int64_t)num_heads * kHeadSize;
+  if (q_row_stride < row || out_row_stride < row)
+    return fail(PKV_ERR_ARG, "q/out row stride below num_heads * head_size (%lld)",
+                (long long)row);
+  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      (q_row_stride % 8) || (out_row_stride % 8))
+    return fail(PKV_ERR_ALIGN, "q/out/caches must be 16-byte aligned with row strides * 2 a "
+                               "multiple of 16 bytes");
+  if (!(scale == scale)) return fail(PKV_ERR_ARG, "scale is NaN");
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Workspace ws;
+  rc = ensure_workspace(s, sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads),
+                        st, &ws);
+  if (rc) return rc;
+
+  AttnArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_stride = q_row_stride;
+  a.q_rows = q_rows;
+  a.hq = num_heads;
+  a.kc = static_cast<const uint16_t*>(key_cache);
+  a.vc = static_cast<const uint16_t*>(value_cache);
+  a.num_blocks = num_blocks;
+  a.hkv = num_kv_heads;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.bt = block_table;
+  a.bt_width = block_table_width;
+  a.num_reqs = num_reqs;
+  a.scale = scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_stride = out_row_stride;
+
+  const int dec_grid = s->sms * decode_ctas_per_sm(num_heads / num_kv_heads);
+  cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, dec_grid, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  e = traced(2, st, [&] { return launch_decode(a, ws, dec_grid, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PKV_OK;
+}
+
+extern "C" int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows,
+                                     int64_t block_table_width, int32_t num_heads,
+                                     int32_t num_kv_heads) {
+  g_msg[0] = 0;
+  if (max_reqs < 0 || max_q_rows < 0 || block_table_width < 0 || num_kv_heads <= 0 ||
+      num_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_ARG, "bad sizes");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc) return rc;
+  Workspace ws;
+  return ensure_workspace(s, sizes_for(max_reqs, max_q_rows, block_table_width, num_heads,
+                                       num_kv_heads),
+                          nullptr, &ws);
+}
+
+extern "C" int pkv_get_error(void* stream, int32_t* bits) {
+  g_msg[0] = 0;
+  if (!bits) return fail(PKV_ERR_ARG, "bits is null");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, s->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  e = cudaMemset(s->err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  *bits = v;
+  return PKV_OK;
+}
+
+extern "C" const char* pkv_last_error_string(void) { return g_msg; }
+
+extern "C" int pkv_num_sms(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  if (current_state(&s)) return -1;
+  return s->sms;
+}
+
+extern "C" int pkv_trace_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_trace_on = on != 0;
+  return PKV_OK;
+}
+
+extern "C" int pkv_trace_read(double* ms, int64_t* launches, int n) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  double tot[PKV_TRACE_KINDS] = {0, 0, 0, 0};
+  int64_t cnt[PKV_TRACE_KINDS] = {0, 0, 0, 0};
+  int rc = PKV_OK;
+  for (const TraceRec& r : g_trace) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+    if (e != cudaSuccess) rc = cuda_fail(e, "trace event");
+    if (r.kind >= 0 && r.kind < PKV_TRACE_KINDS) {
+      tot[r.kind] += t;
+      cnt[r.kind] += 1;
+    }
+    g_ev_pool.push_back(r.a);
+    g_ev_pool.push_back(r.b);
+  }
+  g_trace.clear();
+  for (int i = 0; i < n && i < PKV_TRACE_KINDS; ++i) {
+    if (ms) ms[i] = tot[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return rc == PKV_OK ? PKV_TRACE_KINDS : rc;
+}
+
+extern "C" int64_t pkv_launch_count(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_launches;
+}

@@ -1,0 +1,92 @@
+// Internal declarations shared by the CUDA translation units of libpkv.
+// Not part of the public C ABI (include/pkv.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kHeadSize = 128;   // elements per head row
+constexpr int kBlockSize = 16;   // tokens per cache block (page)
+constexpr int kMaxGroup = 32;    // query heads per KV head handled by one decode unit
+constexpr int kDecTile = 64;     // tokens per decode pipeline stage (4 pages)
+constexpr int kDecStages = 3;    // decode cp.async pipeline depth
+constexpr int kDecThreads = 128; // 4 warps, one page of each stage per warp
+constexpr int kMinChunk = 256;   // smallest split-KV chunk (tokens)
+constexpr int kMaxChunk = 1024;  // largest split-KV chunk (tokens)
+constexpr int kPreTileQ = 128;   // query rows per prefill tile
+
+// One decode work unit: request r, KV head g, keys [k0, k1) of the request.
+struct DecUnit {
+  int r, g, split, nsplit, k0, k1, part, pad;
+};
+
+// One prefill work entry: request r, 128-row query tile qt; nkv = number of
+// 128-key tiles it reads (work estimate used for longest-first ordering).
+struct PreEntry {
+  int r, qt, nkv, pad;
+};
+
+// Header of the step plan, written by the plan kernel each call.
+struct PlanHeader {
+  int n_dec_units;
+  int n_pre_entries;
+  int dec_counter;  // dynamic scheduler cursors, reset by the plan kernel
+  int pre_counter;
+  int chunk;
+  int pad[11];
+};
+
+// Device pointers into the per-device workspace.
+struct Workspace {
+  PlanHeader* hdr;
+  DecUnit* units;
+  PreEntry* pre;
+  int* counters;     // [max_reqs * hkv] split-arrival tickets
+  float* part_ml;    // [part_slots * group][2]: running max (log2 domain) and sum
+  float* part_o;     // [part_slots * group][128]: unnormalised output
+  int* err;          // device error word
+  int64_t max_units;
+  int64_t max_pre;
+  int64_t max_pairs;
+};
+
+// Bytes needed for a workspace serving up to these sizes.
+size_t workspace_bytes(int64_t max_units, int64_t max_pre, int64_t max_pairs, int group);
+Workspace carve_workspace(void* base, int64_t max_units, int64_t max_pre, int64_t max_pairs,
+                          int group, int* err);
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,
+                         uint16_t* kc, uint16_t* vc, int64_t num_blocks, int hkv,
+                         const int64_t* slots, int64_t n_tokens, int* err, int sms,
+                         cudaStream_t st);
+
+struct AttnArgs {
+  const uint16_t* q;
+  int64_t q_stride;
+  int64_t q_rows;
+  int hq;
+  const uint16_t* kc;
+  const uint16_t* vc;
+  int64_t num_blocks;
+  int hkv;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* bt;
+  int64_t bt_width;
+  int num_reqs;
+  float scale;
+  uint16_t* out;
+  int64_t out_stride;
+};
+
+cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st);
+cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int grid, cudaStream_t st);
+int decode_ctas_per_sm(int group);
+cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
+
+}  // namespace pkv

@@ -1,0 +1,182 @@
+// Step plan: turns the device-resident batch metadata into work lists.
+//
+// "Tour: One forward pass", stop 5: the attention metadata carries
+// query_start_loc, seq_lens and the block table; its max_query_len /
+// max_seq_len come from CPU mirrors.  Here the host never reads the device
+// metadata (no device-to-host copy, so a step can be captured in a CUDA
+// graph): one small kernel reads query_start_loc and seq_lens on the device,
+// checks them, and writes
+//   * decode units (request, KV head, key range) for requests with one query
+//     token, split along the keys so that the persistent decode grid has
+//     several units per CTA (split-KV; the split results are merged by the
+//     last unit of each (request, KV head) to finish);
+//   * prefill entries (request, 128-row query tile) for requests with more
+//     than one query token, ordered longest first;
+//   * a header with the counts, the split size and zeroed scheduler cursors.
+// "vLLM MHA Code Path: From QKV to Paged KV Cache", section "Prefill and
+// decode share an interface": the phase of a request is told apart only by
+// its query and sequence lengths, which is what this kernel does.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive block-wide prefix sum of one int per thread (1024 threads).
+__device__ int block_exclusive_scan(int x, int* total, int* smem32) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) smem32[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = smem32[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    smem32[lane] = wi - w;  // exclusive warp offsets
+    if (lane == 31) smem32[32] = wi;
+  }
+  __syncthreads();
+  const int res = smem32[warp] + incl - x;
+  *total = smem32[32];
+  __syncthreads();
+  return res;
+}
+
+struct ReqInfo {
+  int kind;  // 0 nothing, 1 decode, 2 prefill
+  int n, L, q0;
+  int bad;   // PKV_DEV_ERR_* bits of a request that fails a check
+};
+
+__device__ ReqInfo classify(const AttnArgs& a, int r) {
+  ReqInfo ri{0, 0, 0, 0, 0};
+  const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
+  int bad = 0;
+  if (q0 < 0 || q1 < q0 || (int64_t)q1 > a.q_rows)
+    bad = PKV_DEV_ERR_QSL;
+  else if (L < 0 || L < q1 - q0)
+    bad = PKV_DEV_ERR_SEQ_LEN;
+  else if (((int64_t)L + kBlockSize - 1) / kBlockSize > a.bt_width)
+    bad = PKV_DEV_ERR_BT_WIDTH;
+  if (bad) {
+    ri.bad = bad;
+    return ri;
+  }
+  ri.n = q1 - q0;
+  ri.L = L;
+  ri.q0 = q0;
+  ri.kind = ri.n == 1 ? 1 : (ri.n > 1 ? 2 : 0);
+  return ri;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspace ws,
+                                                            int dec_grid) {
+  __shared__ int smem32[33];
+  __shared__ long long red[32];
+  const int tid = threadIdx.x;
+
+  // pass 1: total decode keys, to size the split-KV chunk
+  long long dec_keys = 0;
+  for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
+    ReqInfo ri = classify(a, r);
+    if (ri.kind == 1) dec_keys += ri.L;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
+  if ((tid & 31) == 0) red[tid >> 5] = dec_keys;
+  __syncthreads();
+  if (tid < 32) {
+    long long x = red[tid];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (tid == 0) red[0] = x;
+  }
+  __syncthreads();
+  const long long total_keys = red[0];
+  // aim for about four units per decode CTA, in whole 64-key tiles
+  long long want = (total_keys * a.hkv + (long long)dec_grid * 4 - 1) / ((long long)dec_grid * 4);
+  want = (want + kDecTile - 1) / kDecTile * kDecTile;
+  const int chunk = (int)(want < kMinChunk ? kMinChunk : (want > kMaxChunk ? kMaxChunk : want));
+
+  // pass 2: offsets and work lists
+  int unit_carry = 0, part_carry = 0, pre_carry = 0;
+  for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
+    const int r = base + tid;
+    ReqInfo ri{0, 0, 0, 0, 0};
+    if (r < a.num_reqs) ri = classify(a, r);
+    if (ri.bad) atomicOr(ws.err, ri.bad);
+    int nsplit = 0, units = 0, parts = 0, tiles = 0;
+    if (ri.kind == 1) {
+      nsplit = (ri.L + chunk - 1) / chunk;
+      units = nsplit * a.hkv;
+      parts = nsplit > 1 ? units : 0;
+    } else if (ri.kind == 2) {
+      tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
+    }
+    int tot_u, tot_p, tot_t;
+    const int off_u = unit_carry + block_exclusive_scan(units, &tot_u, smem32);
+    const int off_p = part_carry + block_exclusive_scan(parts, &tot_p, smem32);
+    const int off_t = pre_carry + block_exclusive_scan(tiles, &tot_t, smem32);
+    if (ri.kind == 1) {
+      for (int g = 0; g < a.hkv; ++g) ws.counters[(int64_t)r * a.hkv + g] = 0;
+      for (int s = 0; s < nsplit; ++s) {
+        for (int g = 0; g < a.hkv; ++g) {
+          const int64_t idx = off_u + (int64_t)s * a.hkv + g;
+          if (idx >= ws.max_units) continue;
+          DecUnit u;
+          u.r = r;
+          u.g = g;
+          u.split = s;
+          u.nsplit = nsplit;
+          u.k0 = s * chunk;
+          u.k1 = min(ri.L, (s + 1) * chunk);
+          u.part = nsplit > 1 ? off_p + g * nsplit + s : -1;
+          u.pad = 0;
+          ws.units[idx] = u;
+        }
+      }
+    } else if (ri.kind == 2) {
+      const int ctx = ri.L - ri.n;
+      for (int t = 0; t < tiles; ++t) {
+        const int64_t idx = off_t + t;
+        if (idx >= ws.max_pre) continue;
+        const int last_row = min(kPreTileQ * (t + 1), ri.n);
+        PreEntry e;
+        e.r = r;
+        e.qt = t;
+        e.nkv = (ctx + last_row + kPreTileQ - 1) / kPreTileQ;
+        e.pad = 0;
+        ws.pre[idx] = e;
+      }
+    }
+    unit_carry += tot_u;
+    part_carry += tot_p;
+    pre_carry += tot_t;
+  }
+  if (tid == 0) {
+    ws.hdr->n_dec_units = (int)min((int64_t)unit_carry, ws.max_units);
+    ws.hdr->n_pre_entries = (int)min((int64_t)pre_carry, ws.max_pre);
+    ws.hdr->dec_counter = 0;
+    ws.hdr->pre_counter = 0;
+    ws.hdr->chunk = chunk;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st) {
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(a, ws, dec_grid);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,69 @@
+// Cache-write scatter: the step's new K/V rows into the block-paged cache.
+//
+// "vLLM 推理全流程深度解析" (vLLM inference deep dive), reshape_and_cache
+// section: a negative slot is skipped; otherwise block = slot / block_size,
+// offset = slot % block_size and the token's [num_kv_heads, head_size] rows
+// land at cache[block][offset].  "Tour: One forward pass", stop 4: padding
+// rows carry PAD_SLOT_ID = -1.
+//
+// GB300 layout of the work: the copy is pure HBM traffic (read 2 rows, write
+// 2 rows per token), so each thread moves 16-byte vectors and consecutive
+// threads move consecutive 16-byte pieces of one token's contiguous
+// [num_kv_heads * 128] row: every warp issues fully coalesced 512-byte
+// transactions on both sides.  The grid is a multiple of the SM count and
+// strides over (token, K/V, 16-byte piece).
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+__global__ void __launch_bounds__(256) write_kernel(const uint16_t* __restrict__ k,
+                                                    int64_t k_stride,
+                                                    const uint16_t* __restrict__ v,
+                                                    int64_t v_stride, uint16_t* __restrict__ kc,
+                                                    uint16_t* __restrict__ vc, int64_t num_slots,
+                                                    int row_vecs, const int64_t* __restrict__ slots,
+                                                    int64_t n_tokens, int* err) {
+  // row_vecs = 16-byte vectors per token row = num_kv_heads * 128 * 2 / 16
+  const int64_t per_token = 2 * (int64_t)row_vecs;
+  const int64_t total = n_tokens * per_token;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const bool is_v = rem >= row_vecs;
+    const int vec = is_v ? rem - row_vecs : rem;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (rem == 0) atomicOr(err, PKV_DEV_ERR_SLOT_RANGE);
+      continue;
+    }
+    // cache row of this slot: [block][offset] == slot * row (contiguous pool)
+    const uint16_t* src = (is_v ? v + t * v_stride : k + t * k_stride) + (int64_t)vec * 8;
+    uint16_t* dst = (is_v ? vc : kc) + slot * (int64_t)row_vecs * 8 + (int64_t)vec * 8;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
+    *reinterpret_cast<uint4*>(dst) = val;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,
+                         uint16_t* kc, uint16_t* vc, int64_t num_blocks, int hkv,
+                         const int64_t* slots, int64_t n_tokens, int* err, int sms,
+                         cudaStream_t st) {
+  const int row_vecs = hkv * kHeadSize * 2 / 16;
+  const int64_t total = n_tokens * 2 * (int64_t)row_vecs;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread CTAs per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  write_kernel<<<(unsigned)blocks, threads, 0, st>>>(k, k_stride, v, v_stride, kc, vc,
+                                                     num_blocks * kBlockSize, row_vecs, slots,
+                                                     n_tokens, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,71 @@
+"""Decode attention (one query token per request) on the GPU against the
+float64 oracle: small batches spanning several tiles, splits and ragged
+tails for every head grouping; the full-size decode workloads; invariances."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_05_gb300 as pkv
+from paged_kv_attention_05_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import DeviceStep, assert_close  # noqa: E402
+
+
+def run_and_check(step, what):
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    ref, err = oracle.attention(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                step.block_table, step.num_reqs, step.scale)
+    assert err == 0
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()
+    assert pkv.pkv_get_error() == 0
+    got = ds.out_f64()
+    n = int(step.query_start_loc[-1])
+    assert_close(got[:n], ref[:n], what)
+    assert np.isnan(got[n:]).all(), "rows past the last request must not be written"
+    return ds, got
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (8, 1), (16, 1), (32, 1), (32, 8), (12, 4)])
+def test_decode_small_batches(hq, hkv):
+    ctx = [0, 1, 15, 16, 63, 64, 65, 200, 1023, 1500, 2100]
+    step = W.build(W.custom(ctx, [1] * len(ctx), hq, hkv, seed=hq * 100 + hkv))
+    run_and_check(step, "decode hq=%d hkv=%d" % (hq, hkv))
+
+
+def test_decode_long_requests_split_and_merge():
+    ctx = [5000, 9000, 3, 4097]
+    step = W.build(W.custom(ctx, [1] * 4, 32, 8, seed=77))
+    run_and_check(step, "split decode")
+
+
+def test_decode_bit_identical_under_block_permutation():
+    ctx = [700, 1800, 33]
+    outs = []
+    for seed in (1, 2):
+        spec = W.custom(ctx, [1, 1, 1], 16, 4, seed=90)
+        step = W.build(spec)
+        # same values, different physical placement: permute the pool
+        rng = np.random.default_rng(seed)
+        perm = rng.permutation(step.key_cache.shape[0]).astype(np.int32)
+        inv = np.argsort(perm).astype(np.int32)
+        step.key_cache = step.key_cache[inv]
+        step.value_cache = step.value_cache[inv]
+        bt = step.block_table
+        step.block_table = np.where(bt >= 0, perm[np.clip(bt, 0, None)], -1).astype(np.int32)
+        sm = step.slot_mapping
+        step.slot_mapping = np.where(sm >= 0, perm[sm // 16].astype(np.int64) * 16 + sm % 16, -1)
+        ds, got = run_and_check(step, "permuted %d" % seed)
+        outs.append(ds.out.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("name", ["mha_decode", "gqa_decode", "mqa_long_decode"])
+def test_decode_full_size(name):
+    step = W.build(W.spec(name))
+    run_and_check(step, name)
