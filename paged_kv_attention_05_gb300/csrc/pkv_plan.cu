@@ -108,60 +108,90 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   want = (want + kDecTile - 1) / kDecTile * kDecTile;
   const int chunk = (int)(want < kMinChunk ? kMinChunk : (want > kMaxChunk ? kMaxChunk : want));
 
-  // pass 2: offsets and work lists
+  // pass 2: per-request offsets (block scans), then the work lists written
+  // cooperatively: consecutive threads write consecutive entries, each
+  // finding its request by binary search over the chunk's offsets
+  __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1];
+  __shared__ int s_off_p[kPlanThreads], s_len[kPlanThreads], s_n[kPlanThreads];
   int unit_carry = 0, part_carry = 0, pre_carry = 0;
   for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
     if (r < a.num_reqs) ri = classify(a, r);
     if (ri.bad) atomicOr(ws.err, ri.bad);
-    int nsplit = 0, units = 0, parts = 0, tiles = 0;
+    int units = 0, parts = 0, tiles = 0;
     if (ri.kind == 1) {
-      nsplit = (ri.L + chunk - 1) / chunk;
+      const int nsplit = (ri.L + chunk - 1) / chunk;
       units = nsplit * a.hkv;
       parts = nsplit > 1 ? units : 0;
     } else if (ri.kind == 2) {
       tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
     }
     int tot_u, tot_p, tot_t;
-    const int off_u = unit_carry + block_exclusive_scan(units, &tot_u, smem32);
-    const int off_p = part_carry + block_exclusive_scan(parts, &tot_p, smem32);
-    const int off_t = pre_carry + block_exclusive_scan(tiles, &tot_t, smem32);
-    if (ri.kind == 1) {
-      for (int g = 0; g < a.hkv; ++g) ws.counters[(int64_t)r * a.hkv + g] = 0;
-      for (int s = 0; s < nsplit; ++s) {
-        for (int g = 0; g < a.hkv; ++g) {
-          const int64_t idx = off_u + (int64_t)s * a.hkv + g;
-          if (idx >= ws.max_units) continue;
-          DecUnit u;
-          u.r = r;
-          u.g = g;
-          u.split = s;
-          u.nsplit = nsplit;
-          u.k0 = s * chunk;
-          u.k1 = min(ri.L, (s + 1) * chunk);
-          u.part = nsplit > 1 ? off_p + g * nsplit + s : -1;
-          u.pad = 0;
-          ws.units[idx] = u;
-        }
+    const int off_u = block_exclusive_scan(units, &tot_u, smem32);
+    const int off_p = block_exclusive_scan(parts, &tot_p, smem32);
+    const int off_t = block_exclusive_scan(tiles, &tot_t, smem32);
+    s_off_u[tid] = off_u;
+    s_off_t[tid] = off_t;
+    s_off_p[tid] = part_carry + off_p;
+    s_len[tid] = ri.L;
+    s_n[tid] = ri.n;
+    if (tid == 0) {
+      s_off_u[kPlanThreads] = tot_u;
+      s_off_t[kPlanThreads] = tot_t;
+    }
+    __syncthreads();
+    const int nreq = min(kPlanThreads, a.num_reqs - base);
+    // split tickets start at zero (every request of the chunk, every KV head)
+    for (int i = tid; i < nreq * a.hkv; i += kPlanThreads)
+      ws.counters[(int64_t)base * a.hkv + i] = 0;
+    for (int i = tid; i < tot_u; i += kPlanThreads) {
+      int lo = 0, hi = kPlanThreads - 1;  // last request with s_off_u <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off_u[mid] <= i) lo = mid; else hi = mid - 1;
       }
-    } else if (ri.kind == 2) {
-      const int ctx = ri.L - ri.n;
-      for (int t = 0; t < tiles; ++t) {
-        const int64_t idx = off_t + t;
-        if (idx >= ws.max_pre) continue;
-        const int last_row = min(kPreTileQ * (t + 1), ri.n);
-        PreEntry e;
-        e.r = r;
-        e.qt = t;
-        e.nkv = (ctx + last_row + kPreTileQ - 1) / kPreTileQ;
-        e.pad = 0;
-        ws.pre[idx] = e;
+      const int rem = i - s_off_u[lo];
+      const int L = s_len[lo];
+      const int nsplit = (L + chunk - 1) / chunk;
+      const int sp = rem / a.hkv, g = rem - sp * a.hkv;
+      const int64_t idx = (int64_t)unit_carry + i;
+      if (idx >= ws.max_units) break;
+      DecUnit u;
+      u.r = base + lo;
+      u.g = g;
+      u.split = sp;
+      u.nsplit = nsplit;
+      u.k0 = sp * chunk;
+      u.k1 = min(L, (sp + 1) * chunk);
+      u.part = nsplit > 1 ? s_off_p[lo] + g * nsplit + sp : -1;
+      u.pad = 0;
+      ws.units[idx] = u;
+    }
+    for (int i = tid; i < tot_t; i += kPlanThreads) {
+      int lo = 0, hi = kPlanThreads - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off_t[mid] <= i) lo = mid; else hi = mid - 1;
       }
+      // a request's query tiles from the last (most keys) to the first, so
+      // that the persistent prefill grid starts with the longest items
+      const int n = s_n[lo], ctx = s_len[lo] - n;
+      const int t = (n + kPreTileQ - 1) / kPreTileQ - 1 - (i - s_off_t[lo]);
+      const int64_t idx = (int64_t)pre_carry + i;
+      if (idx >= ws.max_pre) break;
+      const int last_row = min(kPreTileQ * (t + 1), n);
+      PreEntry e;
+      e.r = base + lo;
+      e.qt = t;
+      e.nkv = (ctx + last_row + kPreTileQ - 1) / kPreTileQ;
+      e.pad = 0;
+      ws.pre[idx] = e;
     }
     unit_carry += tot_u;
     part_carry += tot_p;
     pre_carry += tot_t;
+    __syncthreads();  // the chunk's offsets are reused by the next chunk
   }
   if (tid == 0) {
     ws.hdr->n_dec_units = (int)min((int64_t)unit_carry, ws.max_units);

@@ -1,0 +1,131 @@
+"""Prefill and chunked-prefill attention (query_len > 1) and mixed batches on
+the GPU against the float64 oracle: ragged query tiles, chunks continuing a
+cached prompt, every head grouping, the trace step, the mixed 512-token batch
+and the large prefill (sampled rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_05_gb300 as pkv
+from paged_kv_attention_05_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import DeviceStep, assert_close  # noqa: E402
+
+
+def run_and_check(step, what):
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    ref, err = oracle.attention(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                step.block_table, step.num_reqs, step.scale)
+    assert err == 0
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()
+    assert pkv.pkv_get_error() == 0
+    got = ds.out_f64()
+    n = int(step.query_start_loc[-1])
+    assert_close(got[:n], ref[:n], what)
+    assert np.isnan(got[n:]).all(), "rows past the last request must not be written"
+    return ds, got
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 1), (8, 2), (6, 3)])
+def test_prefill_single_tile_and_ragged(hq, hkv):
+    step = W.build(W.custom([0, 0, 0], [2, 17, 128], hq, hkv, seed=hq * 31 + hkv))
+    run_and_check(step, "prefill hq=%d hkv=%d" % (hq, hkv))
+
+
+def test_prefill_many_query_and_key_tiles():
+    step = W.build(W.custom([0, 0], [300, 513], 4, 2, seed=12))
+    run_and_check(step, "multi-tile prefill")
+
+
+@pytest.mark.parametrize("ctx,n", [(1, 5), (15, 2), (16, 16), (100, 129), (1024, 224), (250, 7)])
+def test_chunk_continuing_a_cached_prompt(ctx, n):
+    step = W.build(W.custom([ctx, 3], [n, 40], 8, 2, seed=ctx + n))
+    run_and_check(step, "chunk ctx=%d n=%d" % (ctx, n))
+
+
+def test_trace_step_mixed():
+    ds, got = run_and_check(W.build(W.spec("tiny_mixed")), "tiny_mixed")
+
+
+def test_mixed_chunked_512_tokens():
+    run_and_check(W.build(W.spec("mixed_chunked")), "mixed_chunked")
+
+
+def test_mixed_decode_and_prefill_interleaved():
+    ctx = [0, 700, 0, 33, 1500, 0]
+    q_len = [40, 1, 1, 130, 1, 260]
+    step = W.build(W.custom(ctx, q_len, 16, 4, seed=44, pad_tokens=5))
+    run_and_check(step, "interleaved")
+
+
+def test_two_chunks_match_one_prefill():
+    """448 prompt tokens as one prefill vs 224 + 224 with the second chunk
+    continuing the first: same rows (both within tolerance of the oracle and
+    of each other)."""
+    whole = W.build(W.custom([0], [448], 8, 2, seed=55))
+    _, a = run_and_check(whole, "whole")
+    two = W.build(W.custom([0, 224], [224, 224], 8, 2, seed=55))
+    # same prompt: reuse the whole prefill's q/k/v rows and place the second
+    # chunk's history (the first chunk) in its cache like the first request's
+    two.qkv[:] = whole.qkv
+    two.q = two.qkv[:, :8 * 128].reshape(448, 8, 128)
+    two.k = two.qkv[:, 8 * 128:10 * 128].reshape(448, 2, 128)
+    two.v = two.qkv[:, 10 * 128:].reshape(448, 2, 128)
+    kc, vc = two.key_cache, two.value_cache
+    for j in range(224):
+        blk = two.block_table[1, j // 16]
+        kc[blk, j % 16] = whole.k[j]
+        vc[blk, j % 16] = whole.v[j]
+    _, b = run_and_check(two, "two chunks")
+    # chunk 2's rows equal the whole prefill's rows 224..447
+    diff = np.abs(a[224:448] - b[224:448])
+    assert (diff <= 1e-2 + 1e-2 * np.abs(a[224:448])).all()
+
+
+def test_prefill_bit_identical_under_block_permutation():
+    outs = []
+    for seed in (3, 4):
+        step = W.build(W.custom([100, 0], [60, 200], 8, 2, seed=66))
+        rng = np.random.default_rng(seed)
+        perm = rng.permutation(step.key_cache.shape[0]).astype(np.int32)
+        inv = np.argsort(perm).astype(np.int32)
+        step.key_cache = step.key_cache[inv]
+        step.value_cache = step.value_cache[inv]
+        bt = step.block_table
+        step.block_table = np.where(bt >= 0, perm[np.clip(bt, 0, None)], -1).astype(np.int32)
+        sm = step.slot_mapping
+        step.slot_mapping = np.where(sm >= 0, perm[sm // 16].astype(np.int64) * 16 + sm % 16, -1)
+        ds, _ = run_and_check(step, "permuted %d" % seed)
+        outs.append(ds.out.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_large_prefill_sampled_rows():
+    step = W.build(W.spec("large_prefill"))
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()
+    assert pkv.pkv_get_error() == 0
+    got = ds.out_f64()
+    rng = np.random.default_rng(0)
+    # rows at tile edges and in the ragged parts of every request, all heads
+    rows = []
+    for r in range(step.num_reqs):
+        q0 = int(step.query_start_loc[r])
+        rows += [q0, q0 + 1, q0 + 127, q0 + 128, q0 + 1023, q0 + 2047]
+        rows += (q0 + rng.integers(0, 2048, 4)).tolist()
+    rows = np.repeat(np.array(rows, dtype=np.int64), 4)
+    heads = rng.integers(0, step.spec.hq, rows.shape[0]).astype(np.int32)
+    ref, err = oracle.attention_sampled(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                        step.block_table, step.num_reqs, step.scale, rows, heads)
+    assert err == 0
+    assert_close(got[rows, heads], ref, "large_prefill sampled")
+    assert np.isfinite(got).all()
