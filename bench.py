@@ -210,12 +210,17 @@ def main():
     ap.add_argument("--config", default="mha_decode", choices=W.CONFIG_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--reqs", type=int, default=0,
+                    help="first N requests of the workload only, with a pool sized for them "
+                         "(a small case of the same kernel shapes, e.g. for profiling)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     spec = W.spec(args.config)
+    if args.reqs:
+        spec = W.subset(spec, args.reqs)
     if args.impl == "reference":
         run_reference(args, spec, rank)
         return

@@ -253,6 +253,9 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
   if (!q || !key_cache || !value_cache || !query_start_loc || !seq_lens || !block_table || !out)
     return fail(PKV_ERR_ARG, "null pointer argument");
   if (block_table_width < 1) return fail(PKV_ERR_ARG, "block_table_width < 1");
+  if (block_table_width > kMaxBtWidth)
+    return fail(PKV_ERR_UNSUPPORTED, "block_table_width %lld > %d (longest supported request is "
+                "%d keys)", (long long)block_table_width, kMaxBtWidth, kMaxBtWidth * kBlockSize);
   const int64_t row = (int64_t)num_heads * kHeadSize;
   if (q_row_stride < row || out_row_stride < row)
     return fail(PKV_ERR_ARG, "q/out row stride below num_heads * head_size (%lld)",
@@ -291,7 +294,7 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
   a.out = static_cast<uint16_t*>(out);
   a.out_stride = out_row_stride;
 
-  const int dec_grid = s->sms * decode_ctas_per_sm(num_heads / num_kv_heads);
+  const int dec_grid = decode_grid(num_heads / num_kv_heads, s->sms);
   cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, dec_grid, st); });
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   e = traced(2, st, [&] { return launch_decode(a, ws, dec_grid, st); });

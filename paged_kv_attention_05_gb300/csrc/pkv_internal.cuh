@@ -2,6 +2,7 @@
 // Not part of the public C ABI (include/pkv.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,20 +14,19 @@ constexpr int kHeadSize = 128;   // elements per head row
 constexpr int kBlockSize = 16;   // tokens per cache block (page)
 constexpr int kMaxGroup = 32;    // query heads per KV head handled by one decode unit
 constexpr int kDecTile = 64;     // tokens per decode pipeline stage (4 pages)
-constexpr int kDecStages = 3;    // decode cp.async pipeline depth
-constexpr int kDecThreads = 128; // 4 warps, one page of each stage per warp
 constexpr int kMinChunk = 256;   // smallest split-KV chunk (tokens)
 constexpr int kMaxChunk = 1024;  // largest split-KV chunk (tokens)
+constexpr int kMaxBtWidth = 32768;  // block-table entries per request (524,288 keys) at most
 constexpr int kPreTileQ = 128;   // query rows per prefill tile
 
 // One decode work unit: request r, KV head g, keys [k0, k1) of the request.
-struct DecUnit {
+struct __align__(16) DecUnit {
   int r, g, split, nsplit, k0, k1, part, pad;
 };
 
 // One prefill work entry: request r, 128-row query tile qt; nkv = number of
 // 128-key tiles it reads (work estimate used for longest-first ordering).
-struct PreEntry {
+struct __align__(16) PreEntry {
   int r, qt, nkv, pad;
 };
 
@@ -84,9 +84,18 @@ struct AttnArgs {
   int64_t out_stride;
 };
 
+// TMA descriptors (pkv_tma.cu).  rows map: [rows, heads, 128] bf16 with a row
+// stride, box = 64 columns x box_heads x box_rows; cache map: [num_blocks, 16,
+// hkv, 128] bf16, box = 64 columns x 1 head x 16 slots x 1 block.  Both use
+// the 128-byte swizzle.
+bool tma_available();
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t row_stride,
+                   int box_heads, int box_rows);
+bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv);
+
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int grid, cudaStream_t st);
-int decode_ctas_per_sm(int group);
+int decode_grid(int group, int sms);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
 }  // namespace pkv

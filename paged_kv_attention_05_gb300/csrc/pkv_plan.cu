@@ -157,16 +157,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       const int sp = rem / a.hkv, g = rem - sp * a.hkv;
       const int64_t idx = (int64_t)unit_carry + i;
       if (idx >= ws.max_units) break;
-      DecUnit u;
-      u.r = base + lo;
-      u.g = g;
-      u.split = sp;
-      u.nsplit = nsplit;
-      u.k0 = sp * chunk;
-      u.k1 = min(L, (sp + 1) * chunk);
-      u.part = nsplit > 1 ? s_off_p[lo] + g * nsplit + sp : -1;
-      u.pad = 0;
-      ws.units[idx] = u;
+      // two 16-byte stores per unit: consecutive threads fill consecutive units
+      int4* dst = reinterpret_cast<int4*>(ws.units + idx);
+      dst[0] = make_int4(base + lo, g, sp, nsplit);
+      dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
+                         nsplit > 1 ? s_off_p[lo] + g * nsplit + sp : -1, 0);
     }
     for (int i = tid; i < tot_t; i += kPlanThreads) {
       int lo = 0, hi = kPlanThreads - 1;
@@ -181,12 +176,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       const int64_t idx = (int64_t)pre_carry + i;
       if (idx >= ws.max_pre) break;
       const int last_row = min(kPreTileQ * (t + 1), n);
-      PreEntry e;
-      e.r = base + lo;
-      e.qt = t;
-      e.nkv = (ctx + last_row + kPreTileQ - 1) / kPreTileQ;
-      e.pad = 0;
-      ws.pre[idx] = e;
+      *reinterpret_cast<int4*>(ws.pre + idx) =
+          make_int4(base + lo, t, (ctx + last_row + kPreTileQ - 1) / kPreTileQ, 0);
     }
     unit_carry += tot_u;
     part_carry += tot_p;

@@ -36,14 +36,12 @@
 //               the bf16 rows of the item straight to global memory.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // PKV_DEV_ERR_TIMEOUT, stops issuing work, frees its TMEM and returns.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cudaTypedefs.h>
-
-#include "pkv_internal.cuh"
+#include "pkv_device.cuh"
 
 namespace pkv {
 namespace {
+
+using namespace dev;
 
 constexpr int kThreads = 256;
 constexpr int kStages = 2;
@@ -52,9 +50,7 @@ constexpr int kHalfBytes = 128 * 128;             // 128 rows x 64 bf16
 constexpr int kTileBytes = 2 * kHalfBytes;        // Q, K, V or P tile: 32 KB
 constexpr int kPageBoxBytes = 16 * 128;           // one 16-slot x 64-dim box
 constexpr int kTmemCols = 512;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
-constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
@@ -70,80 +66,6 @@ constexpr int kSmemBytes = kOffCtl + 64 + 1024;  // + alignment slack
 
 enum { B_Q = 0, B_K = 1, B_V = 3, B_VT = 5, B_EMPTY = 7, B_S = 9, B_P = 11, B_O = 12 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-// Bounded wait: true when the phase completed; false after kWaitNs or when
-// another role has given up (abort flag), in which case the caller unwinds.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
-  if (mbar_try(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
-  while (true) {
-    if (mbar_try(bar, parity)) return true;
-    if (*abort) return false;
-    if (now_ns() - t0 > kWaitNs) {
-      *abort = 1;
-      atomicOr(err, PKV_DEV_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// The same wait taken by every lane of a warp, with a warp-uniform result
-// (warp-collective tcgen05 and shuffle instructions follow it).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
-                                               int* err) {
-  const bool ok = mbar_wait(bar, parity, abort, err);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -217,17 +139,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 struct Item {
   int r, qt, h, g;
   int q0, n, L, ctx;
@@ -262,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_P), 128);
     mbar_init(bar(B_O), 1);
     ctl[1] = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    fence_async_smem();
+    fence_barrier_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
@@ -529,43 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// q / out: [rows, hq, 128] with row stride; box = 64 dims x 1 head x 128 rows
-bool make_q_map(CUtensorMap* m, const void* base, int64_t rows, int hq, int64_t row_stride) {
-  cuuint64_t dims[3] = {128, (cuuint64_t)hq, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {256, (cuuint64_t)row_stride * 2};
-  cuuint32_t box[3] = {64, 1, 128};
-  cuuint32_t es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// cache: [num_blocks, 16, hkv, 128]; box = 64 dims x 1 head x 16 slots x 1 block
-bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv) {
-  cuuint64_t dims[4] = {128, (cuuint64_t)hkv, 16, (cuuint64_t)num_blocks};
-  cuuint64_t strides[3] = {256, (cuuint64_t)hkv * 256, (cuuint64_t)hkv * 256 * 16};
-  cuuint32_t box[4] = {64, 1, 16, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
@@ -576,9 +449,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cuda
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  if (!encode_fn()) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv;
-  if (!make_q_map(&tq, a.q, a.q_rows, a.hq, a.q_stride) ||
+  if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, 1, kPreTileQ) ||
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;

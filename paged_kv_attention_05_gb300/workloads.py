@@ -257,3 +257,13 @@ def custom(ctx, q_len, hq, hkv, num_blocks=None, seed=7, pad_tokens=0, std=1.0,
     nb = num_blocks if num_blocks is not None else max(need + need // 2 + 3, 4)
     return StepSpec("custom", list(ctx), list(q_len), hq, hkv, nb, seed,
                     pad_tokens=pad_tokens, std=std, bt_width=bt_width)
+
+
+def subset(s: StepSpec, n_reqs: int) -> StepSpec:
+    """The first n_reqs requests of a workload, with a pool 10% larger than
+    they need (same seeds, same shapes per request)."""
+    ctx, q_len = s.ctx[:n_reqs], s.q_len[:n_reqs]
+    need = sum(-(-(c + n) // s.block_size) for c, n in zip(ctx, q_len))
+    return StepSpec(s.name, ctx, q_len, s.hq, s.hkv, need + need // 10 + 1, s.seed,
+                    pad_tokens=s.pad_tokens if n_reqs >= s.num_reqs else 0, std=s.std,
+                    head_size=s.head_size, block_size=s.block_size, bt_width=s.bt_width)
