@@ -172,9 +172,9 @@ int pkv_num_sms(void);
  * launch's duration to its kernel kind, copies up to n kinds of totals into
  * ms[] and launches[] (either may be NULL), clears the record and returns the
  * number of kinds (PKV_TRACE_KINDS).  Kinds: 0 cache write, 1 step plan,
- * 2 decode attention, 3 prefill attention.
+ * 2 decode attention, 3 prefill attention, 4 split-KV merge.
  */
-#define PKV_TRACE_KINDS 4
+#define PKV_TRACE_KINDS 5
 int pkv_trace_enable(int on);
 int pkv_trace_read(double* ms, int64_t* launches, int n);
 

@@ -18,7 +18,7 @@ DEV_ERR_BITS = {
 EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
            "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
            "pkv_launch_count"]
-TRACE_KINDS = ["write", "plan", "decode", "prefill"]
+TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine"]
 
 
 class PkvError(RuntimeError):

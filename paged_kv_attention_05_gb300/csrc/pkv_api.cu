@@ -158,7 +158,7 @@ size_t workspace_bytes(int64_t max_units, int64_t max_pre, int64_t max_pairs, in
   size_t b = 256;                                      // header
   b += (size_t)max_units * sizeof(DecUnit);
   b += (size_t)max_pre * sizeof(PreEntry);
-  b += (size_t)max_pairs * sizeof(int);
+  b += (size_t)max_pairs * sizeof(SplitPair);
   b = (b + 255) & ~(size_t)255;
   b += (size_t)max_units * group * 2 * sizeof(float);  // part_ml
   b = (b + 255) & ~(size_t)255;
@@ -177,8 +177,8 @@ Workspace carve_workspace(void* base, int64_t max_units, int64_t max_pre, int64_
   off += (size_t)max_units * sizeof(DecUnit);
   w.pre = reinterpret_cast<PreEntry*>(p + off);
   off += (size_t)max_pre * sizeof(PreEntry);
-  w.counters = reinterpret_cast<int*>(p + off);
-  off += (size_t)max_pairs * sizeof(int);
+  w.pairs = reinterpret_cast<SplitPair*>(p + off);
+  off += (size_t)max_pairs * sizeof(SplitPair);
   off = (off + 255) & ~(size_t)255;
   w.part_ml = reinterpret_cast<float*>(p + off);
   off += (size_t)max_units * group * 2 * sizeof(float);
@@ -294,11 +294,13 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
   a.out = static_cast<uint16_t*>(out);
   a.out_stride = out_row_stride;
 
-  const int dec_grid = decode_grid(num_heads / num_kv_heads, s->sms);
-  cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, dec_grid, st); });
+  const int workers = decode_workers(num_heads / num_kv_heads, s->sms);
+  cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  e = traced(2, st, [&] { return launch_decode(a, ws, dec_grid, st); });
+  e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return PKV_OK;
@@ -357,8 +359,8 @@ extern "C" int pkv_trace_enable(int on) {
 
 extern "C" int pkv_trace_read(double* ms, int64_t* launches, int n) {
   std::lock_guard<std::mutex> lock(g_mu);
-  double tot[PKV_TRACE_KINDS] = {0, 0, 0, 0};
-  int64_t cnt[PKV_TRACE_KINDS] = {0, 0, 0, 0};
+  double tot[PKV_TRACE_KINDS] = {};
+  int64_t cnt[PKV_TRACE_KINDS] = {};
   int rc = PKV_OK;
   for (const TraceRec& r : g_trace) {
     float t = 0.f;

@@ -1,6 +1,5 @@
 // Split-KV decode attention over the paged cache (requests with one query
-// token), with the split merge fused into the last unit of each
-// (request, KV head) to finish.
+// token), and the merge of split results.
 //
 // What it computes: "vLLM 推理全流程深度解析" (vLLM inference deep dive),
 // paged_attention_v1 section — find the request's physical blocks through
@@ -11,31 +10,28 @@
 // Cache", section "One Path Covers MHA, GQA, and MQA": the G = Hq / Hkv query
 // heads of a KV head read the same K/V rows.
 //
-// GB300 design.  Decode is bound by HBM: every key and value row is read once
-// per KV head and used by the G query heads of that KV head.
-//   * Work unit = (request, KV head, key range of at most 1024 keys); the plan
-//     kernel lists the units.  One CTA per SM runs until the list is empty.
-//   * Warp 4 is the producer.  It takes units from an atomic cursor, fetches
-//     the unit's block ids with the whole warp, and streams the unit's pages
-//     with TMA (one 16-slot x 64-dim box per page, K and V, two 64-dim halves,
-//     128-byte swizzle) into a ring of 64-key stages (4 pages).  It does not
-//     wait for the consumers at unit boundaries, so the ring stays full across
-//     units; the unit's G query rows come with the unit descriptor, also by
-//     TMA, into one of two query slots.
-//   * Warps 0-3 consume: warp w takes page w of every stage.  The G query
-//     heads are the rows of 16-row tiles, so S = Q.K^T and O += P.V run on the
-//     tensor cores with bf16 mma.sync m16n8k16 and fp32 accumulation (with up
-//     to 32 heads per K/V row the FMA pipes could not keep pace with HBM);
-//     the running max and sum stay in registers, with quad shuffles for the
-//     row reductions and exp2 with the scale folded in.  Keys at or past the
-//     unit's end are masked in S and their V values zeroed in the fragments,
-//     so stale or NaN cache slots never reach the product.
-//   * At the end of a unit the four warps merge through shared memory.  A
-//     unit that is one split of several writes (max, sum, unnormalised output)
-//     in fp32 to the workspace and takes a ticket; the split that arrives last
-//     merges all splits (the weights staged in shared memory, then one output
-//     column per thread with independent loads) and writes the bf16 result.
-//     No CTA ever waits on another; every mbarrier wait is bounded.
+// GB300 design.  Decode is bound by HBM: each K/V row is read once per KV head
+// and used by the G query heads of that head.
+//   * Work unit = (request, KV head, range of at most 2048 keys), listed by the
+//     plan kernel.  A CTA per SM holds 8 warps.  Each warp takes units from an
+//     atomic cursor and streams the unit's pages by itself: TMA boxes of 16
+//     slots x 64 dims (K and V, two halves, 128-byte swizzle) into its own
+//     ring of 8 KB page stages (3 deep, 2 for 32-head groups).  Warps never
+//     wait for each other, so each SM keeps 8 independent streams of loads in
+//     flight and 8 warps to hide the latency of the math.
+//   * A warp owns the G query-head rows of its KV head in one or two 16-row
+//     tiles (zero rows past G): S = Q.K^T and O += P.V run
+//     on the tensor cores with bf16 mma.sync m16n8k16 and fp32 accumulation
+//     (with up to 32 heads per K/V row the FMA pipes could not keep pace with
+//     HBM); the softmax state stays in registers, row reductions by quad
+//     shuffles, exp2 with the scale folded in, and the output is rescaled only
+//     when a row's maximum grows by more than 2^8 (exact; rarely needed).
+//     Keys past the unit's end are masked in S and their V values zeroed in
+//     the fragments, so stale or NaN cache slots never reach the product.
+//   * A unit that covers a whole request writes the bf16 output; one split of
+//     several writes (max, sum, unnormalised output) in fp32 to the workspace,
+//     and the combine kernel merges the splits afterwards.  Every mbarrier wait
+//     is bounded.
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -43,30 +39,21 @@ namespace {
 
 using namespace dev;
 
-constexpr int kConsumers = 4;                    // consumer warps
-constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
-constexpr int kHalf = kDecTile * 128;            // 64 keys x 64 dims (8 KB)
-constexpr int kStageBytes = 4 * kHalf;           // K lo | K hi | V lo | V hi
-constexpr int kPageHalf = kBlockSize * 128;      // one TMA box: 16 slots x 64 dims
-constexpr int kMaxUnitPages = kMaxChunk / kBlockSize;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2 KB)
+constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
+constexpr int kIdRegs = kMaxChunk / kBlockSize / 32;  // block ids per lane per unit
 
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = MT == 1 ? 5 : 4;
-  static constexpr int kRows = MT * 16;                  // query rows per tile
-  static constexpr int kQHalf = kRows * 128;             // one 64-dim half of a query slot
-  static constexpr int kQSlot = 2 * kQHalf;
-  static constexpr int kMerge = kConsumers * kRows * (kHeadSize + 2) * 4;
-  // layout (from a 1024-byte aligned base)
-  static constexpr int kOffStage = 0;
-  static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
-  static constexpr int kOffMerge = kOffQ + 2 * kQSlot;
-  static constexpr int kOffUnit = kOffMerge + kMerge;     // 2 x (DecUnit + block ids)
-  static constexpr int kUnitSlot = 32 + kMaxUnitPages * 4;
-  static constexpr int kOffBar = (kOffUnit + 2 * kUnitSlot + 7) & ~7;
-  static constexpr int kNumBars = 2 * kStages + 4;         // full, empty, ufull[2], uempty[2]
-  static constexpr int kOffCtl = kOffBar + kNumBars * 8;
-  static constexpr int kSmem = kOffCtl + 32 + 1024;
+  static constexpr int kStages = MT == 1 ? 3 : 2;
+  static constexpr int kQHalf = MT * 16 * 128;        // query rows x one 64-dim half
+  static constexpr int kWarpBytes = kStages * kPage + 2 * kQHalf;
+  static constexpr int kBarsPerWarp = kStages + 1;     // page stages, query
+  static constexpr int kOffBar = kWarps * kWarpBytes;
+  static constexpr int kOffCtl = kOffBar + kWarps * kBarsPerWarp * 8;
+  static constexpr int kSmem = kOffCtl + 16 + 1024;
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -83,20 +70,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 
 // D += A(16x16, row) * B(16x8, col); bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers * 32) : "memory");
-}
-
-// keep the bf16 halves of a register whose token index is below `valid`
+// keep the bf16 halves of a register whose key index is below `valid`
 __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok_lo, int valid) {
   const uint32_t lo = tok_lo < valid ? 0x0000FFFFu : 0u;
   const uint32_t hi = tok_lo + 1 < valid ? 0xFFFF0000u : 0u;
@@ -111,128 +94,105 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + C::kOffBar;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
-  auto ufull_bar = [&](int s) { return bar0 + 8u * (2 * C::kStages + s); };
-  auto uempty_bar = [&](int s) { return bar0 + 8u * (2 * C::kStages + 2 + s); };
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffCtl);
-  int* s_ticket = reinterpret_cast<int*>(smem + C::kOffCtl + 4);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.hq / a.hkv;
-  const int n_units = ws.hdr->n_dec_units;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t wbase = sbase + warp * C::kWarpBytes;        // this warp's page stages
+  const uint32_t qbuf = wbase + C::kStages * kPage;           // and query rows
+  const uint32_t bars = sbase + C::kOffBar + warp * C::kBarsPerWarp * 8;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  const uint32_t q_bar = bars + 8u * C::kStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffCtl);
 
-  if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumers);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(ufull_bar(s), 1);
-      mbar_init(uempty_bar(s), kConsumers);
-    }
-    *abort = 0;
+  if (lane == 0) {
+    for (int s = 0; s <= C::kStages; ++s) mbar_init(bars + 8u * s, 1);
+    if (warp == 0) *abort = 0;
     fence_barrier_init();
   }
-  // query rows G..kRows-1 of both slots are never loaded: keep them zero
-  for (int i = tid; i < 2 * 2 * C::kRows * 8; i += kThreads) {
-    const int c = i & 7, row = (i >> 3) % C::kRows, half = (i >> 3) / C::kRows;  // half 0..3
+  // query rows G .. MT*16-1 are never loaded: keep them zero
+  for (int i = lane; i < 2 * MT * 16 * 8; i += 32) {
+    const int row = (i >> 3) % (MT * 16), half = (i >> 3) / (MT * 16), c = i & 7;
     if (row >= G)
-      *reinterpret_cast<uint4*>(smem + C::kOffQ + half * C::kQHalf + row * 128 + c * 16) =
+      *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
 
-  if (warp == kConsumers) {
-    // ------------------------------ producer ------------------------------
-    uint32_t tile_cnt = 0, unit_cnt = 0;
-    for (;; ++unit_cnt) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(&ws.hdr->dec_counter, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      const int slot = unit_cnt & 1;
-      if (unit_cnt >= 2 &&
-          !mbar_wait_warp(uempty_bar(slot), ((unit_cnt >> 1) - 1) & 1, abort, ws.err))
-        break;
-      uint8_t* us = smem + C::kOffUnit + slot * C::kUnitSlot;
-      DecUnit* ud = reinterpret_cast<DecUnit*>(us);
-      int* ids = reinterpret_cast<int*>(us + 32);
-      if (u >= n_units) {
-        if (lane == 0) {
-          ud->r = -1;
-          mbar_arrive(ufull_bar(slot));
-        }
-        break;
-      }
-      const DecUnit un = ws.units[u];
-      const int* btrow = a.bt + (int64_t)un.r * a.bt_width;
-      const int p0 = un.k0 / kBlockSize;
-      const int npages = (un.k1 + kBlockSize - 1) / kBlockSize - p0;
-      for (int i = lane; i < npages; i += 32) {
-        int blk = __ldg(btrow + p0 + i);
-        if (blk < 0 || (int64_t)blk >= a.num_blocks) {
-          atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
-          blk = 0;
-        }
-        ids[i] = blk;
-      }
-      if (lane == 0) *ud = un;
-      __syncwarp();
-      if (lane == 0) {
-        // the unit's query rows: heads g*G .. g*G+G-1 of token query_start_loc[r]
-        const int q0 = a.qsl[un.r];
-        const uint32_t qdst = sbase + C::kOffQ + slot * C::kQSlot;
-        mbar_expect_tx(ufull_bar(slot), 2 * G * 128);
-        tma_load_3d(qdst, &tm_q, ufull_bar(slot), 0, un.g * G, q0);
-        tma_load_3d(qdst + C::kQHalf, &tm_q, ufull_bar(slot), 64, un.g * G, q0);
-      }
-      const int ntiles = (un.k1 - un.k0 + kDecTile - 1) / kDecTile;
-      bool ok = true;
-      for (int t = 0; t < ntiles; ++t, ++tile_cnt) {
-        const int s = tile_cnt % C::kStages;
-        if (tile_cnt >= (uint32_t)C::kStages &&
-            !mbar_wait_warp(empty_bar(s), ((tile_cnt / C::kStages) - 1) & 1, abort, ws.err)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const int pages = min(4, npages - t * 4);
-          const uint32_t st = sbase + C::kOffStage + s * kStageBytes;
-          mbar_expect_tx(full_bar(s), pages * 4 * kPageHalf);
-          for (int p = 0; p < pages; ++p) {
-            const int blk = ids[t * 4 + p];
-            const uint32_t off = p * kPageHalf;
-            tma_load_4d(st + off, &tm_k, full_bar(s), 0, un.g, 0, blk);
-            tma_load_4d(st + kHalf + off, &tm_k, full_bar(s), 64, un.g, 0, blk);
-            tma_load_4d(st + 2 * kHalf + off, &tm_v, full_bar(s), 0, un.g, 0, blk);
-            tma_load_4d(st + 3 * kHalf + off, &tm_v, full_bar(s), 64, un.g, 0, blk);
-          }
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-    }
-    return;
-  }
-
-  // ------------------------------ consumers ------------------------------
+  const int n_units = ws.hdr->n_dec_units;
+  const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
-  const float sl2 = a.scale * kLog2e;
-  float* mw = reinterpret_cast<float*>(smem + C::kOffMerge);
-  float* lw = mw + kConsumers * C::kRows;
-  float* ow = lw + kConsumers * C::kRows;
-  uint32_t tile_cnt = 0;
+  uint32_t page_cnt = 0;
+
   for (uint32_t unit_cnt = 0;; ++unit_cnt) {
-    const int slot = unit_cnt & 1;
-    if (!mbar_wait_warp(ufull_bar(slot), (unit_cnt >> 1) & 1, abort, ws.err)) break;
-    const DecUnit un = *reinterpret_cast<const DecUnit*>(smem + C::kOffUnit + slot * C::kUnitSlot);
-    if (un.r < 0) break;
-    const uint32_t qs = sbase + C::kOffQ + slot * C::kQSlot;
+    int u = 0;
+    if (lane == 0) u = atomicAdd(&ws.hdr->dec_counter, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= n_units || *abort) break;
+    const DecUnit un = ws.units[u];
     const int k0 = un.k0, k1 = un.k1;
-    const int ntiles = (k1 - k0 + kDecTile - 1) / kDecTile;
+    const int p0 = k0 / kBlockSize;
+    const int npages = (k1 + kBlockSize - 1) / kBlockSize - p0;
+
+    // block ids of the unit, one per lane per 32 pages
+    int ids[kIdRegs];
+    {
+      const int* btrow = a.bt + (int64_t)un.r * a.bt_width + p0;
+#pragma unroll
+      for (int j = 0; j < kIdRegs; ++j) {
+        const int p = lane + 32 * j;
+        int blk = 0;
+        if (p < npages) {
+          blk = __ldg(btrow + p);
+          if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+            atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
+            blk = 0;
+          }
+        }
+        ids[j] = blk;
+      }
+    }
+    // the G query rows of this KV head (heads g*G ..) by TMA
+    if (lane == 0) {
+      fence_async_smem();  // the previous unit's reads of the buffer are done
+      mbar_expect_tx(q_bar, 2 * G * 128);
+      const int q0 = a.qsl[un.r];
+      tma_load_3d(qbuf, &tm_q, q_bar, 0, un.g * G, q0);
+      tma_load_3d(qbuf + C::kQHalf, &tm_q, q_bar, 64, un.g * G, q0);
+    }
+
+    // page p of the unit into stage (page_cnt + p) % kStages; the stage's
+    // previous page was consumed by this warp already (program order)
+    auto issue_page = [&](int p) {
+      const uint32_t x = page_cnt + p;
+      const int s = x % C::kStages;
+      int idv = ids[0];
+#pragma unroll
+      for (int j = 1; j < kIdRegs; ++j)
+        if ((p >> 5) == j) idv = ids[j];
+      const int blk = __shfl_sync(0xffffffffu, idv, p & 31);
+      if (lane == 0) {
+        fence_async_smem();
+        const uint32_t st = wbase + s * kPage;
+        mbar_expect_tx(full_bar(s), kPage);
+        tma_load_4d(st, &tm_k, full_bar(s), 0, un.g, 0, blk);
+        tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, un.g, 0, blk);
+        tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, un.g, 0, blk);
+        tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, un.g, 0, blk);
+      }
+    };
+    for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
+    if (!mbar_wait_warp(q_bar, unit_cnt & 1, abort, ws.err)) break;
+
+    // query fragments: registers for one tile, re-read from shared memory for two
+    uint32_t qa[MT == 1 ? 8 : 1][4];
+    if (MT == 1) {
+#pragma unroll
+      for (int kstep = 0; kstep < (MT == 1 ? 8 : 1); ++kstep)
+        ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf + sw128(rr + ((mi & 1) << 3),
+                                                         (kstep & 3) * 2 + (mi >> 1)),
+                qa[kstep][0], qa[kstep][1], qa[kstep][2], qa[kstep][3]);
+    }
 
     float o[MT][16][4];
     float m_run[MT][2], l_run[MT][2];
@@ -247,79 +207,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t, ++tile_cnt) {
-      const int s = tile_cnt % C::kStages;
-      if (!mbar_wait_warp(full_bar(s), (tile_cnt / C::kStages) & 1, abort, ws.err)) {
+    for (int p = 0; p < npages; ++p) {
+      const uint32_t x = page_cnt + p;
+      const int s = x % C::kStages;
+      if (!mbar_wait_warp(full_bar(s), (x / C::kStages) & 1, abort, ws.err)) {
         ok = false;
         break;
       }
-      const int pos0 = k0 + t * kDecTile + warp * 16;
-      if (pos0 < k1) {
-        const int valid = k1 - pos0;  // keys of this page inside the unit (may be >= 16)
-        const uint32_t st = sbase + C::kOffStage + s * kStageBytes;
-        const int prow = warp * 16;   // first row of this warp's page in the stage
-        // S = Q K^T for the page's 16 keys (two n-tiles of 8)
-        float sacc[MT][2][4];
+      const int valid = k1 - (k0 + p * kBlockSize);  // keys of this page inside the unit
+      const uint32_t st = wbase + s * kPage;
+
+      // S = Q K^T for the page's 16 keys (two n-tiles of 8)
+      float sacc[MT][2][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
 #pragma unroll
-        for (int kstep = 0; kstep < 8; ++kstep) {
-          const int half = kstep >> 2, c0 = (kstep & 3) * 2;
-          uint32_t b0, b1, b2, b3;
-          {
-            const int krow = prow + rr + ((mi >> 1) << 3);
-            ldsm_x4(st + half * kHalf + sw128(krow, c0 + (mi & 1)), b0, b1, b2, b3);
-          }
+      for (int kstep = 0; kstep < 8; ++kstep) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + (kstep >> 2) * kBox + sw128(rr + ((mi >> 1) << 3), (kstep & 3) * 2 + (mi & 1)),
+                b0, b1, b2, b3);
+        if (MT == 1) {
+          mma_bf16(sacc[0][0], qa[MT == 1 ? kstep : 0], b0, b1);
+          mma_bf16(sacc[0][1], qa[MT == 1 ? kstep : 0], b2, b3);
+        } else {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            const int qrow = mt * 16 + rr + ((mi & 1) << 3);
-            ldsm_x4(qs + half * C::kQHalf + sw128(qrow, c0 + (mi >> 1)), a0, a1, a2, a3);
-            mma_bf16(sacc[mt][0], a0, a1, a2, a3, b0, b1);
-            mma_bf16(sacc[mt][1], a0, a1, a2, a3, b2, b3);
+            uint32_t qf[4];
+            ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf +
+                        sw128(mt * 16 + rr + ((mi & 1) << 3), (kstep & 3) * 2 + (mi >> 1)),
+                    qf[0], qf[1], qf[2], qf[3]);
+            mma_bf16(sacc[mt][0], qf, b0, b1);
+            mma_bf16(sacc[mt][1], qf, b2, b3);
           }
         }
+      }
 
-        // online softmax (log2 domain), masking keys >= k1
-        uint32_t pa[MT][4];
+      // online softmax in the log2 domain, keys >= k1 masked; the output is
+      // rescaled only when a row's maximum grows by more than 2^8
+      uint32_t pa[MT][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          float x[2][4];
-          float mx0 = -INFINITY, mx1 = -INFINITY;
+      for (int mt = 0; mt < MT; ++mt) {
+        float xs[2][4];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = nt * 8 + tig * 2 + (e & 1);
-              x[nt][e] = tok < valid ? sacc[mt][nt][e] * sl2 : -INFINITY;
-            }
-            mx0 = fmaxf(mx0, fmaxf(x[nt][0], x[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(x[nt][2], x[nt][3]));
+          for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + tig * 2 + (e & 1);
+            xs[nt][e] = tok < valid ? sacc[mt][nt][e] * sl2 : -INFINITY;
           }
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m_run[mt][0], mx0), mn1 = fmaxf(m_run[mt][1], mx1);
-          const float al0 = fast_exp2(m_run[mt][0] - mn0), al1 = fast_exp2(m_run[mt][1] - mn1);
-          m_run[mt][0] = mn0;
-          m_run[mt][1] = mn1;
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            x[nt][0] = fast_exp2(x[nt][0] - mn0);
-            x[nt][1] = fast_exp2(x[nt][1] - mn0);
-            x[nt][2] = fast_exp2(x[nt][2] - mn1);
-            x[nt][3] = fast_exp2(x[nt][3] - mn1);
-            s0 += x[nt][0] + x[nt][1];
-            s1 += x[nt][2] + x[nt][3];
-          }
-          l_run[mt][0] = l_run[mt][0] * al0 + s0;
-          l_run[mt][1] = l_run[mt][1] * al1 + s1;
+          mx0 = fmaxf(mx0, fmaxf(xs[nt][0], xs[nt][1]));
+          mx1 = fmaxf(mx1, fmaxf(xs[nt][2], xs[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const bool up0 = mx0 > m_run[mt][0] + 8.f, up1 = mx1 > m_run[mt][1] + 8.f;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+          const float n0 = up0 ? mx0 : m_run[mt][0], n1 = up1 ? mx1 : m_run[mt][1];
+          const float al0 = fast_exp2(m_run[mt][0] - n0), al1 = fast_exp2(m_run[mt][1] - n1);
+          m_run[mt][0] = n0;
+          m_run[mt][1] = n1;
+          l_run[mt][0] *= al0;
+          l_run[mt][1] *= al1;
 #pragma unroll
           for (int dn = 0; dn < 16; ++dn) {
             o[mt][dn][0] *= al0;
@@ -327,42 +282,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[mt][dn][2] *= al1;
             o[mt][dn][3] *= al1;
           }
-          pa[mt][0] = pack_bf16(x[0][0], x[0][1]);
-          pa[mt][1] = pack_bf16(x[0][2], x[0][3]);
-          pa[mt][2] = pack_bf16(x[1][0], x[1][1]);
-          pa[mt][3] = pack_bf16(x[1][2], x[1][3]);
         }
+        const float c0 = m_run[mt][0], c1 = m_run[mt][1];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          xs[nt][0] = fast_exp2(xs[nt][0] - c0);
+          xs[nt][1] = fast_exp2(xs[nt][1] - c0);
+          xs[nt][2] = fast_exp2(xs[nt][2] - c1);
+          xs[nt][3] = fast_exp2(xs[nt][3] - c1);
+          l_run[mt][0] += xs[nt][0] + xs[nt][1];
+          l_run[mt][1] += xs[nt][2] + xs[nt][3];
+        }
+        pa[mt][0] = pack_bf16(xs[0][0], xs[0][1]);
+        pa[mt][1] = pack_bf16(xs[0][2], xs[0][3]);
+        pa[mt][2] = pack_bf16(xs[1][0], xs[1][1]);
+        pa[mt][3] = pack_bf16(xs[1][2], xs[1][3]);
+      }
 
-        // O += P V (V rows read transposed); zero V of keys past the unit
+      // O += P V (V rows read transposed); V of keys past the unit zeroed
 #pragma unroll
-        for (int dn = 0; dn < 16; dn += 2) {
-          const int half = dn >> 3, c = dn & 7;
-          uint32_t b0, b1, b2, b3;
-          const int vrow = prow + rr + ((mi & 1) << 3);
-          ldsm_x4_t(st + (2 + half) * kHalf + sw128(vrow, c + (mi >> 1)), b0, b1, b2, b3);
-          if (valid < 16) {
-            b0 = mask_pair(b0, 2 * tig, valid);
-            b2 = mask_pair(b2, 2 * tig, valid);
-            b1 = mask_pair(b1, 8 + 2 * tig, valid);
-            b3 = mask_pair(b3, 8 + 2 * tig, valid);
-          }
+      for (int dn = 0; dn < 16; dn += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(st + (2 + (dn >> 3)) * kBox + sw128(rr + ((mi & 1) << 3), (dn & 7) + (mi >> 1)),
+                  b0, b1, b2, b3);
+        if (valid < 16) {
+          b0 = mask_pair(b0, 2 * tig, valid);
+          b2 = mask_pair(b2, 2 * tig, valid);
+          b1 = mask_pair(b1, 8 + 2 * tig, valid);
+          b3 = mask_pair(b3, 8 + 2 * tig, valid);
+        }
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            mma_bf16(o[mt][dn], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
-            mma_bf16(o[mt][dn + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
-          }
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16(o[mt][dn], pa[mt], b0, b1);
+          mma_bf16(o[mt][dn + 1], pa[mt], b2, b3);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (p + C::kStages < npages) issue_page(p + C::kStages);
     }
     if (!ok) break;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(uempty_bar(slot));  // query slot free for the producer
+    page_cnt += npages;
 
-    // merge the four warps' states: [warp][row] m, l and [warp][row][128] o
-    constexpr int ROWS = C::kRows;
-    consumer_sync();  // the merge buffer is free (previous unit done with it)
+    // finish: row sums across the quad, then output or split partials
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       float l0 = l_run[mt][0], l1 = l_run[mt][1];
@@ -370,100 +331,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int ra = mt * 16 + gid, rb = ra + 8;
-      if (tig == 0) {
-        mw[warp * ROWS + ra] = m_run[mt][0];
-        mw[warp * ROWS + rb] = m_run[mt][1];
-        lw[warp * ROWS + ra] = l0;
-        lw[warp * ROWS + rb] = l1;
-      }
+      const int ra = mt * 16 + gid, rb = ra + 8;  // head rows inside the KV head's group
+      if (un.nsplit == 1) {
+        const int q0 = a.qsl[un.r];
+        uint16_t* orow = a.out + (int64_t)q0 * a.out_stride + (int64_t)un.g * G * kHeadSize;
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
-      for (int dn = 0; dn < 16; ++dn) {
-        const int col = dn * 8 + tig * 2;
-        *reinterpret_cast<float2*>(ow + (warp * ROWS + ra) * kHeadSize + col) =
-            make_float2(o[mt][dn][0], o[mt][dn][1]);
-        *reinterpret_cast<float2*>(ow + (warp * ROWS + rb) * kHeadSize + col) =
-            make_float2(o[mt][dn][2], o[mt][dn][3]);
-      }
-    }
-    consumer_sync();
-
-    const int d = tid;  // one output column per consumer thread
-    const int q0 = a.qsl[un.r];
-    uint16_t* out_row = a.out + (int64_t)q0 * a.out_stride + (int64_t)un.g * G * kHeadSize + d;
-    if (un.nsplit == 1) {
-      for (int row = 0; row < G; ++row) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mw[w * ROWS + row]);
-        float acc = 0.f, lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-          const float f = fast_exp2(mw[w * ROWS + row] - M);
-          acc += f * ow[(w * ROWS + row) * kHeadSize + d];
-          lsum += f * lw[w * ROWS + row];
+        for (int dn = 0; dn < 16; ++dn) {
+          const int col = dn * 8 + tig * 2;
+          if (ra < G)
+            *reinterpret_cast<uint32_t*>(orow + ra * kHeadSize + col) =
+                pack_bf16(o[mt][dn][0] * i0, o[mt][dn][1] * i0);
+          if (rb < G)
+            *reinterpret_cast<uint32_t*>(orow + rb * kHeadSize + col) =
+                pack_bf16(o[mt][dn][2] * i1, o[mt][dn][3] * i1);
         }
-        out_row[row * kHeadSize] = __bfloat16_as_ushort(__float2bfloat16_rn(acc / lsum));
-      }
-      continue;
-    }
-    for (int row = 0; row < G; ++row) {
-      float M = -INFINITY;
+      } else {
+        const int64_t pra = (int64_t)un.part * G + ra, prb = (int64_t)un.part * G + rb;
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mw[w * ROWS + row]);
-      float acc = 0.f, lsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float f = fast_exp2(mw[w * ROWS + row] - M);
-        acc += f * ow[(w * ROWS + row) * kHeadSize + d];
-        lsum += f * lw[w * ROWS + row];
+        for (int dn = 0; dn < 16; ++dn) {
+          const int col = dn * 8 + tig * 2;
+          if (ra < G)
+            *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
+                make_float2(o[mt][dn][0], o[mt][dn][1]);
+          if (rb < G)
+            *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
+                make_float2(o[mt][dn][2], o[mt][dn][3]);
+        }
+        if (tig == 0) {
+          if (ra < G)
+            *reinterpret_cast<float2*>(ws.part_ml + pra * 2) = make_float2(m_run[mt][0], l0);
+          if (rb < G)
+            *reinterpret_cast<float2*>(ws.part_ml + prb * 2) = make_float2(m_run[mt][1], l1);
+        }
       }
-      const int64_t prow = (int64_t)un.part * G + row;
-      ws.part_o[prow * kHeadSize + d] = acc;
-      if (d == 0) {
-        ws.part_ml[prow * 2] = M;
-        ws.part_ml[prow * 2 + 1] = lsum;
-      }
-    }
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) *s_ticket = atomicAdd(&ws.counters[(int64_t)un.r * a.hkv + un.g], 1);
-    consumer_sync();
-    if (*s_ticket != un.nsplit - 1) continue;
-
-    // the last split to finish merges all splits of (r, g)
-    __threadfence();
-    const int first = un.part - un.split, ns = un.nsplit;
-    float* wm = mw;              // [ns][G] weights
-    float* wl = mw + ns * G;     // [G] 1 / total sum
-    consumer_sync();             // everyone is past the reads of mw/lw/ow above
-    for (int i = tid; i < ns * G; i += kConsumers * 32)
-      wm[i] = __ldcg(ws.part_ml + ((int64_t)first * G + i) * 2);
-    consumer_sync();
-    if (tid < G) {
-      float M = -INFINITY;
-      for (int s = 0; s < ns; ++s) M = fmaxf(M, wm[s * G + tid]);
-      float lsum = 0.f;
-      for (int s = 0; s < ns; ++s) {
-        const float f = fast_exp2(wm[s * G + tid] - M);
-        lsum += f * __ldcg(ws.part_ml + ((int64_t)(first + s) * G + tid) * 2 + 1);
-        wm[s * G + tid] = f;
-      }
-      wl[tid] = 1.f / lsum;
-    }
-    consumer_sync();
-    for (int row = 0; row < G; ++row) {
-      float acc = 0.f;
-      const float* po = ws.part_o + ((int64_t)first * G + row) * kHeadSize + d;
-#pragma unroll 8
-      for (int s = 0; s < ns; ++s) acc += wm[s * G + row] * __ldcg(po + (int64_t)s * G * kHeadSize);
-      out_row[row * kHeadSize] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * wl[row]));
     }
   }
 }
 
+// Merge of split results: one (split pair, query head) per CTA iteration,
+// one output column per thread; the weights exp2(m_s - max) renormalise the
+// splits' running sums and outputs (the same online-softmax identity the
+// decode loop uses between pages).
+__global__ void __launch_bounds__(kHeadSize) combine_kernel(AttnArgs a, Workspace ws) {
+  const int G = a.hq / a.hkv;
+  const int n_items = ws.hdr->n_pairs * G;
+  const int d = threadIdx.x;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const SplitPair sp = ws.pairs[item / G];
+    const int row = item % G;
+    const float* ml = ws.part_ml + ((int64_t)sp.first * G + row) * 2;
+    const float* po = ws.part_o + ((int64_t)sp.first * G + row) * kHeadSize + d;
+    float M = -INFINITY;
+    for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, __ldcg(ml + (int64_t)s * G * 2));
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < sp.nsplit; ++s) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + (int64_t)s * G * 2));
+      const float f = fast_exp2(v.x - M);
+      lsum += f * v.y;
+      acc += f * __ldcg(po + (int64_t)s * G * kHeadSize);
+    }
+    const int q0 = a.qsl[sp.r];
+    a.out[(int64_t)q0 * a.out_stride + (int64_t)(sp.g * G + row) * kHeadSize + d] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc / lsum));
+  }
+}
+
 template <int MT>
-cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int grid, cudaStream_t st) {
+cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>,
@@ -478,20 +414,25 @@ cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int grid, cudaStre
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  decode_kernel<MT><<<grid, kThreads, Cfg<MT>::kSmem, st>>>(tq, tk, tv, a, ws);
+  decode_kernel<MT><<<sms, kThreads, Cfg<MT>::kSmem, st>>>(tq, tk, tv, a, ws);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_grid(int group, int sms) {
+int decode_workers(int group, int sms) {
   (void)group;
-  return sms;  // one CTA per SM
+  return sms * kWarps;
 }
 
-cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int grid, cudaStream_t st) {
+cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   const int G = a.hq / a.hkv;
-  return G <= 16 ? launch_mt<1>(a, ws, grid, st) : launch_mt<2>(a, ws, grid, st);
+  return G <= 16 ? launch_mt<1>(a, ws, sms, st) : launch_mt<2>(a, ws, sms, st);
+}
+
+cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
+  combine_kernel<<<sms * 8, kHeadSize, 0, st>>>(a, ws);
+  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -15,7 +15,7 @@ constexpr int kBlockSize = 16;   // tokens per cache block (page)
 constexpr int kMaxGroup = 32;    // query heads per KV head handled by one decode unit
 constexpr int kDecTile = 64;     // tokens per decode pipeline stage (4 pages)
 constexpr int kMinChunk = 256;   // smallest split-KV chunk (tokens)
-constexpr int kMaxChunk = 1024;  // largest split-KV chunk (tokens)
+constexpr int kMaxChunk = 2048;  // largest split-KV chunk (tokens)
 constexpr int kMaxBtWidth = 32768;  // block-table entries per request (524,288 keys) at most
 constexpr int kPreTileQ = 128;   // query rows per prefill tile
 
@@ -30,6 +30,12 @@ struct __align__(16) PreEntry {
   int r, qt, nkv, pad;
 };
 
+// A (request, KV head) whose keys were split over several decode units: its
+// partial results live in part slots first .. first + nsplit - 1.
+struct __align__(16) SplitPair {
+  int r, g, first, nsplit;
+};
+
 // Header of the step plan, written by the plan kernel each call.
 struct PlanHeader {
   int n_dec_units;
@@ -37,7 +43,8 @@ struct PlanHeader {
   int dec_counter;  // dynamic scheduler cursors, reset by the plan kernel
   int pre_counter;
   int chunk;
-  int pad[11];
+  int n_pairs;      // split pairs to merge
+  int pad[10];
 };
 
 // Device pointers into the per-device workspace.
@@ -45,7 +52,7 @@ struct Workspace {
   PlanHeader* hdr;
   DecUnit* units;
   PreEntry* pre;
-  int* counters;     // [max_reqs * hkv] split-arrival tickets
+  SplitPair* pairs;  // [max_reqs * hkv] split pairs (n_pairs used)
   float* part_ml;    // [part_slots * group][2]: running max (log2 domain) and sum
   float* part_o;     // [part_slots * group][128]: unnormalised output
   int* err;          // device error word
@@ -94,8 +101,11 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads, in
 bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv);
 
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st);
-cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int grid, cudaStream_t st);
-int decode_grid(int group, int sms);
+cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
+cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
+// Independent decode workers (warp groups) the decode grid runs for a head
+// grouping; the plan sizes its split chunks for this many.
+int decode_workers(int group, int sms);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
 }  // namespace pkv

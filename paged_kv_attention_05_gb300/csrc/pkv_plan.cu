@@ -52,6 +52,17 @@ __device__ int block_exclusive_scan(int x, int* total, int* smem32) {
   return res;
 }
 
+// Last index i in [0, kPlanThreads) with off[i] <= x: the request that owns
+// entry x when off[] holds the exclusive prefix sums of per-request counts.
+__device__ __forceinline__ int find_owner(const int* off, int x) {
+  int lo = 0, hi = kPlanThreads - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 struct ReqInfo {
   int kind;  // 0 nothing, 1 decode, 2 prefill
   int n, L, q0;
@@ -103,54 +114,55 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   }
   __syncthreads();
   const long long total_keys = red[0];
-  // aim for about four units per decode CTA, in whole 64-key tiles
+  // aim for about four units per decode worker (dec_grid = workers), in
+  // whole 64-key tiles, at most kMaxChunk keys; at least kMinChunk keys, and
+  // at least 32 keys per query head of the group, so that a split's partial
+  // result (G rows of 130 fp32) stays small next to the K/V bytes it read
   long long want = (total_keys * a.hkv + (long long)dec_grid * 4 - 1) / ((long long)dec_grid * 4);
   want = (want + kDecTile - 1) / kDecTile * kDecTile;
-  const int chunk = (int)(want < kMinChunk ? kMinChunk : (want > kMaxChunk ? kMaxChunk : want));
+  const int G = a.hq / a.hkv;
+  const int lo_chunk = max(kMinChunk, 32 * G);
+  const int chunk = (int)(want < lo_chunk ? lo_chunk : (want > kMaxChunk ? kMaxChunk : want));
 
   // pass 2: per-request offsets (block scans), then the work lists written
   // cooperatively: consecutive threads write consecutive entries, each
   // finding its request by binary search over the chunk's offsets
-  __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1];
+  __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1], s_off_q[kPlanThreads + 1];
   __shared__ int s_off_p[kPlanThreads], s_len[kPlanThreads], s_n[kPlanThreads];
-  int unit_carry = 0, part_carry = 0, pre_carry = 0;
+  int unit_carry = 0, part_carry = 0, pre_carry = 0, pair_carry = 0;
   for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
     if (r < a.num_reqs) ri = classify(a, r);
     if (ri.bad) atomicOr(ws.err, ri.bad);
-    int units = 0, parts = 0, tiles = 0;
+    int units = 0, parts = 0, tiles = 0, pairs = 0;
     if (ri.kind == 1) {
       const int nsplit = (ri.L + chunk - 1) / chunk;
       units = nsplit * a.hkv;
       parts = nsplit > 1 ? units : 0;
+      pairs = nsplit > 1 ? a.hkv : 0;
     } else if (ri.kind == 2) {
       tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
     }
-    int tot_u, tot_p, tot_t;
+    int tot_u, tot_p, tot_t, tot_q;
     const int off_u = block_exclusive_scan(units, &tot_u, smem32);
     const int off_p = block_exclusive_scan(parts, &tot_p, smem32);
     const int off_t = block_exclusive_scan(tiles, &tot_t, smem32);
+    const int off_q = block_exclusive_scan(pairs, &tot_q, smem32);
     s_off_u[tid] = off_u;
     s_off_t[tid] = off_t;
+    s_off_q[tid] = off_q;
     s_off_p[tid] = part_carry + off_p;
     s_len[tid] = ri.L;
     s_n[tid] = ri.n;
     if (tid == 0) {
       s_off_u[kPlanThreads] = tot_u;
       s_off_t[kPlanThreads] = tot_t;
+      s_off_q[kPlanThreads] = tot_q;
     }
     __syncthreads();
-    const int nreq = min(kPlanThreads, a.num_reqs - base);
-    // split tickets start at zero (every request of the chunk, every KV head)
-    for (int i = tid; i < nreq * a.hkv; i += kPlanThreads)
-      ws.counters[(int64_t)base * a.hkv + i] = 0;
     for (int i = tid; i < tot_u; i += kPlanThreads) {
-      int lo = 0, hi = kPlanThreads - 1;  // last request with s_off_u <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_off_u[mid] <= i) lo = mid; else hi = mid - 1;
-      }
+      const int lo = find_owner(s_off_u, i);
       const int rem = i - s_off_u[lo];
       const int L = s_len[lo];
       const int nsplit = (L + chunk - 1) / chunk;
@@ -163,12 +175,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
                          nsplit > 1 ? s_off_p[lo] + g * nsplit + sp : -1, 0);
     }
+    for (int i = tid; i < tot_q; i += kPlanThreads) {
+      const int lo = find_owner(s_off_q, i);
+      const int g = i - s_off_q[lo];
+      const int nsplit = (s_len[lo] + chunk - 1) / chunk;
+      const int64_t idx = (int64_t)pair_carry + i;
+      if (idx >= ws.max_pairs) break;
+      *reinterpret_cast<int4*>(ws.pairs + idx) =
+          make_int4(base + lo, g, s_off_p[lo] + g * nsplit, nsplit);
+    }
     for (int i = tid; i < tot_t; i += kPlanThreads) {
-      int lo = 0, hi = kPlanThreads - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_off_t[mid] <= i) lo = mid; else hi = mid - 1;
-      }
+      const int lo = find_owner(s_off_t, i);
       // a request's query tiles from the last (most keys) to the first, so
       // that the persistent prefill grid starts with the longest items
       const int n = s_n[lo], ctx = s_len[lo] - n;
@@ -182,6 +199,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     unit_carry += tot_u;
     part_carry += tot_p;
     pre_carry += tot_t;
+    pair_carry += tot_q;
     __syncthreads();  // the chunk's offsets are reused by the next chunk
   }
   if (tid == 0) {
@@ -190,6 +208,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     ws.hdr->dec_counter = 0;
     ws.hdr->pre_counter = 0;
     ws.hdr->chunk = chunk;
+    ws.hdr->n_pairs = (int)min((int64_t)pair_carry, ws.max_pairs);
   }
 }
 
