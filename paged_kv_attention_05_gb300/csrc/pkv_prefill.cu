@@ -12,28 +12,32 @@
 // Cache", "One Path Covers MHA, GQA, and MQA": query head h reads KV head
 // h / (Hq / Hkv).
 //
-// GB300 design.  One work item = (request, 128-row query tile, query head);
-// a persistent grid (one CTA per SM, 512 TMEM columns each) takes items from
-// an atomic cursor in the order the plan wrote them.  Inside a CTA:
-//   warp 0      TMA producer: the Q tile once per item; per 128-key tile,
-//               the 8 K pages and 8 V pages (each page a 16-slot x 64-dim
-//               box, two per page for the two 64-dim halves, 128-byte
-//               swizzle) into a 2-stage ring; in the last tile of a request
-//               it zero-fills V rows past seq_len so that no stale value
-//               (NaN) reaches the P.V product;
-//   warp 1      allocates TMEM and issues the MMAs from one thread:
-//               S = Q K^T (M = N = 128, K = 128 in 8 steps of 16) into one of
-//               two TMEM score buffers, then O += P V (P from shared memory,
-//               V read MN-major) into the TMEM output buffer; tcgen05.commit
-//               signals the mbarriers;
-//   warps 4-7   softmax, one query row per thread (TMEM lane = row): load
-//               the 128 scores of the row, causal/length mask, running max in
-//               the log2 domain, exp2, row sum, P as bf16 into shared memory
-//               (the operand layout of the next MMA).  The output in TMEM is
-//               rescaled only when a row's max grows by more than 2^8, which
-//               is exact (softmax is shift invariant) and rare; the final
-//               division by the row sum happens in the epilogue, which writes
-//               the bf16 rows of the item straight to global memory.
+// GB300 design.  A work item is a 128-row query tile of one request for two
+// query heads of the same KV head (one head when Hq / Hkv is odd): tiles "a"
+// and "b" share every K/V tile.  A persistent grid (one CTA per SM, all 512
+// TMEM columns) takes items from an atomic cursor, longest first.  Roles:
+//   warp 0      producer: publishes the item in a two-slot ring, loads the two
+//               Q tiles by TMA as soon as the previous item's last S = Q K^T
+//               has consumed them, then the K and V tiles of 128 keys (8 pages
+//               each, one 16-slot x 64-dim box per page and half, 128-byte
+//               swizzle) into a 2-stage ring, K and V released separately; in
+//               a request's last tile it zero-fills the V rows of keys past
+//               seq_len so that no stale value (NaN) reaches P.V;
+//   warp 1      allocates TMEM and issues every MMA from one thread, in the
+//               order S_a(0) S_b(0) | PV_a(j) S_a(j+1) PV_b(j) S_b(j+1) ...:
+//               S into TMEM, P taken from TMEM (the scores' columns,
+//               overwritten with bf16 probabilities) and V from shared memory
+//               (MN-major), O accumulating in TMEM; tcgen05.commit drives the
+//               mbarriers.  Because one thread's MMAs complete in order, S(j+1)
+//               being ready also means PV(j) is done;
+//   warps 2-5   softmax for tile a, warps 6-9 for tile b, one query row per
+//               thread (TMEM lane = 32 * (warp % 4) + lane = row): scores -> causal/length mask (only
+//               on tiles that cross the diagonal) -> running max in the log2
+//               domain -> exp2 -> row sum -> bf16 P back into TMEM.  The two
+//               warpgroups alternate with the tensor pipe.  O is rescaled in
+//               TMEM only when a row's max grows by more than 2^8 (exact,
+//               rare).  At the end of an item the same warps divide by the row
+//               sum and write the bf16 rows to global memory.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // PKV_DEV_ERR_TIMEOUT, stops issuing work, frees its TMEM and returns.
 #include "pkv_device.cuh"
@@ -43,28 +47,45 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;                     // 10 warps
 constexpr int kStages = 2;
 constexpr int kTileK = 128;                       // keys per KV tile
 constexpr int kHalfBytes = 128 * 128;             // 128 rows x 64 bf16
-constexpr int kTileBytes = 2 * kHalfBytes;        // Q, K, V or P tile: 32 KB
+constexpr int kTileBytes = 2 * kHalfBytes;        // a Q, K or V tile: 32 KB
 constexpr int kPageBoxBytes = 16 * 128;           // one 16-slot x 64-dim box
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffQ = 0;                          // Q_a | Q_b
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
-// barriers: q_full, k_full[2], v_full[2], v_tma[2], kv_empty[2], s_full[2],
-// p_full, o_done  (15 x 8 bytes), then the TMEM address and control words
-constexpr int kNumBars = 15;
-constexpr int kOffCtl = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffCtl + 64 + 1024;  // + alignment slack
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+enum {
+  B_QF = 0,   // [2] Q tile loaded
+  B_QE = 2,   // [2] Q tile consumed by the item's last S
+  B_KF = 4,   // [2] K stage loaded
+  B_KE = 6,   // [2] K stage free
+  B_VF = 8,   // [2] V stage ready
+  B_VT = 10,  // [2] V stage loaded (tail tiles: before the zero fill)
+  B_VE = 12,  // [2] V stage free
+  B_SF = 14,  // [2] S_x ready
+  B_PF = 16,  // [2] P_x written
+  B_OF = 18,  // [2] O_x final for the item
+  B_OE = 20,  // [2] O_x read by the epilogue
+  B_IF = 22,  // [2] item slot published
+  B_IE = 24,  // [2] item slot released
+  kNumBars = 26
+};
+constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 item slots
+constexpr int kOffCtl = kOffItems + 2 * 48;        // TMEM address, abort flag
+constexpr int kSmemBytes = kOffCtl + 16 + 1024;    // + alignment slack
 
-enum { B_Q = 0, B_K = 1, B_V = 3, B_VT = 5, B_EMPTY = 7, B_S = 9, B_P = 11, B_O = 12 };
+struct Item {
+  int r, qt, ha, hb;  // hb < 0: single-tile item
+  int g, q0, n, L;
+  int ctx, nkv, pad0, pad1;
+};
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -87,20 +108,30 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = N = 128.
 __host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
-  return (1u << 4)                       // D format f32
-         | (1u << 7)                     // A format bf16
-         | (1u << 10)                    // B format bf16
+  return (1u << 4)                         // D format f32
+         | (1u << 7)                       // A format bf16
+         | (1u << 10)                      // B format bf16
          | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
-         | ((128u >> 3) << 17)           // N
-         | ((128u >> 4) << 24);          // M
+         | ((128u >> 3) << 17)             // N
+         | ((128u >> 4) << 24);            // M
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t acc) {
+// D (TMEM) (+)= A (shared) * B (shared)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D (TMEM) (+)= A (TMEM) * B (shared)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                       uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -132,6 +163,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])                              \
       : "memory")
 
+#define PKV_ST32U(taddr, v)                                                                    \
+  asm volatile(                                                                                \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"  \
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),        \
+      "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),         \
+      "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),     \
+      "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),     \
+      "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                              \
+      : "memory")
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
@@ -139,13 +181,7 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-struct Item {
-  int r, qt, h, g;
-  int q0, n, L, ctx;
-  int nkv;
-};
-
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   extern __shared__ uint8_t smem_raw[];
@@ -155,23 +191,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + kOffBar;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + kOffCtl);
-  // ctl[0] = TMEM base address, ctl[1] = abort flag, ctl[2] = current item
-  volatile int* abort = ctl + 1;
+  volatile int* abort = ctl + 1;  // ctl[0] = TMEM base address
+  Item* items = reinterpret_cast<Item*>(smem + kOffItems);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.hq / a.hkv;
+  const bool pairs = (G % 2) == 0;  // two heads of one KV head per item
+  const int per_entry = pairs ? a.hq / 2 : a.hq;
 
   if (tid == 0) {
-    mbar_init(bar(B_Q), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_K + s), 1);
-      mbar_init(bar(B_V + s), 1);
-      mbar_init(bar(B_VT + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1);
-      mbar_init(bar(B_S + s), 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(B_PF + x), 128);
+      mbar_init(bar(B_OE + x), 128);
+      mbar_init(bar(B_IE + x), 1 + 8);  // MMA thread + one lane of each softmax warp
     }
-    mbar_init(bar(B_P), 128);
-    mbar_init(bar(B_O), 1);
     ctl[1] = 0;
     fence_barrier_init();
   }
@@ -185,249 +219,315 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)ctl[0];
-  const uint32_t tm_s0 = tmem, tm_o = tmem + 256;
+  const int n_items = ws.hdr->n_pre_entries * per_entry;
 
-  const int n_items = ws.hdr->n_pre_entries * a.hq;
-  uint32_t tile_base = 0;  // KV tiles processed by this CTA so far (all items)
-  uint32_t item_cnt = 0;
-  uint32_t vt_uses[kStages] = {0, 0};
-
-  for (;;) {
-    if (tid == 0) ctl[2] = atomicAdd(&ws.hdr->pre_counter, 1);
-    __syncthreads();
-    const int w = ctl[2];
-    if (w >= n_items || *abort) break;
-    Item it;
-    {
-      const PreEntry e = ws.pre[w / a.hq];
-      it.r = e.r;
-      it.qt = e.qt;
-      it.h = w % a.hq;
-      it.g = it.h / G;
-      it.nkv = e.nkv;
-      it.q0 = a.qsl[it.r];
-      it.n = a.qsl[it.r + 1] - it.q0;
-      it.L = a.seq_lens[it.r];
-      it.ctx = it.L - it.n;
-    }
-    const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
-
-    if (warp == 0) {
-      // ---------------- TMA producer ----------------
-      if (lane == 0) {
-        mbar_expect_tx(bar(B_Q), kTileBytes);
-        const int row0 = it.q0 + it.qt * kPreTileQ;
-        tma_load_3d(sbase + kOffQ, &tm_q, bar(B_Q), 0, it.h, row0);
-        tma_load_3d(sbase + kOffQ + kHalfBytes, &tm_q, bar(B_Q), 64, it.h, row0);
-      }
-      for (int j = 0; j < it.nkv; ++j) {
-        const uint32_t c = tile_base + j;
-        const int s = c % kStages;
-        if (c >= (uint32_t)kStages) {
-          if (!mbar_wait_warp(bar(B_EMPTY + s), ((c / kStages) - 1) & 1, abort, ws.err)) break;
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    uint32_t tile_cnt = 0, vt_uses[kStages] = {0, 0}, qx_cnt[2] = {0, 0};
+    for (uint32_t it_cnt = 0;; ++it_cnt) {
+      const int slot = it_cnt & 1;
+      int w = 0;
+      if (lane == 0) w = atomicAdd(&ws.hdr->pre_counter, 1);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (it_cnt >= 2 &&
+          !mbar_wait_warp(bar(B_IE + slot), ((it_cnt >> 1) - 1) & 1, abort, ws.err))
+        break;
+      if (w >= n_items || *abort) {
+        if (lane == 0) {
+          items[slot].r = -1;
+          mbar_arrive(bar(B_IF + slot));
         }
+        break;
+      }
+      Item it;
+      {
+        const PreEntry e = ws.pre[w / per_entry];
+        const int hp = w % per_entry;
+        it.r = e.r;
+        it.qt = e.qt;
+        it.nkv = e.nkv;
+        it.ha = pairs ? 2 * hp : hp;
+        it.hb = pairs ? 2 * hp + 1 : -1;
+        it.g = it.ha / G;
+        it.q0 = a.qsl[it.r];
+        it.n = a.qsl[it.r + 1] - it.q0;
+        it.L = a.seq_lens[it.r];
+        it.ctx = it.L - it.n;
+        it.pad0 = it.pad1 = 0;
+      }
+      if (lane == 0) {
+        items[slot] = it;
+        mbar_arrive(bar(B_IF + slot));
+      }
+      const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
+      const int row0 = it.q0 + it.qt * kPreTileQ;
+      // Q tiles, once the previous item's last S has read them
+      bool ok = true;
+      for (int x = 0; x < 2 && ok; ++x) {
+        const int h = x == 0 ? it.ha : it.hb;
+        if (h < 0) continue;
+        if (qx_cnt[x] > 0 &&
+            !mbar_wait_warp(bar(B_QE + x), (qx_cnt[x] - 1) & 1, abort, ws.err)) {
+          ok = false;
+          break;
+        }
+        qx_cnt[x]++;
+        if (lane == 0) {
+          const uint32_t qd = sbase + kOffQ + x * kTileBytes;
+          mbar_expect_tx(bar(B_QF + x), kTileBytes);
+          tma_load_3d(qd, &tm_q, bar(B_QF + x), 0, h, row0);
+          tma_load_3d(qd + kHalfBytes, &tm_q, bar(B_QF + x), 64, h, row0);
+        }
+      }
+      for (int j = 0; ok && j < it.nkv; ++j) {
+        const uint32_t c = tile_cnt++;
+        const int s = c % kStages;
         const int key0 = j * kTileK;
         const int pages = min(8, (it.L - key0 + 15) / 16);
         const bool tail = key0 + kTileK > it.L;
+        int blk = 0;  // lane p < pages holds the block id of page p
+        if (lane < pages) {
+          blk = __ldg(btrow + (key0 >> 4) + lane);
+          if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+            atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
+            blk = 0;
+          }
+        }
+        if (c >= (uint32_t)kStages &&
+            !mbar_wait_warp(bar(B_KE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
+          ok = false;
+          break;
+        }
         const uint32_t kdst = sbase + kOffK + s * kTileBytes;
+        if (lane == 0) mbar_expect_tx(bar(B_KF + s), pages * 2 * kPageBoxBytes);
+        __syncwarp();
+        if (lane < pages) {
+          tma_load_4d(kdst + lane * kPageBoxBytes, &tm_k, bar(B_KF + s), 0, it.g, 0, blk);
+          tma_load_4d(kdst + kHalfBytes + lane * kPageBoxBytes, &tm_k, bar(B_KF + s), 64, it.g,
+                      0, blk);
+        }
+        if (c >= (uint32_t)kStages &&
+            !mbar_wait_warp(bar(B_VE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
+          ok = false;
+          break;
+        }
         const uint32_t vdst = sbase + kOffV + s * kTileBytes;
-        if (lane == 0) {
-          mbar_expect_tx(bar(B_K + s), pages * 2 * kPageBoxBytes);
-          for (int p = 0; p < pages; ++p) {
-            int blk = __ldg(btrow + (key0 >> 4) + p);
-            if (blk < 0 || (int64_t)blk >= a.num_blocks) {
-              atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
-              blk = 0;
-            }
-            tma_load_4d(kdst + p * kPageBoxBytes, &tm_k, bar(B_K + s), 0, it.g, 0, blk);
-            tma_load_4d(kdst + kHalfBytes + p * kPageBoxBytes, &tm_k, bar(B_K + s), 64, it.g, 0,
-                        blk);
-          }
-          const uint32_t vbar = tail ? bar(B_VT + s) : bar(B_V + s);
-          mbar_expect_tx(vbar, pages * 2 * kPageBoxBytes);
-          for (int p = 0; p < pages; ++p) {
-            int blk = __ldg(btrow + (key0 >> 4) + p);
-            if (blk < 0 || (int64_t)blk >= a.num_blocks) blk = 0;
-            tma_load_4d(vdst + p * kPageBoxBytes, &tm_v, vbar, 0, it.g, 0, blk);
-            tma_load_4d(vdst + kHalfBytes + p * kPageBoxBytes, &tm_v, vbar, 64, it.g, 0, blk);
-          }
+        const uint32_t vbar = tail ? bar(B_VT + s) : bar(B_VF + s);
+        if (lane == 0) mbar_expect_tx(vbar, pages * 2 * kPageBoxBytes);
+        __syncwarp();
+        if (lane < pages) {
+          tma_load_4d(vdst + lane * kPageBoxBytes, &tm_v, vbar, 0, it.g, 0, blk);
+          tma_load_4d(vdst + kHalfBytes + lane * kPageBoxBytes, &tm_v, vbar, 64, it.g, 0, blk);
         }
         if (tail) {
           // wait for the V boxes, zero the rows of keys >= seq_len, publish
-          const bool ok = mbar_wait_warp(bar(B_VT + s), vt_uses[s] & 1, abort, ws.err);
+          ok = mbar_wait_warp(bar(B_VT + s), vt_uses[s] & 1, abort, ws.err);
           vt_uses[s]++;
           if (!ok) break;
-          const int z0 = it.L - key0;  // first key row to clear
-          const int chunks = (kTileK - z0) * 16;
+          const int z0 = it.L - key0;
           uint8_t* v = smem + kOffV + s * kTileBytes;
-          for (int i = lane; i < chunks; i += 32) {
+          for (int i = lane; i < (kTileK - z0) * 16; i += 32) {
             const int row = z0 + (i >> 4), within = i & 15;
-            const int half = within >> 3, ch = within & 7;
-            *reinterpret_cast<uint4*>(v + half * kHalfBytes + row * 128 + ch * 16) =
-                make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(v + (within >> 3) * kHalfBytes + row * 128 +
+                                      (within & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_V + s));
+          if (lane == 0) mbar_arrive(bar(B_VF + s));
         }
       }
-    } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
-        const uint32_t id_s = idesc_bf16(false), id_o = idesc_bf16(true);
-        const uint32_t qa = sbase + kOffQ;
-        auto issue_s = [&](uint32_t c) -> bool {
-          const int s = c % kStages;
-          if (!mbar_wait(bar(B_K + s), (c / kStages) & 1, abort, ws.err)) return false;
-          tc_fence_after();
-          const uint32_t kb = sbase + kOffK + s * kTileBytes;
-          const uint32_t d = tm_s0 + (c & 1) * 128;
+      if (!ok) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(false), id_o = idesc_bf16(true);
+      uint32_t tile_cnt = 0, s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
+      // S_x(c) = Q_x K_c^T
+      auto issue_s = [&](int x, uint32_t c) {
+        const uint32_t qa = sbase + kOffQ + x * kTileBytes;
+        const uint32_t kb = sbase + kOffK + (c % kStages) * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_bf16(d, sdesc(qa + off, 16), sdesc(kb + off, 16), id_s, kk > 0);
-          }
-          mma_commit(bar(B_S + (c & 1)));
-          return true;
-        };
-        bool ok = mbar_wait(bar(B_Q), item_cnt & 1, abort, ws.err);
-        if (ok) ok = issue_s(tile_base);
-        for (int j = 0; ok && j < it.nkv; ++j) {
-          const uint32_t c = tile_base + j;
-          const int s = c % kStages;
-          if (j + 1 < it.nkv && !issue_s(c + 1)) break;
-          if (!mbar_wait(bar(B_P), c & 1, abort, ws.err)) break;
-          if (!mbar_wait(bar(B_V + s), (c / kStages) & 1, abort, ws.err)) break;
-          tc_fence_after();
-          const uint32_t pa = sbase + kOffP, vb = sbase + kOffV + s * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            const uint32_t boff = kk * 16 * 128;  // 16 key rows per step
-            mma_bf16(tm_o, sdesc(pa + aoff, 16), sdesc(vb + boff, kHalfBytes), id_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(B_O));
-          mma_commit(bar(B_EMPTY + s));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + x * 128, sdesc(qa + off, 16), sdesc(kb + off, 16), id_s, kk > 0);
         }
+        mma_commit(bar(B_SF + x));
+        s_cnt[x]++;
+      };
+      // O_x (+)= P_x V_c  (P_x: bf16 pairs in the first 64 columns of S_x)
+      auto issue_pv = [&](int x, uint32_t c, bool acc) {
+        const uint32_t vb = sbase + kOffV + (c % kStages) * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8,
+                 sdesc(vb + kk * 16 * 128, kHalfBytes), id_o, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      for (uint32_t it_cnt = 0; ok; ++it_cnt) {
+        const int slot = it_cnt & 1;
+        if (!mbar_wait(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+        const Item it = items[slot];
+        mbar_arrive(bar(B_IE + slot));
+        if (it.r < 0) break;
+        const int nx = it.hb >= 0 ? 2 : 1;
+        for (int x = 0; x < nx && ok; ++x)
+          ok = mbar_wait(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
+        const uint32_t c0 = tile_cnt;
+        if (!ok || !mbar_wait(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
+        tc_fence_after();
+        for (int x = 0; x < nx; ++x) issue_s(x, c0);
+        mma_commit(bar(B_KE + c0 % kStages));
+        if (it.nkv == 1)
+          for (int x = 0; x < nx; ++x) mma_commit(bar(B_QE + x));
+        for (int j = 0; j < it.nkv && ok; ++j) {
+          const uint32_t c = c0 + j;
+          const bool more = j + 1 < it.nkv;
+          if (!mbar_wait(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
+            ok = false;
+            break;
+          }
+          for (int x = 0; x < nx; ++x) {
+            if (!mbar_wait(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
+                (j == 0 && o_cnt[x] > 0 &&
+                 !mbar_wait(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err)) ||
+                (more && x == 0 &&
+                 !mbar_wait(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1, abort,
+                            ws.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(x, c, j > 0);
+            if (more) issue_s(x, c + 1);
+          }
+          if (!ok) break;
+          mma_commit(bar(B_VE + c % kStages));
+          if (more) {
+            mma_commit(bar(B_KE + (c + 1) % kStages));
+            if (j + 2 == it.nkv)
+              for (int x = 0; x < nx; ++x) mma_commit(bar(B_QE + x));
+          }
+        }
+        if (!ok) break;
+        for (int x = 0; x < nx; ++x) {
+          mma_commit(bar(B_OF + x));
+          o_cnt[x]++;
+        }
+        tile_cnt += it.nkv;
       }
+    }
+    __syncwarp();
+  } else {
+    // ------------------- softmax + epilogue, one row per thread -------------------
+    const int x = (warp - 2) >> 2;           // 0: tile a (warps 2-5), 1: tile b (warps 6-9)
+    const int row = (warp & 3) * 32 + lane;  // == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + x * 128 + lane_off, t_o = tmem + 256 + x * 128 + lane_off;
+    const float sl2 = a.scale * kLog2e;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    for (uint32_t it_cnt = 0;; ++it_cnt) {
+      const int slot = it_cnt & 1;
+      if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+      const Item it = items[slot];
       __syncwarp();
-    } else if (warp >= 4) {
-      // ---------------- softmax + epilogue, one row per thread ----------------
-      const int row = tid - 128;  // == 32 * (warp % 4) + lane == TMEM lane
-      const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+      if (lane == 0) mbar_arrive(bar(B_IE + slot));
+      if (it.r < 0) break;
+      if (x == 1 && it.hb < 0) continue;  // single-tile item: warps of tile b idle
+      const int h = x == 0 ? it.ha : it.hb;
       const int qrow = it.qt * kPreTileQ + row;  // row inside the request
       const bool valid_row = qrow < it.n;
       const int qpos = valid_row ? it.ctx + qrow : 0;  // last visible key
-      const float sl2 = a.scale * kLog2e;
       float m_used = -INFINITY, l_sum = 0.f;
-      uint8_t* P = smem + kOffP;
       bool ok = true;
       for (int j = 0; j < it.nkv; ++j) {
-        const uint32_t c = tile_base + j;
-        if (!mbar_wait_warp(bar(B_S + (c & 1)), (c >> 1) & 1, abort, ws.err)) {
+        if (!mbar_wait_warp(bar(B_SF + x), s_cnt++ & 1, abort, ws.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         float sv[128];
-        const uint32_t sa = tm_s0 + (c & 1) * 128 + lane_off;
-        PKV_LD32(sa + 0, (sv + 0));
-        PKV_LD32(sa + 32, (sv + 32));
-        PKV_LD32(sa + 64, (sv + 64));
-        PKV_LD32(sa + 96, (sv + 96));
+        PKV_LD32(t_s + 0, (sv + 0));
+        PKV_LD32(t_s + 32, (sv + 32));
+        PKV_LD32(t_s + 64, (sv + 64));
+        PKV_LD32(t_s + 96, (sv + 96));
         tmem_wait_ld();
-        const int key0 = j * kTileK;
-        const int lim = qpos - key0;  // columns <= lim are visible
-        float mt = -INFINITY;
+        const int lim = qpos - j * kTileK;  // columns <= lim are visible
+        if (!__all_sync(0xffffffffu, lim >= kTileK - 1)) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          sv[i] = (i <= lim) ? sv[i] * sl2 : -INFINITY;
-          mt = fmaxf(mt, sv[i]);
+          for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
         }
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+        for (int i = 8; i < 128; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[i + k]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
         float alpha = 1.f;
-        bool resc = false;
-        if (mt > m_used + kRescaleThreshold) {
+        const bool resc = mt > m_used + kRescaleThreshold;
+        if (resc) {
           alpha = fast_exp2(m_used - mt);  // 0 on the first tile
-          resc = (j > 0);
           m_used = mt;
         }
-        float rs = 0.f;
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          sv[i] = fast_exp2(sv[i] - m_used);
-          rs += sv[i];
-        }
-        l_sum = l_sum * alpha + rs;
-        if (j > 0) {
-          // the previous P.V must be complete before P and O are touched
-          if (!mbar_wait_warp(bar(B_O), (c - 1) & 1, abort, ws.err)) {
-            ok = false;
-            break;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(fmaf(sv[hh * 64 + 2 * i], sl2, -m_used));
+            const float p1 = fast_exp2(fmaf(sv[hh * 64 + 2 * i + 1], sl2, -m_used));
+            rs[i & 3] += p0 + p1;
+            pk[i] = pack_bf16(p0, p1);
           }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, resc)) {
-            float ov[32];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              const uint32_t oa = tm_o + ch * 32 + lane_off;
-              PKV_LD32(oa, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-              PKV_ST32(oa, ov);
-            }
-            tmem_wait_st();
-          }
+          PKV_ST32U(t_s + hh * 32, pk);
         }
-        // P row (bf16) in the 128-byte swizzled K-major layout
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          uint4 pk;
-          pk.x = pack_bf16(sv[ch * 8 + 0], sv[ch * 8 + 1]);
-          pk.y = pack_bf16(sv[ch * 8 + 2], sv[ch * 8 + 3]);
-          pk.z = pack_bf16(sv[ch * 8 + 4], sv[ch * 8 + 5]);
-          pk.w = pack_bf16(sv[ch * 8 + 6], sv[ch * 8 + 7]);
-          const int half = ch >> 3, c8 = ch & 7;
-          *reinterpret_cast<uint4*>(P + half * kHalfBytes + row * 128 +
-                                    ((c8 ^ (row & 7)) << 4)) = pk;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(B_P));
-      }
-      if (ok) {
-        const uint32_t c_last = tile_base + it.nkv - 1;
-        if (mbar_wait_warp(bar(B_O), c_last & 1, abort, ws.err)) {
-          tc_fence_after();
-          const float inv = 1.f / l_sum;
-          uint16_t* orow = a.out + (int64_t)(it.q0 + qrow) * a.out_stride +
-                           (int64_t)it.h * kHeadSize;
+        l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // PV(j-1) is complete (S(j) is, and one thread's MMAs finish in order)
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             float ov[32];
-            PKV_LD32(tm_o + ch * 32 + lane_off, ov);
+            PKV_LD32(t_o + ch * 32, ov);
             tmem_wait_ld();
-            if (valid_row) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                uint4 pk;
-                pk.x = pack_bf16(ov[i + 0] * inv, ov[i + 1] * inv);
-                pk.y = pack_bf16(ov[i + 2] * inv, ov[i + 3] * inv);
-                pk.z = pack_bf16(ov[i + 4] * inv, ov[i + 5] * inv);
-                pk.w = pack_bf16(ov[i + 6] * inv, ov[i + 7] * inv);
-                *reinterpret_cast<uint4*>(orow + ch * 32 + i) = pk;
-              }
-            }
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            PKV_ST32(t_o + ch * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_PF + x));
+      }
+      if (!ok) break;
+      // epilogue: O / l in bf16 to the output rows
+      if (!mbar_wait_warp(bar(B_OF + x), o_cnt++ & 1, abort, ws.err)) break;
+      tc_fence_after();
+      const float inv = 1.f / l_sum;
+      uint16_t* orow = a.out + (int64_t)(it.q0 + qrow) * a.out_stride + (int64_t)h * kHeadSize;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float ov[32];
+        PKV_LD32(t_o + ch * 32, ov);
+        tmem_wait_ld();
+        if (valid_row) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16(ov[i + 0] * inv, ov[i + 1] * inv);
+            v.y = pack_bf16(ov[i + 2] * inv, ov[i + 3] * inv);
+            v.z = pack_bf16(ov[i + 4] * inv, ov[i + 5] * inv);
+            v.w = pack_bf16(ov[i + 6] * inv, ov[i + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + ch * 32 + i) = v;
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(B_OE + x));
     }
-    tile_base += it.nkv;
-    item_cnt++;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
 
   tc_fence_before();
