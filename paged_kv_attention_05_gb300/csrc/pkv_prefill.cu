@@ -181,7 +181,7 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   extern __shared__ uint8_t smem_raw[];
@@ -446,42 +446,56 @@ __global__ void __maxnreg__(200)
           break;
         }
         tc_fence_after();
-        float sv[128];
-        PKV_LD32(t_s + 0, (sv + 0));
-        PKV_LD32(t_s + 32, (sv + 32));
-        PKV_LD32(t_s + 64, (sv + 64));
-        PKV_LD32(t_s + 96, (sv + 96));
-        tmem_wait_ld();
         const int lim = qpos - j * kTileK;  // columns <= lim are visible
-        if (!__all_sync(0xffffffffu, lim >= kTileK - 1)) {
+        const bool masked = !__all_sync(0xffffffffu, lim >= kTileK - 1);
+        // pass 1: the row maximum, 32 columns at a time
+        float mt = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          PKV_LD32(t_s + ch * 32, v);
+          tmem_wait_ld();
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (ch * 32 + i <= lim) ? v[i] : -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], v[i + 16]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = fmaxf(v[i], v[i + 8]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = fmaxf(v[i], v[i + 4]);
+          mt = fmaxf(mt, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
         }
-        float mx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = sv[k];
-#pragma unroll
-        for (int i = 8; i < 128; i += 8)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[i + k]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        mt *= sl2;
         float alpha = 1.f;
         const bool resc = mt > m_used + kRescaleThreshold;
         if (resc) {
           alpha = fast_exp2(m_used - mt);  // 0 on the first tile
           m_used = mt;
         }
+        // pass 2: probabilities, row sum, bf16 P over the first 64 columns
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(sv[hh * 64 + 2 * i], sl2, -m_used));
-            const float p1 = fast_exp2(fmaf(sv[hh * 64 + 2 * i + 1], sl2, -m_used));
-            rs[i & 3] += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int ch = hh * 2 + c2;
+            float v[32];
+            PKV_LD32(t_s + ch * 32, v);
+            tmem_wait_ld();
+            if (masked) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = (ch * 32 + i <= lim) ? v[i] : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = fast_exp2(fmaf(v[2 * i], sl2, -m_used));
+              const float p1 = fast_exp2(fmaf(v[2 * i + 1], sl2, -m_used));
+              rs[i & 3] += p0 + p1;
+              pk[c2 * 16 + i] = pack_bf16(p0, p1);
+            }
           }
           PKV_ST32U(t_s + hh * 32, pk);
         }
