@@ -140,6 +140,41 @@ int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t n
                   float scale, void* out, int64_t out_row_stride, void* stream);
 
 /*
+ * pkv_attention_noalloc — pkv_attention for callers that cannot allocate
+ * device memory.  The pages this library follows have no counterpart to it.
+ *
+ * Some callers cannot call cudaMalloc: code running while a CUDA graph is
+ * being captured, services that fix their device-memory footprint at start-up,
+ * or hosts whose device memory is handed out by an allocator the library must
+ * not bypass.  pkv_attention grows its workspace with cudaMalloc on first
+ * use; this call computes the same result with the same kernels but keeps the
+ * scratch (step plan, work lists, split-KV partials) in one statically sized
+ * device array inside the library (32 MiB; every GPU that loads the library
+ * holds it until the process exits), and allocates nothing.
+ *
+ * Arguments, layouts and results are those of pkv_attention.  A batch whose
+ * scratch bound (the bound pkv_attention sizes its workspace by: num_reqs *
+ * num_kv_heads * ceil(16 * block_table_width / 256) split units of 32 bytes
+ * plus (num_heads / num_kv_heads) * 520 bytes each, and the prefill/pair
+ * lists) exceeds 32 MiB is refused with PKV_ERR_UNSUPPORTED before anything
+ * is enqueued.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call shares the one array: calls
+ * whose kernels overlap on the GPU (e.g. on two streams) race, and must be
+ * serialised by the caller.  Device-side metadata errors are skipped as in
+ * pkv_attention but are not reported (pkv_get_error reads only the word of
+ * the allocating calls), and pkv_last_error_string is not set: the return
+ * code alone says which host check failed.
+ */
+int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
+                          const void* key_cache, const void* value_cache, int64_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t head_size,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          const int32_t* block_table, int64_t block_table_width,
+                          int32_t num_reqs, float scale, void* out, int64_t out_row_stride,
+                          void* stream);
+
+/*
  * pkv_reserve_workspace — sizes the current device's workspace for
  * pkv_attention calls with up to max_reqs requests, max_q_rows query rows,
  * block-table rows of up to block_table_width entries and this head

@@ -15,9 +15,11 @@ seq_lens / block_table.  Both calls enqueue on ``stream`` (default: torch's
 current stream) and return immediately.
 """
 from ._binding import (DEV_ERR_BITS, TRACE_KINDS, PkvError, library_path, load,
-                       pkv_attention, pkv_get_error, pkv_launch_count, pkv_num_sms,
+                       pkv_attention, pkv_attention_noalloc, pkv_get_error, pkv_launch_count,
+                       pkv_num_sms,
                        pkv_reserve_workspace, pkv_trace_enable, pkv_trace_read, pkv_write)
 
-__all__ = ["pkv_write", "pkv_attention", "pkv_get_error", "pkv_reserve_workspace",
+__all__ = ["pkv_write", "pkv_attention", "pkv_attention_noalloc", "pkv_get_error",
+           "pkv_reserve_workspace",
            "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read", "pkv_launch_count",
            "PkvError", "DEV_ERR_BITS", "TRACE_KINDS", "load", "library_path"]

@@ -186,3 +186,37 @@ def pkv_trace_read():
 
 def pkv_launch_count() -> int:
     return load().pkv_launch_count()
+
+
+def pkv_attention_noalloc(q, key_cache, value_cache, query_start_loc, seq_lens, block_table,
+                          num_reqs, scale, out, stream=None):
+    """pkv_attention computed with the library's static scratch array instead
+    of a cudaMalloc'd workspace, for callers that cannot allocate device
+    memory (see include/pkv.h).  Same arguments and result; raises PkvError
+    with the return code when a host check refuses the call."""
+    import torch
+    L = load()
+    fn = L.pkv_attention_noalloc
+    if fn.argtypes is None:
+        i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+        fn.restype = ctypes.c_int
+        fn.argtypes = [vp, i64, i64, i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64, i32, f32,
+                       vp, i64, vp]
+    for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"), (out, "out")):
+        _require(t, torch.bfloat16, n)
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_table, "block_table")):
+        _require(t, torch.int32, n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
+    nb, bs, hkv, d = key_cache.shape
+    rows, hq, _ = q.shape
+    bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
+    rc = fn(q.data_ptr(), _rows3(q, "q"), rows, hq, key_cache.data_ptr(), value_cache.data_ptr(),
+            nb, bs, hkv, d, query_start_loc.data_ptr(), seq_lens.data_ptr(),
+            block_table.data_ptr(), bt_width, int(num_reqs), float(scale), out.data_ptr(),
+            _rows3(out, "out"), _stream(stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_attention_noalloc refused the call")
