@@ -349,7 +349,9 @@ def main():
         peak = peaks.get("bf16_tflops")
         roof = {"bound": "tensor", "achieved": algo / (avg_ms / 1e3) / 1e12,
                 "peak": peak, "unit": "TFLOP/s", "peak_source": "measured" if peak else None}
-        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu"]
+        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu",
+                "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
+                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
     else:
         algo = decode_algorithmic_bytes(spec) if dominant == "decode" else \
             2 * s.num_tokens * s.hkv * d * 2 * 2
@@ -357,6 +359,7 @@ def main():
         roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
                 "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
         srcs = ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % dominant,
+                "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
                 "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
     if roof["peak"] is None:
         roof["peak"] = 1900.0 if roof["unit"] == "TFLOP/s" else 6800.0
