@@ -148,6 +148,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, dist, device):
+    """The slowest rank's time: every rank's replica must finish for the
+    whole-job throughput (all ranks' work / this time)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(work_per_rank, world, seconds_max):
+    """Weak scaling: each rank processes one replica of the batch."""
+    return work_per_rank * world / seconds_max
+
+
 def cpu_baseline(step, sample_reqs=None):
     """The float64 oracle on the host cores over (a sample of) the same step."""
     import oracle
@@ -290,14 +306,11 @@ def main():
     trace = pkv.pkv_trace_read()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
-    t_max = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms = float(t_max.item())
+    ms = max_over_ranks(ms, dist, "cuda")
     ms_per_step = ms / args.steps
     name, unit = metric_of(spec)
     work = metric_work(spec)
-    value = work * world / (ms_per_step / 1e3)
+    value = whole_job_value(work, world, ms_per_step / 1e3)
 
     # end to end through the public API with host buffers: pinned host inputs
     # copied in, the two calls, the output copied back, every step
@@ -330,12 +343,10 @@ def main():
             e2e_step()
         barrier()
         e2e_s = (time.perf_counter() - t0) / args.steps
-        tt = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        if dist is not None:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e = {"value": work * world / float(tt.item()), "unit": unit,
+        e2e_s = max_over_ranks(e2e_s, dist, "cuda")
+        e2e = {"value": work * world / e2e_s, "unit": unit,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": float(tt.item()) * 1e3}
+               "ms_per_step": e2e_s * 1e3}
 
     # roofline of the dominant kernel, from its live CUDA-event durations
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
