@@ -223,12 +223,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
+    // Global loads are issued one step before their values are needed: the
+    // next item's cursor and entry while the current item is being issued,
+    // its request's lengths after the current item's first tile, and each
+    // tile's block ids one tile ahead; a load only stalls at its first use.
     uint32_t tile_cnt = 0, vt_uses[kStages] = {0, 0}, qx_cnt[2] = {0, 0};
+    int w_nxt = 0;
+    if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
+    w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
+    PreEntry e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : PreEntry{-1, 0, 0, 0};
+    int q0_nxt = 0, q1_nxt = 0, L_nxt = 0;
+    if (e_nxt.r >= 0) {
+      q0_nxt = a.qsl[e_nxt.r];
+      q1_nxt = a.qsl[e_nxt.r + 1];
+      L_nxt = a.seq_lens[e_nxt.r];
+    }
     for (uint32_t it_cnt = 0;; ++it_cnt) {
       const int slot = it_cnt & 1;
-      int w = 0;
-      if (lane == 0) w = atomicAdd(&ws.hdr->pre_counter, 1);
-      w = __shfl_sync(0xffffffffu, w, 0);
+      const int w = w_nxt;
+      const PreEntry e = e_nxt;
+      const int q0 = q0_nxt, q1 = q1_nxt, Lr = L_nxt;
       if (it_cnt >= 2 &&
           !mbar_wait_warp(bar(B_IE + slot), ((it_cnt >> 1) - 1) & 1, abort, ws.err))
         break;
@@ -241,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       Item it;
       {
-        const PreEntry e = ws.pre[w / per_entry];
         const int hp = w % per_entry;
         it.r = e.r;
         it.qt = e.qt;
@@ -249,16 +262,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.ha = pairs ? 2 * hp : hp;
         it.hb = pairs ? 2 * hp + 1 : -1;
         it.g = it.ha / G;
-        it.q0 = a.qsl[it.r];
-        it.n = a.qsl[it.r + 1] - it.q0;
-        it.L = a.seq_lens[it.r];
-        it.ctx = it.L - it.n;
+        it.q0 = q0;
+        it.n = q1 - q0;
+        it.L = Lr;
+        it.ctx = Lr - it.n;
         it.pad0 = it.pad1 = 0;
       }
       if (lane == 0) {
         items[slot] = it;
         mbar_arrive(bar(B_IF + slot));
       }
+      // the next item's cursor and entry (consumed after this item)
+      if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
+      w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
+      e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : PreEntry{-1, 0, 0, 0};
       const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
       const int row0 = it.q0 + it.qt * kPreTileQ;
       // Q tiles, once the previous item's last S has read them
@@ -279,24 +296,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(qd + kHalfBytes, &tm_q, bar(B_QF + x), 64, h, row0);
         }
       }
+      // lane p < pages(j) holds the block id of page p of tile j
+      auto tile_pages = [&](int j) { return min(8, (it.L - j * kTileK + 15) / 16); };
+      int blk_nxt = lane < tile_pages(0) ? __ldg(btrow + lane) : 0;
       for (int j = 0; ok && j < it.nkv; ++j) {
         const uint32_t c = tile_cnt++;
         const int s = c % kStages;
         const int key0 = j * kTileK;
-        const int pages = min(8, (it.L - key0 + 15) / 16);
+        const int pages = tile_pages(j);
         const bool tail = key0 + kTileK > it.L;
-        int blk = 0;  // lane p < pages holds the block id of page p
-        if (lane < pages) {
-          blk = __ldg(btrow + (key0 >> 4) + lane);
-          if (blk < 0 || (int64_t)blk >= a.num_blocks) {
-            atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
-            blk = 0;
-          }
+        int blk = blk_nxt;
+        if (j + 1 < it.nkv && lane < tile_pages(j + 1))
+          blk_nxt = __ldg(btrow + ((key0 + kTileK) >> 4) + lane);
+        if (j == 0 && e_nxt.r >= 0) {  // the next item's request lengths
+          q0_nxt = a.qsl[e_nxt.r];
+          q1_nxt = a.qsl[e_nxt.r + 1];
+          L_nxt = a.seq_lens[e_nxt.r];
         }
         if (c >= (uint32_t)kStages &&
             !mbar_wait_warp(bar(B_KE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
           ok = false;
           break;
+        }
+        if (lane < pages && (blk < 0 || (int64_t)blk >= a.num_blocks)) {
+          atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
+          blk = 0;
         }
         const uint32_t kdst = sbase + kOffK + s * kTileBytes;
         if (lane == 0) mbar_expect_tx(bar(B_KF + s), pages * 2 * kPageBoxBytes);
@@ -448,57 +472,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int lim = qpos - j * kTileK;  // columns <= lim are visible
         const bool masked = !__all_sync(0xffffffffu, lim >= kTileK - 1);
-        // pass 1: the row maximum, 32 columns at a time
-        float mt = -INFINITY;
+        // the row's 128 scores in registers (one wait), max, then P in place
+        float sv[128];
+        PKV_LD32(t_s + 0, (sv + 0));
+        PKV_LD32(t_s + 32, (sv + 32));
+        PKV_LD32(t_s + 64, (sv + 64));
+        PKV_LD32(t_s + 96, (sv + 96));
+        tmem_wait_ld();
+        if (masked) {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          PKV_LD32(t_s + ch * 32, v);
-          tmem_wait_ld();
-          if (masked) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = (ch * 32 + i <= lim) ? v[i] : -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = fmaxf(v[i], v[i + 16]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = fmaxf(v[i], v[i + 8]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) v[i] = fmaxf(v[i], v[i + 4]);
-          mt = fmaxf(mt, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+          for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
         }
-        mt *= sl2;
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(sv[k], sv[k + 8]);
+#pragma unroll
+        for (int i = 16; i < 128; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[i + k]);
+        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
         float alpha = 1.f;
         const bool resc = mt > m_used + kRescaleThreshold;
         if (resc) {
           alpha = fast_exp2(m_used - mt);  // 0 on the first tile
           m_used = mt;
         }
-        // pass 2: probabilities, row sum, bf16 P over the first 64 columns
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
+        // packed bf16 pairs over sv[0..63] (sv[2i], sv[2i+1] read before sv[i] is written)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int ch = hh * 2 + c2;
-            float v[32];
-            PKV_LD32(t_s + ch * 32, v);
-            tmem_wait_ld();
-            if (masked) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = (ch * 32 + i <= lim) ? v[i] : -INFINITY;
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = fast_exp2(fmaf(v[2 * i], sl2, -m_used));
-              const float p1 = fast_exp2(fmaf(v[2 * i + 1], sl2, -m_used));
-              rs[i & 3] += p0 + p1;
-              pk[c2 * 16 + i] = pack_bf16(p0, p1);
-            }
-          }
-          PKV_ST32U(t_s + hh * 32, pk);
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = fast_exp2(fmaf(sv[2 * i], sl2, -m_used));
+          const float p1 = fast_exp2(fmaf(sv[2 * i + 1], sl2, -m_used));
+          rs[i & 3] += p0 + p1;
+          sv[i] = __uint_as_float(pack_bf16(p0, p1));
         }
+        PKV_ST32(t_s + 0, (sv + 0));
+        PKV_ST32(t_s + 32, (sv + 32));
         l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // PV(j-1) is complete (S(j) is, and one thread's MMAs finish in order)
