@@ -140,6 +140,36 @@ int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t n
                   float scale, void* out, int64_t out_row_stride, void* stream);
 
 /*
+ * pkv_prepare_step — the step-side metadata the two calls read, computed on
+ * the device from the request state (no host round trip).
+ *
+ * Defined by "Tour: One forward pass", stop 3 (prepare_pos_seq_lens: token t
+ * of request r sits at num_computed[r] + (t - query_start_loc[r]); seq_len =
+ * num_computed + query_len; padding rows of positions are not written) and
+ * stop 4 (gather_block_tables: each request's persistent row, idx_mapping,
+ * copied into batch order; compute_slot_mappings: slot = block_number *
+ * block_size + offset; rows past the last request's tokens get -1).
+ *
+ *   query_start_loc       int32 [num_reqs + 1], non-decreasing.
+ *   num_computed          int32 [num_reqs]: tokens already in the cache.
+ *   idx_mapping           int32 [num_reqs]: persistent row of each batch row
+ *                         (NULL: batch row r uses persistent row r).
+ *   persistent_block_table int32 [persistent_rows, block_table_width].
+ *   positions (out)       int64 [num_tokens_padded]; rows of scheduled tokens.
+ *   seq_lens (out)        int32 [num_reqs].
+ *   slot_mapping (out)    int64 [num_tokens_padded]; -1 for padding rows.
+ *   block_table (out)     int32 [num_reqs, block_table_width] in batch order,
+ *                         or NULL to skip the gather.
+ * A position past the row width, or a persistent row outside the table,
+ * gives slot -1 for that token and PKV_DEV_ERR_BT_WIDTH in the error word.
+ */
+int pkv_prepare_step(const int32_t* query_start_loc, const int32_t* num_computed,
+                     const int32_t* idx_mapping, const int32_t* persistent_block_table,
+                     int64_t persistent_rows, int64_t block_table_width, int32_t num_reqs,
+                     int64_t num_tokens_padded, int64_t* positions, int32_t* seq_lens,
+                     int64_t* slot_mapping, int32_t* block_table, void* stream);
+
+/*
  * pkv_attention_noalloc — pkv_attention for callers that cannot allocate
  * device memory.  The pages this library follows have no counterpart to it.
  *
@@ -207,9 +237,9 @@ int pkv_num_sms(void);
  * launch's duration to its kernel kind, copies up to n kinds of totals into
  * ms[] and launches[] (either may be NULL), clears the record and returns the
  * number of kinds (PKV_TRACE_KINDS).  Kinds: 0 cache write, 1 step plan,
- * 2 decode attention, 3 prefill attention, 4 split-KV merge.
+ * 2 decode attention, 3 prefill attention, 4 split-KV merge, 5 step metadata.
  */
-#define PKV_TRACE_KINDS 5
+#define PKV_TRACE_KINDS 6
 int pkv_trace_enable(int on);
 int pkv_trace_read(double* ms, int64_t* launches, int n);
 

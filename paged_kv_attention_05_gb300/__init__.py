@@ -16,10 +16,11 @@ current stream) and return immediately.
 """
 from ._binding import (DEV_ERR_BITS, TRACE_KINDS, PkvError, library_path, load,
                        pkv_attention, pkv_attention_noalloc, pkv_get_error, pkv_launch_count,
-                       pkv_num_sms,
+                       pkv_num_sms, pkv_prepare_step,
                        pkv_reserve_workspace, pkv_trace_enable, pkv_trace_read, pkv_write)
 
-__all__ = ["pkv_write", "pkv_attention", "pkv_attention_noalloc", "pkv_get_error",
+__all__ = ["pkv_write", "pkv_attention", "pkv_attention_noalloc", "pkv_prepare_step",
+           "pkv_get_error",
            "pkv_reserve_workspace",
            "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read", "pkv_launch_count",
            "PkvError", "DEV_ERR_BITS", "TRACE_KINDS", "load", "library_path"]

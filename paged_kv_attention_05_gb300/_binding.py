@@ -17,8 +17,8 @@ DEV_ERR_BITS = {
 
 EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
            "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
-           "pkv_launch_count"]
-TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine"]
+           "pkv_launch_count", "pkv_prepare_step"]
+TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine", "prepare"]
 
 
 class PkvError(RuntimeError):
@@ -220,3 +220,36 @@ def pkv_attention_noalloc(q, key_cache, value_cache, query_start_loc, seq_lens, 
             _rows3(out, "out"), _stream(stream))
     if rc != 0:
         raise PkvError(rc, "pkv_attention_noalloc refused the call")
+
+
+def pkv_prepare_step(query_start_loc, num_computed, persistent_block_table, num_reqs,
+                     num_tokens_padded, positions, seq_lens, slot_mapping, block_table=None,
+                     idx_mapping=None, stream=None):
+    """Positions, seq_lens, slot mapping and the batch-order block table on
+    the device (see include/pkv.h)."""
+    import torch
+    L = load()
+    fn = L.pkv_prepare_step
+    if fn.argtypes is None:
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        fn.restype = ctypes.c_int
+        fn.argtypes = [vp, vp, vp, vp, i64, i64, i32, i64, vp, vp, vp, vp, vp]
+    for t, n, dt in ((query_start_loc, "query_start_loc", torch.int32),
+                     (num_computed, "num_computed", torch.int32),
+                     (persistent_block_table, "persistent_block_table", torch.int32),
+                     (positions, "positions", torch.int64), (seq_lens, "seq_lens", torch.int32),
+                     (slot_mapping, "slot_mapping", torch.int64)):
+        _require(t, dt, n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    if block_table is not None:
+        _require(block_table, torch.int32, "block_table")
+    if idx_mapping is not None:
+        _require(idx_mapping, torch.int32, "idx_mapping")
+    rows, width = persistent_block_table.shape
+    _check(fn(query_start_loc.data_ptr(), num_computed.data_ptr(),
+              idx_mapping.data_ptr() if idx_mapping is not None else None,
+              persistent_block_table.data_ptr(), rows, width, int(num_reqs),
+              int(num_tokens_padded), positions.data_ptr(), seq_lens.data_ptr(),
+              slot_mapping.data_ptr(), block_table.data_ptr() if block_table is not None else None,
+              _stream(stream)))

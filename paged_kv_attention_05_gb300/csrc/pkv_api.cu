@@ -351,6 +351,43 @@ extern "C" int pkv_num_sms(void) {
   return s->sms;
 }
 
+extern "C" int pkv_prepare_step(const int32_t* query_start_loc, const int32_t* num_computed,
+                                const int32_t* idx_mapping, const int32_t* persistent_block_table,
+                                int64_t persistent_rows, int64_t block_table_width,
+                                int32_t num_reqs, int64_t num_tokens_padded, int64_t* positions,
+                                int32_t* seq_lens, int64_t* slot_mapping, int32_t* block_table,
+                                void* stream) {
+  g_msg[0] = 0;
+  if (num_reqs < 0 || num_tokens_padded < 0 || block_table_width < 1 || persistent_rows < 0)
+    return fail(PKV_ERR_ARG, "negative size or empty block-table row");
+  if (num_reqs == 0 && num_tokens_padded == 0) return PKV_OK;
+  if (!positions || !slot_mapping || (num_reqs > 0 && (!query_start_loc || !num_computed ||
+                                                       !persistent_block_table || !seq_lens)))
+    return fail(PKV_ERR_ARG, "null pointer argument");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  int rc = current_state(&s);
+  if (rc) return rc;
+  PrepArgs p;
+  p.qsl = query_start_loc;
+  p.num_computed = num_computed;
+  p.idx = idx_mapping;
+  p.pbt = persistent_block_table;
+  p.pbt_rows = persistent_rows;
+  p.bt_width = block_table_width;
+  p.num_reqs = num_reqs;
+  p.num_tokens_padded = num_tokens_padded;
+  p.positions = positions;
+  p.seq_lens = seq_lens;
+  p.slot_mapping = slot_mapping;
+  p.block_table = block_table;
+  p.err = s->err;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(5, st, [&] { return launch_prepare(p, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
+  return PKV_OK;
+}
+
 extern "C" int pkv_trace_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_trace_on = on != 0;
@@ -359,7 +396,7 @@ extern "C" int pkv_trace_enable(int on) {
 
 extern "C" int pkv_trace_read(double* ms, int64_t* launches, int n) {
   std::lock_guard<std::mutex> lock(g_mu);
-  double tot[PKV_TRACE_KINDS] = {};
+  double tot[PKV_TRACE_KINDS] = {};  // NOLINT
   int64_t cnt[PKV_TRACE_KINDS] = {};
   int rc = PKV_OK;
   for (const TraceRec& r : g_trace) {

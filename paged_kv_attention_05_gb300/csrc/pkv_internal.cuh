@@ -100,6 +100,23 @@ bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads, in
                    int box_heads, int box_rows);
 bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv);
 
+struct PrepArgs {
+  const int32_t* qsl;           // [num_reqs + 1]
+  const int32_t* num_computed;  // [num_reqs]
+  const int32_t* idx;           // [num_reqs] persistent row of each batch row, or null
+  const int32_t* pbt;           // [pbt_rows, bt_width] persistent block-table rows
+  int64_t pbt_rows;
+  int64_t bt_width;
+  int num_reqs;
+  int64_t num_tokens_padded;
+  int64_t* positions;           // [num_tokens_padded]
+  int32_t* seq_lens;            // [num_reqs]
+  int64_t* slot_mapping;        // [num_tokens_padded]
+  int32_t* block_table;         // [num_reqs, bt_width], or null
+  int* err;
+};
+cudaError_t launch_prepare(const PrepArgs& p, int sms, cudaStream_t st);
+
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
