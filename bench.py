@@ -226,6 +226,9 @@ def main():
     ap.add_argument("--config", default="mha_decode", choices=W.CONFIG_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--with-prepare", action="store_true",
+                    help="start each step with pkv_prepare_step (positions, seq_lens, slot "
+                         "mapping and block table computed on the device)")
     ap.add_argument("--reqs", type=int, default=0,
                     help="first N requests of the workload only, with a pool sized for them "
                          "(a small case of the same kernel shapes, e.g. for profiling)")
@@ -271,7 +274,15 @@ def main():
     stream = torch.cuda.current_stream()
     pkv.pkv_reserve_workspace(s.num_reqs, rows, step.block_table.shape[1], s.hq, s.hkv)
 
+    if args.with_prepare:
+        num_computed = torch.tensor(s.ctx, dtype=torch.int32, device="cuda")
+        persistent_bt = block_table.clone()
+        positions = torch.empty(rows, dtype=torch.int64, device="cuda")
+
     def one_step():
+        if args.with_prepare:
+            pkv.pkv_prepare_step(qsl, num_computed, persistent_bt, s.num_reqs, rows, positions,
+                                 seq_lens, slot_mapping, block_table, stream=stream)
         pkv.pkv_write(k, v, key_cache, value_cache, slot_mapping, stream=stream)
         pkv.pkv_attention(q, key_cache, value_cache, qsl, seq_lens, block_table, s.num_reqs,
                           s.scale, out, stream=stream)
@@ -385,6 +396,7 @@ def main():
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": spec.name, "requests": s.num_reqs, "query_tokens": s.num_tokens,
+                      "step": ("prepare + " if args.with_prepare else "") + "write + attention",
                       "num_heads": s.hq, "num_kv_heads": s.hkv, "head_size": d,
                       "block_size": s.block_size, "kv_bytes_per_step": s.kv_bytes(),
                       "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB)" %

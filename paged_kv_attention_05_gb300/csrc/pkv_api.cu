@@ -99,25 +99,9 @@ int current_state(DeviceState** out) {
   return PKV_OK;
 }
 
-struct Sizes {
-  int64_t units, pre, pairs;
-  int group;
-};
-
-Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv) {
-  Sizes z;
-  const int64_t max_keys = bt_width * kBlockSize;
-  const int64_t splits = (max_keys + kMinChunk - 1) / kMinChunk;
-  z.units = reqs * hkv * (splits < 1 ? 1 : splits);
-  z.pre = (q_rows + kPreTileQ - 1) / kPreTileQ + reqs;
-  z.pairs = reqs * hkv;
-  z.group = hq / hkv;
-  return z;
-}
-
 // Makes sure the workspace holds at least `z`; allocation only outside capture.
 int ensure_workspace(DeviceState* s, const Sizes& z, cudaStream_t st, Workspace* ws) {
-  const size_t need = workspace_bytes(z.units, z.pre, z.pairs, z.group);
+  const size_t need = workspace_bytes(z);
   if (need > s->ws_bytes) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (st != nullptr) cudaStreamIsCapturing(st, &cap);
@@ -139,7 +123,7 @@ int ensure_workspace(DeviceState* s, const Sizes& z, cudaStream_t st, Workspace*
     s->ws_bytes = grow;
   }
   // carve for the capacity actually held, scaled from the request
-  *ws = carve_workspace(s->ws, z.units, z.pre, z.pairs, z.group, s->err);
+  *ws = carve_workspace(s->ws, z, s->err);
   return PKV_OK;
 }
 
@@ -154,40 +138,56 @@ int check_geometry(int32_t block_size, int32_t hkv, int32_t head_size) {
 
 }  // namespace
 
-size_t workspace_bytes(int64_t max_units, int64_t max_pre, int64_t max_pairs, int group) {
+Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv) {
+  Sizes z;
+  const int64_t max_keys = bt_width * kBlockSize;
+  int64_t splits = (max_keys + kMinChunk - 1) / kMinChunk;
+  if (splits < 1) splits = 1;
+  const int group = hq / hkv;
+  z.units = reqs * hkv * splits;
+  z.pre = (q_rows + kPreTileQ - 1) / kPreTileQ + reqs;
+  z.pairs = reqs * hkv;
+  // decode query rows (tokens x heads of a group) are at most q_rows * G in
+  // all and dec_rows_cap(G) per request
+  const int64_t rows_a = q_rows * group, rows_b = reqs * dec_rows_cap(group);
+  z.part_rows = splits * hkv * (rows_a < rows_b ? rows_a : rows_b);
+  return z;
+}
+
+size_t workspace_bytes(const Sizes& z) {
   size_t b = 256;                                      // header
-  b += (size_t)max_units * sizeof(DecUnit);
-  b += (size_t)max_pre * sizeof(PreEntry);
-  b += (size_t)max_pairs * sizeof(SplitPair);
+  b += (size_t)z.units * sizeof(DecUnit);
+  b += (size_t)z.pre * sizeof(PreEntry);
+  b += (size_t)z.pairs * sizeof(SplitPair);
   b = (b + 255) & ~(size_t)255;
-  b += (size_t)max_units * group * 2 * sizeof(float);  // part_ml
+  b += (size_t)z.part_rows * 2 * sizeof(float);  // part_ml
   b = (b + 255) & ~(size_t)255;
-  b += (size_t)max_units * group * kHeadSize * sizeof(float);  // part_o
+  b += (size_t)z.part_rows * kHeadSize * sizeof(float);  // part_o
   return b + 256;
 }
 
-Workspace carve_workspace(void* base, int64_t max_units, int64_t max_pre, int64_t max_pairs,
-                          int group, int* err) {
+Workspace carve_workspace(void* base, const Sizes& z, int* err) {
   Workspace w;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
   w.hdr = reinterpret_cast<PlanHeader*>(p);
   off += 256;
   w.units = reinterpret_cast<DecUnit*>(p + off);
-  off += (size_t)max_units * sizeof(DecUnit);
+  off += (size_t)z.units * sizeof(DecUnit);
   w.pre = reinterpret_cast<PreEntry*>(p + off);
-  off += (size_t)max_pre * sizeof(PreEntry);
+  off += (size_t)z.pre * sizeof(PreEntry);
   w.pairs = reinterpret_cast<SplitPair*>(p + off);
-  off += (size_t)max_pairs * sizeof(SplitPair);
+  off += (size_t)z.pairs * sizeof(SplitPair);
   off = (off + 255) & ~(size_t)255;
   w.part_ml = reinterpret_cast<float*>(p + off);
-  off += (size_t)max_units * group * 2 * sizeof(float);
+  off += (size_t)z.part_rows * 2 * sizeof(float);
   off = (off + 255) & ~(size_t)255;
   w.part_o = reinterpret_cast<float*>(p + off);
   w.err = err;
-  w.max_units = max_units;
-  w.max_pre = max_pre;
-  w.max_pairs = max_pairs;
+  w.max_units = z.units;
+  w.max_pre = z.pre;
+  w.max_pairs = z.pairs;
+  w.max_part_rows = z.part_rows;
   return w;
 }
 

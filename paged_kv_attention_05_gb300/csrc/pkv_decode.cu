@@ -1,5 +1,6 @@
 // Split-KV decode attention over the paged cache (requests with one query
-// token), and the merge of split results.
+// token, or a few: speculative or multi-token decode), and the merge of
+// split results.
 //
 // What it computes: "vLLM 推理全流程深度解析" (vLLM inference deep dive),
 // paged_attention_v1 section — find the request's physical blocks through
@@ -19,8 +20,12 @@
 //     ring of 8 KB page stages (3 deep, 2 for 32-head groups).  Warps never
 //     wait for each other, so each SM keeps 8 independent streams of loads in
 //     flight and 8 warps to hide the latency of the math.
-//   * A warp owns the G query-head rows of its KV head in one or two 16-row
-//     tiles (zero rows past G): S = Q.K^T and O += P.V run
+//   * A warp owns the query rows of its KV head in one or two 16-row tiles:
+//     row = token * G + head in group, for the request's qn tokens (qn * G at
+//     most 16, or 32 for groups above 16; longer requests go to prefill).
+//     Row (token i) sees the keys before position ctx + i + 1, ctx = keys
+//     before the request's first query token (causal mask inside the
+//     request's own tokens).  S = Q.K^T and O += P.V run
 //     on the tensor cores with bf16 mma.sync m16n8k16 and fp32 accumulation
 //     (with up to 32 heads per K/V row the FMA pipes could not keep pace with
 //     HBM); the softmax state stays in registers, row reductions by quad
@@ -109,7 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) *abort = 0;
     fence_barrier_init();
   }
-  // query rows G .. MT*16-1 are never loaded: keep them zero
+  // rows past a unit's qn * G query rows hold zeros or an earlier unit's
+  // queries; their results are dropped
   for (int i = lane; i < 2 * MT * 16 * 8; i += 32) {
     const int row = (i >> 3) % (MT * 16), half = (i >> 3) / (MT * 16), c = i & 7;
     if (row >= G)
@@ -152,14 +158,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ids[j] = blk;
       }
     }
-    // the G query rows of this KV head (heads g*G ..) by TMA
+    // the query rows of this KV head by TMA: for each of the unit's qn query
+    // tokens, its G heads (g*G ..), at rows token * G .. token * G + G - 1
+    const int qn = un.qn, nrows = qn * G;
     if (lane == 0) {
       fence_async_smem();  // the previous unit's reads of the buffer are done
-      mbar_expect_tx(q_bar, 2 * G * 128);
+      mbar_expect_tx(q_bar, 2 * nrows * 128);
       const int q0 = a.qsl[un.r];
-      tma_load_3d(qbuf, &tm_q, q_bar, 0, un.g * G, q0);
-      tma_load_3d(qbuf + C::kQHalf, &tm_q, q_bar, 64, un.g * G, q0);
+      for (int i = 0; i < qn; ++i) {
+        tma_load_3d(qbuf + i * G * 128, &tm_q, q_bar, 0, un.g * G, q0 + i);
+        tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, un.g * G, q0 + i);
+      }
     }
+    // last visible key + 1 of the two rows this thread holds in each tile:
+    // row (token i, head) sees keys < ctx + i + 1, clipped to the unit
+    int vis[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int row = mt * 16 + (lane >> 2) + hrow * 8;
+        const int ti = row < nrows ? row / G : qn - 1;
+        vis[mt][hrow] = min(k1, un.ctx + ti + 1);
+      }
 
     // page p of the unit into stage (page_cnt + p) % kStages; the stage's
     // previous page was consumed by this warp already (program order)
@@ -214,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const int valid = k1 - (k0 + p * kBlockSize);  // keys of this page inside the unit
+      const int pos0 = k0 + p * kBlockSize;
+      const int valid = k1 - pos0;  // keys of this page inside the unit
       const uint32_t st = wbase + s * kPage;
 
       // S = Q K^T for the page's 16 keys (two n-tiles of 8)
@@ -258,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = nt * 8 + tig * 2 + (e & 1);
-            xs[nt][e] = tok < valid ? sacc[mt][nt][e] * sl2 : -INFINITY;
+            xs[nt][e] = pos0 + tok < vis[mt][e >> 1] ? sacc[mt][nt][e] * sl2 : -INFINITY;
           }
           mx0 = fmaxf(mx0, fmaxf(xs[nt][0], xs[nt][1]));
           mx1 = fmaxf(mx1, fmaxf(xs[nt][2], xs[nt][3]));
@@ -270,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool up0 = mx0 > m_run[mt][0] + 8.f, up1 = mx1 > m_run[mt][1] + 8.f;
         if (__any_sync(0xffffffffu, up0 || up1)) {
           const float n0 = up0 ? mx0 : m_run[mt][0], n1 = up1 ? mx1 : m_run[mt][1];
-          const float al0 = fast_exp2(m_run[mt][0] - n0), al1 = fast_exp2(m_run[mt][1] - n1);
+          // (a row that did not grow keeps factor 1: its maximum may still be -inf)
+          const float al0 = up0 ? fast_exp2(m_run[mt][0] - n0) : 1.f;
+          const float al1 = up1 ? fast_exp2(m_run[mt][1] - n1) : 1.f;
           m_run[mt][0] = n0;
           m_run[mt][1] = n1;
           l_run[mt][0] *= al0;
@@ -283,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[mt][dn][3] *= al1;
           }
         }
-        const float c0 = m_run[mt][0], c1 = m_run[mt][1];
+        // a row with no visible key yet keeps m = -inf: use 0 as its reference
+        const float c0 = m_run[mt][0] == -INFINITY ? 0.f : m_run[mt][0];
+        const float c1 = m_run[mt][1] == -INFINITY ? 0.f : m_run[mt][1];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           xs[nt][0] = fast_exp2(xs[nt][0] - c0);
@@ -331,37 +357,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int ra = mt * 16 + gid, rb = ra + 8;  // head rows inside the KV head's group
+      const int ra = mt * 16 + gid, rb = ra + 8;  // rows: token * G + head in group
       if (un.nsplit == 1) {
         const int q0 = a.qsl[un.r];
-        uint16_t* orow = a.out + (int64_t)q0 * a.out_stride + (int64_t)un.g * G * kHeadSize;
+        // row -> out[q0 + row / G][g * G + row % G]
+        uint16_t* oa = a.out + (int64_t)(q0 + ra / G) * a.out_stride +
+                       (int64_t)(un.g * G + ra % G) * kHeadSize;
+        uint16_t* ob = a.out + (int64_t)(q0 + rb / G) * a.out_stride +
+                       (int64_t)(un.g * G + rb % G) * kHeadSize;
         const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
         for (int dn = 0; dn < 16; ++dn) {
           const int col = dn * 8 + tig * 2;
-          if (ra < G)
-            *reinterpret_cast<uint32_t*>(orow + ra * kHeadSize + col) =
-                pack_bf16(o[mt][dn][0] * i0, o[mt][dn][1] * i0);
-          if (rb < G)
-            *reinterpret_cast<uint32_t*>(orow + rb * kHeadSize + col) =
-                pack_bf16(o[mt][dn][2] * i1, o[mt][dn][3] * i1);
+          if (ra < nrows)
+            *reinterpret_cast<uint32_t*>(oa + col) = pack_bf16(o[mt][dn][0] * i0, o[mt][dn][1] * i0);
+          if (rb < nrows)
+            *reinterpret_cast<uint32_t*>(ob + col) = pack_bf16(o[mt][dn][2] * i1, o[mt][dn][3] * i1);
         }
       } else {
-        const int64_t pra = (int64_t)un.part * G + ra, prb = (int64_t)un.part * G + rb;
+        const int64_t pra = (int64_t)un.part + ra, prb = (int64_t)un.part + rb;
 #pragma unroll
         for (int dn = 0; dn < 16; ++dn) {
           const int col = dn * 8 + tig * 2;
-          if (ra < G)
+          if (ra < nrows)
             *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
                 make_float2(o[mt][dn][0], o[mt][dn][1]);
-          if (rb < G)
+          if (rb < nrows)
             *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
                 make_float2(o[mt][dn][2], o[mt][dn][3]);
         }
         if (tig == 0) {
-          if (ra < G)
+          if (ra < nrows)
             *reinterpret_cast<float2*>(ws.part_ml + pra * 2) = make_float2(m_run[mt][0], l0);
-          if (rb < G)
+          if (rb < nrows)
             *reinterpret_cast<float2*>(ws.part_ml + prb * 2) = make_float2(m_run[mt][1], l1);
         }
       }
@@ -369,31 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge of split results: one (split pair, query head) per CTA iteration,
-// one output column per thread; the weights exp2(m_s - max) renormalise the
+// Merge of split results: one (split pair, query row) per CTA iteration, one
+// output column per thread; the weights exp2(m_s - max) renormalise the
 // splits' running sums and outputs (the same online-softmax identity the
-// decode loop uses between pages).
+// decode loop uses between pages).  Rows are (query token, head in group);
+// pairs with fewer rows than the largest skip the rest.
 __global__ void __launch_bounds__(kHeadSize) combine_kernel(AttnArgs a, Workspace ws) {
   const int G = a.hq / a.hkv;
-  const int n_items = ws.hdr->n_pairs * G;
+  const int max_rows = ws.hdr->max_rows;
+  const int n_items = ws.hdr->n_pairs * max_rows;
   const int d = threadIdx.x;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const SplitPair sp = ws.pairs[item / G];
-    const int row = item % G;
-    const float* ml = ws.part_ml + ((int64_t)sp.first * G + row) * 2;
-    const float* po = ws.part_o + ((int64_t)sp.first * G + row) * kHeadSize + d;
+    const SplitPair sp = ws.pairs[item / max_rows];
+    const int row = item % max_rows;
+    const int q0 = a.qsl[sp.r];
+    const int rows = (a.qsl[sp.r + 1] - q0) * G;
+    if (row >= rows) continue;
+    const float* ml = ws.part_ml + ((int64_t)sp.first + row) * 2;
+    const float* po = ws.part_o + ((int64_t)sp.first + row) * kHeadSize + d;
     float M = -INFINITY;
-    for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, __ldcg(ml + (int64_t)s * G * 2));
+    for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, __ldcg(ml + (int64_t)s * rows * 2));
     float acc = 0.f, lsum = 0.f;
 #pragma unroll 4
     for (int s = 0; s < sp.nsplit; ++s) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + (int64_t)s * G * 2));
-      const float f = fast_exp2(v.x - M);
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + (int64_t)s * rows * 2));
+      const float f = fast_exp2(v.x - M);  // a split that saw no key of this row has m = -inf
       lsum += f * v.y;
-      acc += f * __ldcg(po + (int64_t)s * G * kHeadSize);
+      acc += f * __ldcg(po + (int64_t)s * rows * kHeadSize);
     }
-    const int q0 = a.qsl[sp.r];
-    a.out[(int64_t)q0 * a.out_stride + (int64_t)(sp.g * G + row) * kHeadSize + d] =
+    a.out[(int64_t)(q0 + row / G) * a.out_stride + (int64_t)(sp.g * G + row % G) * kHeadSize + d] =
         __bfloat16_as_ushort(__float2bfloat16_rn(acc / lsum));
   }
 }

@@ -19,9 +19,14 @@ constexpr int kMaxChunk = 2048;  // largest split-KV chunk (tokens)
 constexpr int kMaxBtWidth = 32768;  // block-table entries per request (524,288 keys) at most
 constexpr int kPreTileQ = 128;   // query rows per prefill tile
 
-// One decode work unit: request r, KV head g, keys [k0, k1) of the request.
+// Query rows a decode unit can carry (query tokens x heads of one KV head).
+__host__ __device__ constexpr int dec_rows_cap(int group) { return group <= 16 ? 16 : 32; }
+
+// One decode work unit: request r with qn query tokens (ctx keys before the
+// first one), KV head g, keys [k0, k1) of the request.  Split results occupy
+// partial rows part .. part + qn * G - 1 (row = token * G + head in group).
 struct __align__(16) DecUnit {
-  int r, g, split, nsplit, k0, k1, part, pad;
+  int r, g, ctx, nsplit, k0, k1, part, qn;
 };
 
 // One prefill work entry: request r, 128-row query tile qt; nkv = number of
@@ -30,8 +35,8 @@ struct __align__(16) PreEntry {
   int r, qt, nkv, pad;
 };
 
-// A (request, KV head) whose keys were split over several decode units: its
-// partial results live in part slots first .. first + nsplit - 1.
+// A (request, KV head) whose keys were split over several decode units: split
+// s keeps its qn * G partial rows from first + s * qn * G.
 struct __align__(16) SplitPair {
   int r, g, first, nsplit;
 };
@@ -44,7 +49,8 @@ struct PlanHeader {
   int pre_counter;
   int chunk;
   int n_pairs;      // split pairs to merge
-  int pad[10];
+  int max_rows;     // most query rows of one split pair (qn * G)
+  int pad[9];
 };
 
 // Device pointers into the per-device workspace.
@@ -53,18 +59,23 @@ struct Workspace {
   DecUnit* units;
   PreEntry* pre;
   SplitPair* pairs;  // [max_reqs * hkv] split pairs (n_pairs used)
-  float* part_ml;    // [part_slots * group][2]: running max (log2 domain) and sum
-  float* part_o;     // [part_slots * group][128]: unnormalised output
+  float* part_ml;    // [part rows][2]: running max (log2 domain) and sum
+  float* part_o;     // [part rows][128]: unnormalised output
   int* err;          // device error word
   int64_t max_units;
   int64_t max_pre;
   int64_t max_pairs;
+  int64_t max_part_rows;
 };
 
 // Bytes needed for a workspace serving up to these sizes.
-size_t workspace_bytes(int64_t max_units, int64_t max_pre, int64_t max_pairs, int group);
-Workspace carve_workspace(void* base, int64_t max_units, int64_t max_pre, int64_t max_pairs,
-                          int group, int* err);
+// Capacities of a workspace for a call (or a reservation) of these sizes.
+struct Sizes {
+  int64_t units, pre, pairs, part_rows;
+};
+Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv);
+size_t workspace_bytes(const Sizes& z);
+Workspace carve_workspace(void* base, const Sizes& z, int* err);
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,

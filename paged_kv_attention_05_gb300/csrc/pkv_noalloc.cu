@@ -83,12 +83,9 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
 
   // the scratch this call can need, by the same bound pkv_attention sizes
   // its workspace with; above the static array's size the call is refused
-  const int64_t splits = (block_table_width * kBlockSize + kMinChunk - 1) / kMinChunk;
-  const int64_t units = (int64_t)num_reqs * num_kv_heads * (splits < 1 ? 1 : splits);
-  const int64_t pre = (q_rows + kPreTileQ - 1) / kPreTileQ + num_reqs;
-  const int64_t pairs = (int64_t)num_reqs * num_kv_heads;
   const int group = num_heads / num_kv_heads;
-  const size_t need = workspace_bytes(units, pre, pairs, group);
+  const Sizes z = sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads);
+  const size_t need = workspace_bytes(z);
   if (need > kScratchBytes)
     return noalloc_fail(PKV_ERR_UNSUPPORTED, "batch needs more scratch than the static array");
 
@@ -126,7 +123,7 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
     sms = g_sms[dev];
   }
 
-  Workspace ws = carve_workspace(scratch, units, pre, pairs, group, err);
+  Workspace ws = carve_workspace(scratch, z, err);
   AttnArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.q_stride = q_row_stride;

@@ -86,7 +86,10 @@ __device__ ReqInfo classify(const AttnArgs& a, int r) {
   ri.n = q1 - q0;
   ri.L = L;
   ri.q0 = q0;
-  ri.kind = ri.n == 1 ? 1 : (ri.n > 1 ? 2 : 0);
+  // decode: the query tokens x heads of a KV head fit one decode unit's rows
+  // (speculative / multi-token decode included); prefill: anything longer
+  const int G = a.hq / a.hkv;
+  ri.kind = ri.n == 0 ? 0 : (ri.n * G <= dec_rows_cap(G) ? 1 : 2);
   return ri;
 }
 
@@ -129,6 +132,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // finding its request by binary search over the chunk's offsets
   __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1], s_off_q[kPlanThreads + 1];
   __shared__ int s_off_p[kPlanThreads], s_len[kPlanThreads], s_n[kPlanThreads];
+  __shared__ int s_max_rows;
+  if (tid == 0) s_max_rows = 0;
+  __syncthreads();
   int unit_carry = 0, part_carry = 0, pre_carry = 0, pair_carry = 0;
   for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
     const int r = base + tid;
@@ -139,8 +145,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     if (ri.kind == 1) {
       const int nsplit = (ri.L + chunk - 1) / chunk;
       units = nsplit * a.hkv;
-      parts = nsplit > 1 ? units : 0;
+      parts = nsplit > 1 ? units * ri.n * G : 0;  // partial rows
       pairs = nsplit > 1 ? a.hkv : 0;
+      if (nsplit > 1) atomicMax(&s_max_rows, ri.n * G);
     } else if (ri.kind == 2) {
       tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
     }
@@ -164,16 +171,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     for (int i = tid; i < tot_u; i += kPlanThreads) {
       const int lo = find_owner(s_off_u, i);
       const int rem = i - s_off_u[lo];
-      const int L = s_len[lo];
+      const int L = s_len[lo], qn = s_n[lo];
       const int nsplit = (L + chunk - 1) / chunk;
       const int sp = rem / a.hkv, g = rem - sp * a.hkv;
       const int64_t idx = (int64_t)unit_carry + i;
       if (idx >= ws.max_units) break;
       // two 16-byte stores per unit: consecutive threads fill consecutive units
       int4* dst = reinterpret_cast<int4*>(ws.units + idx);
-      dst[0] = make_int4(base + lo, g, sp, nsplit);
+      dst[0] = make_int4(base + lo, g, L - qn, nsplit);
       dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
-                         nsplit > 1 ? s_off_p[lo] + g * nsplit + sp : -1, 0);
+                         nsplit > 1 ? s_off_p[lo] + (g * nsplit + sp) * qn * G : -1, qn);
     }
     for (int i = tid; i < tot_q; i += kPlanThreads) {
       const int lo = find_owner(s_off_q, i);
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       const int64_t idx = (int64_t)pair_carry + i;
       if (idx >= ws.max_pairs) break;
       *reinterpret_cast<int4*>(ws.pairs + idx) =
-          make_int4(base + lo, g, s_off_p[lo] + g * nsplit, nsplit);
+          make_int4(base + lo, g, s_off_p[lo] + g * nsplit * s_n[lo] * G, nsplit);
     }
     for (int i = tid; i < tot_t; i += kPlanThreads) {
       const int lo = find_owner(s_off_t, i);
@@ -209,6 +216,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     ws.hdr->pre_counter = 0;
     ws.hdr->chunk = chunk;
     ws.hdr->n_pairs = (int)min((int64_t)pair_carry, ws.max_pairs);
+    ws.hdr->max_rows = s_max_rows;
   }
 }
 

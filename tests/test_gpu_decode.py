@@ -69,3 +69,35 @@ def test_decode_bit_identical_under_block_permutation():
 def test_decode_full_size(name):
     step = W.build(W.spec(name))
     run_and_check(step, name)
+
+
+# Multi-token decode (speculative / multi-token steps): a request whose query
+# tokens x heads of one KV head fit 16 rows (32 for groups above 16) runs in
+# the decode kernel with a causal mask inside its own tokens.
+@pytest.mark.parametrize("hq,hkv,qn", [(4, 4, 2), (4, 4, 5), (4, 4, 16), (8, 4, 8),
+                                       (8, 2, 4), (16, 2, 2), (32, 1, 1), (12, 4, 5)])
+def test_multi_token_decode(hq, hkv, qn):
+    # ctx 253, 2045, 767 with qn up to 16: the last 256-key split starts after
+    # the first token's last visible key, so that row sees nothing there
+    ctx = [0, 3, 16, 253, 767, 2045, 1500]
+    step = W.build(W.custom(ctx, [qn] * len(ctx), hq, hkv, seed=hq * 31 + qn))
+    run_and_check(step, "multi-token decode hq=%d hkv=%d qn=%d" % (hq, hkv, qn))
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (16, 4), (32, 4), (64, 2)])
+def test_decode_prefill_boundary(hq, hkv):
+    """q_len at the decode row cap and one past it, in one batch with single
+    tokens and long prefills."""
+    G = hq // hkv
+    cap = 16 if G <= 16 else 32
+    at = max(cap // G, 1)
+    q_len = [1, at, at + 1, 1, 200, at, 3, 130]
+    ctx = [900, 40, 5000, 0, 17, 2300, 64, 0]
+    step = W.build(W.custom(ctx, q_len, hq, hkv, seed=5 + G))
+    run_and_check(step, "decode/prefill boundary hq=%d hkv=%d" % (hq, hkv))
+
+
+def test_multi_token_decode_long_split():
+    ctx = [9000, 4093, 12000]
+    step = W.build(W.custom(ctx, [4, 4, 4], 16, 4, seed=61))
+    run_and_check(step, "multi-token split decode")

@@ -72,7 +72,8 @@ def test_capture_without_reserved_workspace_is_refused_cleanly():
     big = 4096   # far more requests than any earlier call reserved for
     qsl = torch.zeros(big + 1, dtype=torch.int32, device="cuda")
     sl = torch.zeros(big, dtype=torch.int32, device="cuda")
-    bt = torch.zeros((big, 4096), dtype=torch.int32, device="cuda")
+    # the widest block table: 4096 x 2048 split units alone need 256 MiB
+    bt = torch.zeros((big, 32768), dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     with pytest.raises(pkv.PkvError):
         with torch.cuda.stream(stream):
