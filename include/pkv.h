@@ -111,7 +111,11 @@ int pkv_write(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_
  * head h reads KV head h / (num_heads / num_kv_heads) and keys 0 .. ctx + i,
  * key j living at key_cache[block_table[r][j / 16]][j % 16]:
  *   out[q0+i][h] = sum_j softmax_j(scale * q[q0+i][h] . K_j) * V_j,
- * computed with bf16 inputs, fp32 accumulation and a bf16 result.
+ * computed with bf16 inputs, fp32 accumulation and a bf16 result.  Any n
+ * works; requests whose n * (num_heads / num_kv_heads) fits 16 rows (32 for
+ * groups above 16), single-token decodes and short multi-token (speculative)
+ * steps, take the split-KV decode path, longer ones the prefill path; both
+ * compute the formula above.
  *
  *   q               bf16 [q_rows, num_heads, head_size], row stride
  *                   q_row_stride elements (>= num_heads * head_size).
@@ -183,10 +187,12 @@ int pkv_prepare_step(const int32_t* query_start_loc, const int32_t* num_computed
  * holds it until the process exits), and allocates nothing.
  *
  * Arguments, layouts and results are those of pkv_attention.  A batch whose
- * scratch bound (the bound pkv_attention sizes its workspace by: num_reqs *
- * num_kv_heads * ceil(16 * block_table_width / 256) split units of 32 bytes
- * plus (num_heads / num_kv_heads) * 520 bytes each, and the prefill/pair
- * lists) exceeds 32 MiB is refused with PKV_ERR_UNSUPPORTED before anything
+ * scratch bound (the bound pkv_attention sizes its workspace by: with
+ * S = ceil(16 * block_table_width / 256) splits and G = num_heads /
+ * num_kv_heads, num_reqs * num_kv_heads * S split units of 32 bytes, plus
+ * S * num_kv_heads * min(q_rows * G, num_reqs * (G <= 16 ? 16 : 32)) partial
+ * rows of 520 bytes, plus the prefill and pair lists) exceeds 32 MiB is
+ * refused with PKV_ERR_UNSUPPORTED before anything
  * is enqueued.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture.  Every call shares the one array: calls

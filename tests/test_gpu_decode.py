@@ -101,3 +101,16 @@ def test_multi_token_decode_long_split():
     ctx = [9000, 4093, 12000]
     step = W.build(W.custom(ctx, [4, 4, 4], 16, 4, seed=61))
     run_and_check(step, "multi-token split decode")
+
+
+def test_shared_prefix_blocks():
+    """Requests whose block tables start with the same physical blocks (a
+    shared prompt prefix): every reader sees the shared pages; new tokens are
+    written past the shared part."""
+    ctx = [600, 650, 700, 610]
+    q_len = [1, 4, 40, 1]
+    step = W.build(W.custom(ctx, q_len, 16, 4, seed=808))
+    shared = 600 // 16          # whole pages below every request's ctx
+    for r in range(1, 4):
+        step.block_table[r, :shared] = step.block_table[0, :shared]
+    run_and_check(step, "shared prefix")
