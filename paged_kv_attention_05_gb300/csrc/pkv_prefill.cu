@@ -60,7 +60,9 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr int kOffQ = 0;                          // Q_a | Q_b
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kStageWarp = 32 * 64;               // epilogue staging: 32 rows x 64 bytes
+constexpr int kOffStage = kOffV + kStages * kTileBytes;  // one staging area per softmax warp
+constexpr int kOffBar = kOffStage + 8 * kStageWarp;
 enum {
   B_QF = 0,   // [2] Q tile loaded
   B_QE = 2,   // [2] Q tile consumed by the item's last S
@@ -423,7 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             issue_pv(x, c, j > 0);
-            if (more) issue_s(x, c + 1);
+            if (more) {
+              issue_s(x, c + 1);
+            } else {
+              mma_commit(bar(B_OF + x));  // O_x final: its epilogue need not wait for the other tile
+              o_cnt[x]++;
+            }
           }
           if (!ok) break;
           mma_commit(bar(B_VE + c % kStages));
@@ -434,10 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        for (int x = 0; x < nx; ++x) {
-          mma_commit(bar(B_OF + x));
-          o_cnt[x]++;
-        }
         tile_cnt += it.nkv;
       }
     }
@@ -527,27 +530,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(B_PF + x));
       }
       if (!ok) break;
-      // epilogue: O / l in bf16 to the output rows
+      // epilogue: O / l in bf16 to the output rows.  Each 32-column chunk of
+      // the warp's 32 rows goes through the warp's staging area in shared
+      // memory, so that each global store writes whole 64-byte row pieces
+      // (8 rows x 4 lanes) instead of 32 scattered 16-byte pieces.
       if (!mbar_wait_warp(bar(B_OF + x), o_cnt++ & 1, abort, ws.err)) break;
       tc_fence_after();
       const float inv = 1.f / l_sum;
-      uint16_t* orow = a.out + (int64_t)(it.q0 + qrow) * a.out_stride + (int64_t)h * kHeadSize;
+      // (the thread index passes through an opaque move so that the staging
+      // addresses below are computed here, not kept live across the loop)
+      int ti;
+      asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
+      const int ln = ti & 31;
+      const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
+      const int row_base = it.qt * kPreTileQ + (warp & 3) * 32;  // the warp's first row
+      uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize;
+      // the next chunk's TMEM load is in flight while this one is staged
+      float ov[2][32];
+      PKV_LD32(t_o, ov[0]);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        float ov[32];
-        PKV_LD32(t_o + ch * 32, ov);
         tmem_wait_ld();
-        if (valid_row) {
+        if (ch < 3) PKV_LD32(t_o + (ch + 1) * 32, ov[(ch + 1) & 1]);
+        const float* o = ov[ch & 1];
+        // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
+        // that eight lanes of a store phase hit eight different bank groups
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16(ov[i + 0] * inv, ov[i + 1] * inv);
-            v.y = pack_bf16(ov[i + 2] * inv, ov[i + 3] * inv);
-            v.z = pack_bf16(ov[i + 4] * inv, ov[i + 5] * inv);
-            v.w = pack_bf16(ov[i + 6] * inv, ov[i + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + ch * 32 + i) = v;
-          }
+        for (int k = 0; k < 4; ++k) {
+          uint4 v;
+          v.x = pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
+          v.y = pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+          v.z = pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+          v.w = pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                           stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
+                       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = i * 8 + (ln >> 2), c = ln & 3;
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
+                       : "memory");
+          const int qr = row_base + rr;
+          if (qr < it.n)
+            *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
+        }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(bar(B_OE + x));
