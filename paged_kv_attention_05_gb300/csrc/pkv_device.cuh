@@ -64,6 +64,23 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// The same bounded wait, inlined: for a single thread whose waits sit on the
+// critical path (no call, no register save and restore around it).
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              int* err) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort) return false;
+    if (now_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      atomicOr(err, PKV_DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // The same wait taken by every lane of a warp, with a warp-uniform result
 // (warp-collective instructions follow it).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,

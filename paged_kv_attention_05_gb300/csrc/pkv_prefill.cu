@@ -176,6 +176,28 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                              \
       : "memory")
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed fp32-pair instruction
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (s0, s1) += (a0, a1) as one packed fp32-pair instruction
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n .reg .b64 rs, ra;\n mov.b64 rs, {%0, %1};\n mov.b64 ra, {%2, %3};\n"
+      " add.rn.f32x2 rs, rs, ra;\n mov.b64 {%0, %1}, rs;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
@@ -204,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(B_PF + x), 128);
-      mbar_init(bar(B_OE + x), 128);
+      mbar_init(bar(B_PF + x), 4);  // one arrival per softmax warp of the tile
+      mbar_init(bar(B_OE + x), 4);
       mbar_init(bar(B_IE + x), 1 + 8);  // MMA thread + one lane of each softmax warp
     }
     ctl[1] = 0;
@@ -369,38 +391,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(false), id_o = idesc_bf16(true);
       uint32_t tile_cnt = 0, s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
+      // Operand descriptors of every buffer, built once: a descriptor's low
+      // field is the address / 16, so a k-step's offset is added to it.
+      const uint64_t dq0 = sdesc(sbase + kOffQ, 16), dq1 = sdesc(sbase + kOffQ + kTileBytes, 16);
+      const uint64_t dk0 = sdesc(sbase + kOffK, 16), dk1 = sdesc(sbase + kOffK + kTileBytes, 16);
+      const uint64_t dv0 = sdesc(sbase + kOffV, kHalfBytes);
+      const uint64_t dv1 = sdesc(sbase + kOffV + kTileBytes, kHalfBytes);
+      static_assert(kStages == 2, "one descriptor per stage");
       // S_x(c) = Q_x K_c^T
       auto issue_s = [&](int x, uint32_t c) {
-        const uint32_t qa = sbase + kOffQ + x * kTileBytes;
-        const uint32_t kb = sbase + kOffK + (c % kStages) * kTileBytes;
+        const uint64_t da = x ? dq1 : dq0, db = (c & 1) ? dk1 : dk0;
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + x * 128, sdesc(qa + off, 16), sdesc(kb + off, 16), id_s, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d, da + off, db + off, id_s, kk > 0);
         }
         mma_commit(bar(B_SF + x));
         s_cnt[x]++;
       };
       // O_x (+)= P_x V_c  (P_x: bf16 pairs in the first 64 columns of S_x)
       auto issue_pv = [&](int x, uint32_t c, bool acc) {
-        const uint32_t vb = sbase + kOffV + (c % kStages) * kTileBytes;
+        const uint64_t db = (c & 1) ? dv1 : dv0;
+        const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8,
-                 sdesc(vb + kk * 16 * 128, kHalfBytes), id_o, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, pa + kk * 8, db + ((kk * 16 * 128) >> 4), id_o, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
       for (uint32_t it_cnt = 0; ok; ++it_cnt) {
         const int slot = it_cnt & 1;
-        if (!mbar_wait(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+        if (!mbar_wait_inl(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
         const Item it = items[slot];
         mbar_arrive(bar(B_IE + slot));
         if (it.r < 0) break;
         const int nx = it.hb >= 0 ? 2 : 1;
         for (int x = 0; x < nx && ok; ++x)
-          ok = mbar_wait(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
+          ok = mbar_wait_inl(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
         const uint32_t c0 = tile_cnt;
-        if (!ok || !mbar_wait(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
+        if (!ok || !mbar_wait_inl(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
         tc_fence_after();
         for (int x = 0; x < nx; ++x) issue_s(x, c0);
         mma_commit(bar(B_KE + c0 % kStages));
@@ -409,16 +438,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < it.nkv && ok; ++j) {
           const uint32_t c = c0 + j;
           const bool more = j + 1 < it.nkv;
-          if (!mbar_wait(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
+          if (!mbar_wait_inl(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
             ok = false;
             break;
           }
           for (int x = 0; x < nx; ++x) {
-            if (!mbar_wait(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
+            if (!mbar_wait_inl(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
                 (j == 0 && o_cnt[x] > 0 &&
-                 !mbar_wait(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err)) ||
+                 !mbar_wait_inl(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err)) ||
                 (more && x == 0 &&
-                 !mbar_wait(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1, abort,
+                 !mbar_wait_inl(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1, abort,
                             ws.err))) {
               ok = false;
               break;
@@ -486,28 +515,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
         }
-        float mx[8];
+        // row maximum: four chains of three-input max (two scores per step)
+        float mx[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(sv[k], sv[k + 8]);
+        for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
 #pragma unroll
-        for (int i = 16; i < 128; i += 8)
+        for (int i = 12; i < 124; i += 8)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[i + k]);
-        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+          for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[124 + k]);
+        float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
         float alpha = 1.f;
         const bool resc = mt > m_used + kRescaleThreshold;
         if (resc) {
           alpha = fast_exp2(m_used - mt);  // 0 on the first tile
           m_used = mt;
         }
+        // p = exp2(s * scale * log2(e) - m) two columns at a time (packed fp32
+        // pairs for the multiply-add and the row sums); the bf16 pairs are
+        // packed over sv[0..63] (sv[2i], sv[2i+1] are read before sv[i] is written)
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
-        // packed bf16 pairs over sv[0..63] (sv[2i], sv[2i+1] read before sv[i] is written)
+        const float nm = -m_used;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = fast_exp2(fmaf(sv[2 * i], sl2, -m_used));
-          const float p1 = fast_exp2(fmaf(sv[2 * i + 1], sl2, -m_used));
-          rs[i & 3] += p0 + p1;
+          float x0, x1;
+          fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
           sv[i] = __uint_as_float(pack_bf16(p0, p1));
         }
         PKV_ST32(t_s + 0, (sv + 0));
@@ -527,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(B_PF + x));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PF + x));
       }
       if (!ok) break;
       // epilogue: O / l in bf16 to the output rows.  Each 32-column chunk of
@@ -583,7 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       tc_fence_before();
-      mbar_arrive(bar(B_OE + x));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_OE + x));
     }
   }
 
