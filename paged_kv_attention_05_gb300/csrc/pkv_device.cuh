@@ -85,7 +85,7 @@ __device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, vol
 // (warp-collective instructions follow it).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
                                                int* err) {
-  const bool ok = mbar_wait(bar, parity, abort, err);
+  const bool ok = mbar_wait_inl(bar, parity, abort, err);
   return __all_sync(0xffffffffu, ok);
 }
 
