@@ -445,16 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < nx; ++x) {
             if (!mbar_wait_inl(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
                 (j == 0 && o_cnt[x] > 0 &&
-                 !mbar_wait_inl(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err)) ||
-                (more && x == 0 &&
-                 !mbar_wait_inl(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1, abort,
-                            ws.err))) {
+                 !mbar_wait_inl(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err))) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_pv(x, c, j > 0);
+            if (x == nx - 1) mma_commit(bar(B_VE + c % kStages));  // every PV of V_c issued
             if (more) {
+              // the next K tile is waited for only now, with PV_x already queued
+              if (x == 0 && !mbar_wait_inl(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1,
+                                           abort, ws.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
               issue_s(x, c + 1);
             } else {
               mma_commit(bar(B_OF + x));  // O_x final: its epilogue need not wait for the other tile
@@ -462,7 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(bar(B_VE + c % kStages));
           if (more) {
             mma_commit(bar(B_KE + (c + 1) % kStages));
             if (j + 2 == it.nkv)
