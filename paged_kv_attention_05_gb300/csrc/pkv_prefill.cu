@@ -508,46 +508,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int lim = qpos - j * kTileK;  // columns <= lim are visible
         const bool masked = !__all_sync(0xffffffffu, lim >= kTileK - 1);
-        // the row's 128 scores in registers (one wait), max, then P in place
+        // the row's 128 scores in registers (one wait), then P in place
         float sv[128];
-        PKV_LD32(t_s + 0, (sv + 0));
-        PKV_LD32(t_s + 32, (sv + 32));
-        PKV_LD32(t_s + 64, (sv + 64));
-        PKV_LD32(t_s + 96, (sv + 96));
-        tmem_wait_ld();
-        if (masked) {
+        auto load_scores = [&]() {
+          PKV_LD32(t_s + 0, (sv + 0));
+          PKV_LD32(t_s + 32, (sv + 32));
+          PKV_LD32(t_s + 64, (sv + 64));
+          PKV_LD32(t_s + 96, (sv + 96));
+          tmem_wait_ld();
+          if (masked) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
-        }
-        // row maximum: four chains of three-input max (two scores per step)
-        float mx[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
-#pragma unroll
-        for (int i = 12; i < 124; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[124 + k]);
-        float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-        float alpha = 1.f;
-        const bool resc = mt > m_used + kRescaleThreshold;
-        if (resc) {
-          alpha = fast_exp2(m_used - mt);  // 0 on the first tile
-          m_used = mt;
-        }
+            for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+          }
+        };
         // p = exp2(s * scale * log2(e) - m) two columns at a time (packed fp32
         // pairs for the multiply-add and the row sums); the bf16 pairs are
         // packed over sv[0..63] (sv[2i], sv[2i+1] are read before sv[i] is written)
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
-        const float nm = -m_used;
+        float rs[4];
+        auto exp_pack = [&](float m) {
+          rs[0] = rs[1] = rs[2] = rs[3] = 0.f;
+          const float nm = -m;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float x0, x1;
-          fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
-          sv[i] = __uint_as_float(pack_bf16(p0, p1));
+          for (int i = 0; i < 64; ++i) {
+            float x0, x1;
+            fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
+            sv[i] = __uint_as_float(pack_bf16(p0, p1));
+          }
+        };
+        load_scores();
+        float alpha = 1.f;
+        bool resc = false;
+        // After the first tile, P is computed with the running max straight
+        // away: no p exceeds 2^8 (the rescale threshold) while the row sum
+        // does not, so the max pass is needed only when some row's sum does
+        // (or is not finite); then the warp reloads the scores and takes it.
+        bool fast = j > 0;
+        if (fast) {
+          exp_pack(m_used);
+          const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+          fast = __all_sync(0xffffffffu, tot <= 256.f);
+          if (!fast) load_scores();
+        }
+        if (!fast) {
+          // row maximum: four chains of three-input max (two scores per step)
+          float mx[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
+#pragma unroll
+          for (int i = 12; i < 124; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[124 + k]);
+          const float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
+          resc = mt > m_used + kRescaleThreshold;
+          if (resc) {
+            alpha = fast_exp2(m_used - mt);  // 0 on the first tile
+            m_used = mt;
+          }
+          exp_pack(m_used);
         }
         PKV_ST32(t_s + 0, (sv + 0));
         PKV_ST32(t_s + 32, (sv + 32));

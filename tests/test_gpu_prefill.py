@@ -129,3 +129,25 @@ def test_large_prefill_sampled_rows():
     assert err == 0
     assert_close(got[rows, heads], ref, "large_prefill sampled")
     assert np.isfinite(got).all()
+
+
+def test_prefill_scores_growing_along_the_keys():
+    """Scores that rise steadily along the keys (by about 2^8 in the log2
+    domain every 128 keys): the running maximum grows past the rescale
+    threshold inside most key tiles, so the max pass, the reload of the scores
+    and the rescale of O run on most tiles, next to tiles that take the
+    single-pass route."""
+    step = W.build(W.custom([600, 0], [300, 700], 4, 2, seed=21))
+    u = np.full(128, 0.5, dtype=np.float32)
+    step.q[:] = W.bf16_bits(u)[None, None, :]
+    R = step.num_reqs
+    for r in range(R):
+        ctx = int(step.seq_lens[r]) - int(step.query_start_loc[r + 1] - step.query_start_loc[r])
+        for pos in range(int(step.seq_lens[r])):
+            kv = W.bf16_bits(u * np.float32(pos / 64.0))
+            if pos < ctx:
+                blk = step.block_table[r, pos // 16]
+                step.key_cache[blk, pos % 16, :, :] = kv[None, :]
+            else:
+                step.k[step.query_start_loc[r] + pos - ctx, :, :] = kv[None, :]
+    run_and_check(step, "growing scores")
