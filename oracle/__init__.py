@@ -9,7 +9,8 @@ no arithmetic of the method.
 
 Contents:
   * ``oracle.c`` / ``liboracle.so`` — cache write and paged causal attention in
-    float64 (ctypes wrappers below);
+    float64, for bf16 caches and for int8 caches with one scale each (ctypes
+    wrappers below);
   * ``blocks.py`` — the block/slot arithmetic the pages print;
   * ``brute.py`` — dense causal attention on contiguous K/V, the textbook form
     the paged oracle must reduce to.
@@ -45,6 +46,13 @@ def lib():
         L.oracle_attention_sampled.restype = i32
         L.oracle_attention_sampled.argtypes = [vp, i64, i64, i32, vp, vp, i64, i32, i32, i32,
                                                vp, vp, vp, i64, i64, i32, dbl, vp, vp, i64, vp]
+        f32 = ctypes.c_float
+        L.oracle_write_int8.restype = i32
+        L.oracle_write_int8.argtypes = [vp, i64, vp, i64, vp, vp, i64, i32, i32, i32, vp, i64,
+                                        f32, f32]
+        L.oracle_attention_int8.restype = i32
+        L.oracle_attention_int8.argtypes = [vp, i64, i64, i32, vp, vp, dbl, dbl, i64, i32, i32,
+                                            i32, vp, vp, vp, i64, i64, i32, dbl, vp, i64]
         L.oracle_num_threads.restype = i32
         L.oracle_set_num_threads.argtypes = [i32]
         _lib = L
@@ -89,6 +97,22 @@ def write(k, v, key_cache, value_cache, slot_mapping):
                               _ptr(slot_mapping), n)
 
 
+def write_int8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_scale):
+    """The cache write into int8 caches ([num_blocks, bs, hkv, d] int8,
+    modified in place): code = clamp(rne(x / scale), -127, 127) in fp32.
+    Returns the error bits."""
+    assert k.dtype == np.uint16 and v.dtype == np.uint16
+    assert key_cache.dtype == np.int8 and key_cache.flags.c_contiguous
+    assert value_cache.dtype == np.int8 and value_cache.flags.c_contiguous
+    slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    nb, bs, hkv, d = key_cache.shape
+    n = slot_mapping.shape[0]
+    assert k.shape[0] >= n and v.shape[0] >= n
+    return lib().oracle_write_int8(_ptr(k), _rows(k), _ptr(v), _rows(v), _ptr(key_cache),
+                                   _ptr(value_cache), nb, bs, hkv, d, _ptr(slot_mapping), n,
+                                   float(np.float32(k_scale)), float(np.float32(v_scale)))
+
+
 def _meta(query_start_loc, seq_lens, block_table):
     qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -115,6 +139,27 @@ def attention(q, key_cache, value_cache, query_start_loc, seq_lens, block_table,
                                  _ptr(value_cache), nb, bs, hkv, d, _ptr(qsl), _ptr(sl),
                                  _ptr(bt), bt.shape[1], bt.shape[1], int(num_reqs),
                                  float(scale), _ptr(out), hq * d)
+    return out, err
+
+
+def attention_int8(q, key_cache, value_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                   block_table, num_reqs, scale, out=None):
+    """Paged causal attention in float64 over int8 caches (K = code * k_scale,
+    V = code * v_scale); returns (out float64 [T, hq, d], error bits)."""
+    assert q.dtype == np.uint16 and q.ndim == 3
+    assert key_cache.dtype == np.int8 and value_cache.dtype == np.int8
+    T, hq, d = q.shape
+    nb, bs, hkv, d2 = key_cache.shape
+    assert d == d2
+    qsl, sl, bt = _meta(query_start_loc, seq_lens, block_table)
+    if out is None:
+        out = np.full((T, hq, d), np.nan, dtype=np.float64)
+    assert out.dtype == np.float64 and out.flags.c_contiguous and out.shape == (T, hq, d)
+    err = lib().oracle_attention_int8(_ptr(q), _rows(q), T, hq, _ptr(key_cache),
+                                      _ptr(value_cache), float(np.float32(k_scale)),
+                                      float(np.float32(v_scale)), nb, bs, hkv, d, _ptr(qsl),
+                                      _ptr(sl), _ptr(bt), bt.shape[1], bt.shape[1],
+                                      int(num_reqs), float(scale), _ptr(out), hq * d)
     return out, err
 
 

@@ -38,6 +38,14 @@
  *
  * Numbers: bf16 inputs are widened exactly to double; every sum, the max,
  * exp and the division run in double, in the order of the definition.
+ *
+ * int8 KV cache ("vLLM 推理全流程深度解析", the closing note of the
+ * paged_attention section names KV-cache int8 quantisation as a decode
+ * speed-up and gives no format).  Reading: one fp32 scale per cache (per
+ * layer) and symmetric codes, code = clamp(rne(x / scale), -127, 127) with x
+ * the bf16 value widened to fp32 and the division done in fp32 (a NaN input
+ * gives code 0); the cached value is code * scale.  Attention over an int8
+ * cache is the definition above with those values as K and V.
  */
 #include <math.h>
 #include <stdint.h>
@@ -106,6 +114,52 @@ int oracle_write(const uint16_t *k, int64_t k_row_stride, const uint16_t *v,
   return err;
 }
 
+/* One int8 code: the reading stated in the header, in fp32. */
+static int8_t quantize_int8(uint16_t bits, float scale) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float x;
+  memcpy(&x, &w, sizeof x);
+  float r = rintf(x / scale); /* fp32 division, round half to even */
+  if (r != r) return 0;       /* NaN */
+  if (r > 127.0f) r = 127.0f;
+  if (r < -127.0f) r = -127.0f;
+  return (int8_t)r;
+}
+
+/* The cache write into int8 caches: the same placement as oracle_write, each
+ * element stored as its code. */
+int oracle_write_int8(const uint16_t *k, int64_t k_row_stride, const uint16_t *v,
+                      int64_t v_row_stride, int8_t *key_cache, int8_t *value_cache,
+                      int64_t num_blocks, int block_size, int hkv, int d,
+                      const int64_t *slot_mapping, int64_t n_tokens, float k_scale,
+                      float v_scale) {
+  int err = 0;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue; /* padding token */
+    int64_t block = slot / block_size;
+    int64_t offset = slot % block_size;
+    if (block >= num_blocks) {
+      err |= ORC_ERR_SLOT_RANGE;
+      continue;
+    }
+    for (int h = 0; h < hkv; ++h) {
+      for (int e = 0; e < d; ++e) {
+        int64_t dst = ((block * block_size + offset) * hkv + h) * d + e;
+        key_cache[dst] = quantize_int8(k[t * k_row_stride + (int64_t)h * d + e], k_scale);
+        value_cache[dst] = quantize_int8(v[t * v_row_stride + (int64_t)h * d + e], v_scale);
+      }
+    }
+  }
+  return err;
+}
+
+/* Element idx of a cache: a bf16 value, or an int8 code times the scale. */
+static double kv_value(const void *cache, int64_t idx, int kv_int8, double scale) {
+  if (kv_int8) return (double)((const int8_t *)cache)[idx] * scale;
+  return bf16_to_double(((const uint16_t *)cache)[idx]);
+}
+
 /* Checks one request against the contract; returns its error bits. */
 static int check_request(const int32_t *qsl, const int32_t *seq_lens,
                          const int32_t *block_table, int64_t bt_row_stride,
@@ -126,7 +180,8 @@ static int check_request(const int32_t *qsl, const int32_t *seq_lens,
 /* One output row: request r, query row i (absolute position ctx + i),
  * query head h.  scores is scratch of at least ctx + i + 1 doubles. */
 static void attend_one(const uint16_t *q, int64_t q_row_stride, int hq,
-                       const uint16_t *key_cache, const uint16_t *value_cache,
+                       const void *key_cache, const void *value_cache, int kv_int8,
+                       double k_scale, double v_scale,
                        int block_size, int hkv, int d, const int32_t *qsl,
                        const int32_t *seq_lens, const int32_t *block_table,
                        int64_t bt_row_stride, int r, int64_t i, int h,
@@ -143,10 +198,10 @@ static void attend_one(const uint16_t *q, int64_t q_row_stride, int hq,
   for (int64_t j = 0; j <= last; ++j) {
     int64_t block = block_table[(int64_t)r * bt_row_stride + j / block_size];
     int64_t offset = j % block_size;
-    const uint16_t *krow =
-        key_cache + ((block * block_size + offset) * hkv + g) * d;
+    int64_t krow = ((block * block_size + offset) * hkv + g) * d;
     double s = 0.0;
-    for (int e = 0; e < d; ++e) s += bf16_to_double(qrow[e]) * bf16_to_double(krow[e]);
+    for (int e = 0; e < d; ++e)
+      s += bf16_to_double(qrow[e]) * kv_value(key_cache, krow + e, kv_int8, k_scale);
     s *= scale;
     scores[j] = s;
     if (s > m) m = s;
@@ -160,10 +215,10 @@ static void attend_one(const uint16_t *q, int64_t q_row_stride, int hq,
   for (int64_t j = 0; j <= last; ++j) {
     int64_t block = block_table[(int64_t)r * bt_row_stride + j / block_size];
     int64_t offset = j % block_size;
-    const uint16_t *vrow =
-        value_cache + ((block * block_size + offset) * hkv + g) * d;
+    int64_t vrow = ((block * block_size + offset) * hkv + g) * d;
     double p = scores[j] / l;
-    for (int e = 0; e < d; ++e) out_row[e] += p * bf16_to_double(vrow[e]);
+    for (int e = 0; e < d; ++e)
+      out_row[e] += p * kv_value(value_cache, vrow + e, kv_int8, v_scale);
   }
 }
 
@@ -175,14 +230,14 @@ static void attend_one(const uint16_t *q, int64_t q_row_stride, int hq,
  * out: double [n_rows, hq, d] with row stride out_row_stride; rows that no
  * valid request covers are left as they are.  Returns the OR of the error
  * bits of the requests that were skipped. */
-int oracle_attention(const uint16_t *q, int64_t q_row_stride, int64_t n_rows,
-                     int hq, const uint16_t *key_cache,
-                     const uint16_t *value_cache, int64_t num_blocks,
-                     int block_size, int hkv, int d,
-                     const int32_t *query_start_loc, const int32_t *seq_lens,
-                     const int32_t *block_table, int64_t bt_row_stride,
-                     int64_t bt_width, int num_reqs, double scale, double *out,
-                     int64_t out_row_stride) {
+static int attention_impl(const uint16_t *q, int64_t q_row_stride, int64_t n_rows,
+                          int hq, const void *key_cache, const void *value_cache,
+                          int kv_int8, double k_scale, double v_scale, int64_t num_blocks,
+                          int block_size, int hkv, int d,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          const int32_t *block_table, int64_t bt_row_stride,
+                          int64_t bt_width, int num_reqs, double scale, double *out,
+                          int64_t out_row_stride) {
   if (hkv <= 0 || hq % hkv != 0) return -1;
   int err = 0;
   int *valid = (int *)malloc(sizeof(int) * (num_reqs > 0 ? num_reqs : 1));
@@ -208,15 +263,44 @@ int oracle_attention(const uint16_t *q, int64_t q_row_stride, int64_t n_rows,
       for (int64_t i = 0; i < n; ++i) {
         double *orow = out + ((int64_t)query_start_loc[r] + i) * out_row_stride +
                        (int64_t)h * d;
-        attend_one(q, q_row_stride, hq, key_cache, value_cache, block_size,
-                   hkv, d, query_start_loc, seq_lens, block_table,
-                   bt_row_stride, r, i, h, scale, scores, orow);
+        attend_one(q, q_row_stride, hq, key_cache, value_cache, kv_int8, k_scale,
+                   v_scale, block_size, hkv, d, query_start_loc, seq_lens,
+                   block_table, bt_row_stride, r, i, h, scale, scores, orow);
       }
     }
     free(scores);
   }
   free(valid);
   return err;
+}
+
+int oracle_attention(const uint16_t *q, int64_t q_row_stride, int64_t n_rows,
+                     int hq, const uint16_t *key_cache,
+                     const uint16_t *value_cache, int64_t num_blocks,
+                     int block_size, int hkv, int d,
+                     const int32_t *query_start_loc, const int32_t *seq_lens,
+                     const int32_t *block_table, int64_t bt_row_stride,
+                     int64_t bt_width, int num_reqs, double scale, double *out,
+                     int64_t out_row_stride) {
+  return attention_impl(q, q_row_stride, n_rows, hq, key_cache, value_cache, 0, 1.0, 1.0,
+                        num_blocks, block_size, hkv, d, query_start_loc, seq_lens,
+                        block_table, bt_row_stride, bt_width, num_reqs, scale, out,
+                        out_row_stride);
+}
+
+/* The same attention over int8 caches: K = code * k_scale, V = code * v_scale. */
+int oracle_attention_int8(const uint16_t *q, int64_t q_row_stride, int64_t n_rows,
+                          int hq, const int8_t *key_cache, const int8_t *value_cache,
+                          double k_scale, double v_scale, int64_t num_blocks,
+                          int block_size, int hkv, int d,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          const int32_t *block_table, int64_t bt_row_stride,
+                          int64_t bt_width, int num_reqs, double scale, double *out,
+                          int64_t out_row_stride) {
+  return attention_impl(q, q_row_stride, n_rows, hq, key_cache, value_cache, 1, k_scale,
+                        v_scale, num_blocks, block_size, hkv, d, query_start_loc,
+                        seq_lens, block_table, bt_row_stride, bt_width, num_reqs, scale,
+                        out, out_row_stride);
 }
 
 /* The same definition evaluated only at chosen (token row, query head)
@@ -255,8 +339,8 @@ int oracle_attention_sampled(const uint16_t *q, int64_t q_row_stride,
       continue;
     }
     double *scores = (double *)malloc(sizeof(double) * (size_t)(seq_lens[req] + 1));
-    attend_one(q, q_row_stride, hq, key_cache, value_cache, block_size, hkv, d,
-               query_start_loc, seq_lens, block_table, bt_row_stride, req,
+    attend_one(q, q_row_stride, hq, key_cache, value_cache, 0, 1.0, 1.0, block_size, hkv,
+               d, query_start_loc, seq_lens, block_table, bt_row_stride, req,
                rows[s] - query_start_loc[req], heads[s], scale, scores, orow);
     free(scores);
   }

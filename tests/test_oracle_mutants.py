@@ -15,7 +15,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
-PINS = ["tests/test_oracle_attention.py", "tests/test_oracle_write.py"]
+PINS = ["tests/test_oracle_attention.py", "tests/test_oracle_write.py",
+        "tests/test_oracle_int8.py"]
 
 # (name, text in oracle.c, replacement, occurrence to replace: 0-based or None for all)
 MUTANTS = [
@@ -30,12 +31,20 @@ MUTANTS = [
      "block_table[(int64_t)r * bt_row_stride + j % block_size]", 0),
     ("value-block-index", "block_table[(int64_t)r * bt_row_stride + j / block_size]",
      "block_table[(int64_t)r * bt_row_stride + (j + 1) / block_size]", 1),
-    ("value-head-zero", "value_cache + ((block * block_size + offset) * hkv + g) * d",
-     "value_cache + ((block * block_size + offset) * hkv + 0) * d", None),
+    ("value-head-zero", "int64_t vrow = ((block * block_size + offset) * hkv + g) * d;",
+     "int64_t vrow = ((block * block_size + offset) * hkv + 0) * d;", None),
     ("write-offset-zero", "int64_t offset = slot % block_size;", "int64_t offset = 0;", None),
     ("write-v-from-k", "value_cache[dst] = v[", "value_cache[dst] = k[", None),
     ("write-head-stride", "int64_t dst = ((block * block_size + offset) * hkv + h) * d + e;",
      "int64_t dst = ((block * block_size + offset) * hkv) * d + e;", None),
+    ("int8-truncates", "float r = rintf(x / scale);", "float r = truncf(x / scale);", None),
+    ("int8-rounds-half-up", "float r = rintf(x / scale);", "float r = floorf(x / scale + 0.5f);",
+     None),
+    ("int8-no-clamp", "if (r > 127.0f) r = 127.0f;", "", None),
+    ("int8-v-dequant-k-scale", "kv_value(value_cache, vrow + e, kv_int8, v_scale)",
+     "kv_value(value_cache, vrow + e, kv_int8, k_scale)", None),
+    ("int8-write-v-k-scale", "quantize_int8(v[t * v_row_stride + (int64_t)h * d + e], v_scale)",
+     "quantize_int8(v[t * v_row_stride + (int64_t)h * d + e], k_scale)", None),
 ]
 
 
