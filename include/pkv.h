@@ -60,6 +60,8 @@ extern "C" {
 #define PKV_DEV_ERR_BT_WIDTH 8   /* ceil(seq_len/block_size) > row width      */
 #define PKV_DEV_ERR_BLOCK_ID 16  /* block id outside [0, num_blocks)          */
 #define PKV_DEV_ERR_TIMEOUT 32   /* an on-chip pipeline wait gave up          */
+#define PKV_DEV_ERR_INT8_PREFILL 64 /* pkv_attention_int8: a request too long for
+                                       the decode path (its rows are skipped)  */
 
 /*
  * pkv_write — the cache-write scatter.
@@ -172,6 +174,48 @@ int pkv_prepare_step(const int32_t* query_start_loc, const int32_t* num_computed
                      int64_t persistent_rows, int64_t block_table_width, int32_t num_reqs,
                      int64_t num_tokens_padded, int64_t* positions, int32_t* seq_lens,
                      int64_t* slot_mapping, int32_t* block_table, void* stream);
+
+/*
+ * pkv_write_int8 — the cache-write scatter into int8 caches.
+ *
+ * "vLLM 推理全流程深度解析", the closing note of the paged_attention section,
+ * names KV-cache int8 quantisation as a decode speed-up without giving a
+ * format.  This library's format: one fp32 scale per cache (per layer) and
+ * symmetric codes, code = clamp(rne(x / scale), -127, 127), x the bf16 value
+ * widened to fp32 and the division the IEEE fp32 one (a NaN value gives
+ * code 0); the cached value stands for code * scale.
+ *
+ * Placement, padding, slot checks, arguments and alignment are those of
+ * pkv_write; key_cache and value_cache are int8 [num_blocks, block_size,
+ * num_kv_heads, head_size], contiguous, 16-byte aligned.  k_scale and
+ * v_scale must be finite and positive (else PKV_ERR_ARG).
+ */
+int pkv_write_int8(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                   void* key_cache, void* value_cache, float k_scale, float v_scale,
+                   int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_size, const int64_t* slot_mapping, int64_t n_tokens,
+                   void* stream);
+
+/*
+ * pkv_attention_int8 — pkv_attention over int8 caches written by
+ * pkv_write_int8: the same formula with K_j = k_scale * code and V_j =
+ * v_scale * code.  The codes are widened to bf16 exactly on chip; k_scale is
+ * folded into the softmax scale and v_scale into the output.
+ *
+ * Requests on the decode path only: a request whose query_len * (num_heads /
+ * num_kv_heads) is at most 16 (32 when the group is larger than 16) —
+ * single-token and short multi-token decodes.  A longer request is skipped
+ * (its output rows are not written) and reported as
+ * PKV_DEV_ERR_INT8_PREFILL.  Other arguments, layouts, checks and errors are
+ * those of pkv_attention; k_scale and v_scale must be finite and positive.
+ */
+int pkv_attention_int8(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
+                       const void* key_cache, const void* value_cache, float k_scale,
+                       float v_scale, int64_t num_blocks, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_size, const int32_t* query_start_loc,
+                       const int32_t* seq_lens, const int32_t* block_table,
+                       int64_t block_table_width, int32_t num_reqs, float scale, void* out,
+                       int64_t out_row_stride, void* stream);
 
 /*
  * pkv_attention_noalloc — pkv_attention for callers that cannot allocate

@@ -13,11 +13,12 @@ DEV_ERR_BITS = {
     "BT_WIDTH": 8,
     "BLOCK_ID": 16,
     "TIMEOUT": 32,
+    "INT8_PREFILL": 64,
 }
 
 EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
            "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
-           "pkv_launch_count", "pkv_prepare_step"]
+           "pkv_launch_count", "pkv_prepare_step", "pkv_write_int8", "pkv_attention_int8"]
 TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine", "prepare"]
 
 
@@ -45,6 +46,13 @@ def load():
     L.pkv_attention.restype = ctypes.c_int
     L.pkv_attention.argtypes = [vp, i64, i64, i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64,
                                 i32, f32, vp, i64, vp]
+    f32 = ctypes.c_float
+    L.pkv_write_int8.restype = ctypes.c_int
+    L.pkv_write_int8.argtypes = [vp, i64, vp, i64, vp, vp, f32, f32, i64, i32, i32, i32, vp, i64,
+                                 vp]
+    L.pkv_attention_int8.restype = ctypes.c_int
+    L.pkv_attention_int8.argtypes = [vp, i64, i64, i32, vp, vp, f32, f32, i64, i32, i32, i32, vp,
+                                     vp, vp, i64, i32, f32, vp, i64, vp]
     L.pkv_reserve_workspace.restype = ctypes.c_int
     L.pkv_reserve_workspace.argtypes = [i32, i64, i64, i32, i32]
     L.pkv_get_error.restype = ctypes.c_int
@@ -151,6 +159,68 @@ def pkv_attention(q, key_cache, value_cache, query_start_loc, seq_lens, block_ta
                                 query_start_loc.data_ptr(), seq_lens.data_ptr(),
                                 block_table.data_ptr(), bt_width, int(num_reqs), float(scale),
                                 out.data_ptr(), _rows3(out, "out"), _stream(stream)))
+
+
+def _caches(key_cache, value_cache, dtype):
+    import torch
+    for t, n in ((key_cache, "key_cache"), (value_cache, "value_cache")):
+        _require(t, dtype, n)
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
+    if key_cache.shape != value_cache.shape:
+        raise ValueError("key_cache and value_cache shapes differ")
+    return key_cache.shape
+
+
+def pkv_write_int8(k, v, key_cache, value_cache, slot_mapping, k_scale, v_scale, n_tokens=None,
+                   stream=None):
+    """Quantises k/v ([n, Hkv, 128] bf16) into the int8 caches at slot_mapping:
+    code = clamp(rne(x / scale), -127, 127), one fp32 scale per cache."""
+    import torch
+    _require(k, torch.bfloat16, "k")
+    _require(v, torch.bfloat16, "v")
+    nb, bs, hkv, d = _caches(key_cache, value_cache, torch.int8)
+    _require(slot_mapping, torch.int64, "slot_mapping")
+    if not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous")
+    n = slot_mapping.shape[0] if n_tokens is None else int(n_tokens)
+    if n > slot_mapping.shape[0] or n > k.shape[0] or n > v.shape[0]:
+        raise ValueError("n_tokens exceeds the rows of k/v/slot_mapping")
+    _check(load().pkv_write_int8(k.data_ptr(), _rows3(k, "k"), v.data_ptr(), _rows3(v, "v"),
+                                 key_cache.data_ptr(), value_cache.data_ptr(), float(k_scale),
+                                 float(v_scale), nb, bs, hkv, d, slot_mapping.data_ptr(), n,
+                                 _stream(stream)))
+
+
+def pkv_attention_int8(q, key_cache, value_cache, k_scale, v_scale, query_start_loc, seq_lens,
+                       block_table, num_reqs, scale, out, stream=None):
+    """pkv_attention over int8 caches (K = code * k_scale, V = code * v_scale),
+    decode-path requests only; see include/pkv.h."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require(out, torch.bfloat16, "out")
+    nb, bs, hkv, d = _caches(key_cache, value_cache, torch.int8)
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                 (block_table, "block_table")):
+        _require(t, torch.int32, n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    if q.dim() != 3:
+        raise ValueError("q must be [rows, num_heads, head_size]")
+    rows, hq, _ = q.shape
+    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+        raise ValueError("out must hold [rows, num_heads * head_size]")
+    bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
+    if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
+                              seq_lens.numel() < int(num_reqs) or
+                              (block_table.dim() == 2 and block_table.shape[0] < int(num_reqs))):
+        raise ValueError("metadata shorter than num_reqs")
+    _check(load().pkv_attention_int8(q.data_ptr(), _rows3(q, "q"), rows, hq, key_cache.data_ptr(),
+                                     value_cache.data_ptr(), float(k_scale), float(v_scale), nb,
+                                     bs, hkv, d, query_start_loc.data_ptr(), seq_lens.data_ptr(),
+                                     block_table.data_ptr(), bt_width, int(num_reqs),
+                                     float(scale), out.data_ptr(), _rows3(out, "out"),
+                                     _stream(stream)))
 
 
 def pkv_reserve_workspace(max_reqs, max_q_rows, block_table_width, num_heads, num_kv_heads):

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/pkv.h: argument checks, the
 // per-device workspace and error word, and the kernel launches.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -230,13 +231,55 @@ extern "C" int pkv_write(const void* k, int64_t k_row_stride, const void* v,
   return PKV_OK;
 }
 
-extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows,
-                             int32_t num_heads, const void* key_cache, const void* value_cache,
-                             int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                             int32_t head_size, const int32_t* query_start_loc,
-                             const int32_t* seq_lens, const int32_t* block_table,
-                             int64_t block_table_width, int32_t num_reqs, float scale, void* out,
-                             int64_t out_row_stride, void* stream) {
+extern "C" int pkv_write_int8(const void* k, int64_t k_row_stride, const void* v,
+                              int64_t v_row_stride, void* key_cache, void* value_cache,
+                              float k_scale, float v_scale, int64_t num_blocks,
+                              int32_t block_size, int32_t num_kv_heads, int32_t head_size,
+                              const int64_t* slot_mapping, int64_t n_tokens, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_geometry(block_size, num_kv_heads, head_size);
+  if (rc) return rc;
+  if (n_tokens < 0) return fail(PKV_ERR_ARG, "n_tokens %lld < 0", (long long)n_tokens);
+  if (num_blocks < 1) return fail(PKV_ERR_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (!(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+    return fail(PKV_ERR_ARG, "k_scale and v_scale must be finite and positive");
+  if (n_tokens == 0) return PKV_OK;
+  if (!k || !v || !key_cache || !value_cache || !slot_mapping)
+    return fail(PKV_ERR_ARG, "null pointer argument");
+  const int64_t row = (int64_t)num_kv_heads * kHeadSize;
+  if (k_row_stride < row || v_row_stride < row)
+    return fail(PKV_ERR_ARG, "row stride below num_kv_heads * head_size (%lld)", (long long)row);
+  if (!aligned16(k) || !aligned16(v) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      (k_row_stride % 8) || (v_row_stride % 8))
+    return fail(PKV_ERR_ALIGN, "k/v/caches must be 16-byte aligned with row strides * 2 a "
+                               "multiple of 16 bytes");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced(0, st, [&] {
+    return launch_write_int8(static_cast<const uint16_t*>(k), k_row_stride,
+                             static_cast<const uint16_t*>(v), v_row_stride,
+                             static_cast<int8_t*>(key_cache), static_cast<int8_t*>(value_cache),
+                             num_blocks, num_kv_heads, slot_mapping, n_tokens, k_scale, v_scale,
+                             s->err, s->sms, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_write_int8 launch");
+  return PKV_OK;
+}
+
+namespace {
+
+// pkv_attention and pkv_attention_int8: kv_int8 = 0 for bf16 caches, 1 for
+// int8 codes with the two scales (decode-class requests only).
+int attention_common(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
+                     const void* key_cache, const void* value_cache, int64_t num_blocks,
+                     int32_t block_size, int32_t num_kv_heads, int32_t head_size,
+                     const int32_t* query_start_loc, const int32_t* seq_lens,
+                     const int32_t* block_table, int64_t block_table_width, int32_t num_reqs,
+                     float scale, void* out, int64_t out_row_stride, void* stream, int kv_int8,
+                     float k_scale, float v_scale) {
   g_msg[0] = 0;
   int rc = check_geometry(block_size, num_kv_heads, head_size);
   if (rc) return rc;
@@ -265,6 +308,8 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
     return fail(PKV_ERR_ALIGN, "q/out/caches must be 16-byte aligned with row strides * 2 a "
                                "multiple of 16 bytes");
   if (!(scale == scale)) return fail(PKV_ERR_ARG, "scale is NaN");
+  if (kv_int8 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+    return fail(PKV_ERR_ARG, "k_scale and v_scale must be finite and positive");
 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState* s = nullptr;
@@ -293,6 +338,9 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
   a.scale = scale;
   a.out = static_cast<uint16_t*>(out);
   a.out_stride = out_row_stride;
+  a.kv_int8 = kv_int8;
+  a.k_scale = kv_int8 ? k_scale : 1.f;
+  a.v_scale = kv_int8 ? v_scale : 1.f;
 
   const int workers = decode_workers(num_heads / num_kv_heads, s->sms);
   cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
@@ -301,9 +349,40 @@ extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (!kv_int8) {  // an int8 call has no prefill work (the plan reports such requests)
+    e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows,
+                             int32_t num_heads, const void* key_cache, const void* value_cache,
+                             int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_size, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, const int32_t* block_table,
+                             int64_t block_table_width, int32_t num_reqs, float scale, void* out,
+                             int64_t out_row_stride, void* stream) {
+  return attention_common(q, q_row_stride, q_rows, num_heads, key_cache, value_cache, num_blocks,
+                          block_size, num_kv_heads, head_size, query_start_loc, seq_lens,
+                          block_table, block_table_width, num_reqs, scale, out, out_row_stride,
+                          stream, 0, 1.f, 1.f);
+}
+
+extern "C" int pkv_attention_int8(const void* q, int64_t q_row_stride, int64_t q_rows,
+                                  int32_t num_heads, const void* key_cache,
+                                  const void* value_cache, float k_scale, float v_scale,
+                                  int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                  int32_t head_size, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, const int32_t* block_table,
+                                  int64_t block_table_width, int32_t num_reqs, float scale,
+                                  void* out, int64_t out_row_stride, void* stream) {
+  return attention_common(q, q_row_stride, q_rows, num_heads, key_cache, value_cache, num_blocks,
+                          block_size, num_kv_heads, head_size, query_start_loc, seq_lens,
+                          block_table, block_table_width, num_reqs, scale, out, out_row_stride,
+                          stream, 1, k_scale, v_scale);
 }
 
 extern "C" int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows,

@@ -82,6 +82,10 @@ cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,
                          uint16_t* kc, uint16_t* vc, int64_t num_blocks, int hkv,
                          const int64_t* slots, int64_t n_tokens, int* err, int sms,
                          cudaStream_t st);
+cudaError_t launch_write_int8(const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                              int64_t v_stride, int8_t* kc, int8_t* vc, int64_t num_blocks,
+                              int hkv, const int64_t* slots, int64_t n_tokens, float k_scale,
+                              float v_scale, int* err, int sms, cudaStream_t st);
 
 struct AttnArgs {
   const uint16_t* q;
@@ -100,6 +104,11 @@ struct AttnArgs {
   float scale;
   uint16_t* out;
   int64_t out_stride;
+  // int8 caches (kc / vc then point at int8 codes): K = code * k_scale,
+  // V = code * v_scale; decode-class requests only
+  int kv_int8;
+  float k_scale;
+  float v_scale;
 };
 
 // TMA descriptors (pkv_tma.cu).  rows map: [rows, heads, 128] bf16 with a row
@@ -107,6 +116,9 @@ struct AttnArgs {
 // hkv, 128] bf16, box = 64 columns x 1 head x 16 slots x 1 block.  Both use
 // the 128-byte swizzle.
 bool tma_available();
+// int8 cache map: [num_blocks, 16, hkv, 128] int8, box = 128 codes x 1 head x
+// 16 slots x 1 block (one 2 KB box per page), 128-byte swizzle.
+bool make_cache_map_i8(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv);
 bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t row_stride,
                    int box_heads, int box_rows);
 bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv);

@@ -90,6 +90,10 @@ __device__ ReqInfo classify(const AttnArgs& a, int r) {
   // (speculative / multi-token decode included); prefill: anything longer
   const int G = a.hq / a.hkv;
   ri.kind = ri.n == 0 ? 0 : (ri.n * G <= dec_rows_cap(G) ? 1 : 2);
+  if (ri.kind == 2 && a.kv_int8) {  // int8 caches are read by the decode path only
+    ri.kind = 0;
+    ri.bad = PKV_DEV_ERR_INT8_PREFILL;
+  }
   return ri;
 }
 

@@ -176,28 +176,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                              \
       : "memory")
 
-// max(a, b, c) in one instruction
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-// (d0, d1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed fp32-pair instruction
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                     float c0, float c1) {
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-// (s0, s1) += (a0, a1) as one packed fp32-pair instruction
-__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
-  asm("{\n .reg .b64 rs, ra;\n mov.b64 rs, {%0, %1};\n mov.b64 ra, {%2, %3};\n"
-      " add.rn.f32x2 rs, rs, ra;\n mov.b64 {%0, %1}, rs;\n}\n"
-      : "+f"(s0), "+f"(s1)
-      : "f"(a0), "f"(a1));
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }

@@ -53,4 +53,18 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hk
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_cache_map_i8(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv) {
+  if (!encode_fn()) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadSize, (cuuint64_t)hkv, (cuuint64_t)kBlockSize,
+                        (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)kHeadSize, (cuuint64_t)hkv * kHeadSize,
+                           (cuuint64_t)hkv * kHeadSize * kBlockSize};
+  cuuint32_t box[4] = {(cuuint32_t)kHeadSize, 1, (cuuint32_t)kBlockSize, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pkv

@@ -47,7 +47,71 @@ __global__ void __launch_bounds__(256) write_kernel(const uint16_t* __restrict__
   }
 }
 
+// The same scatter into int8 caches: each thread turns 16 bf16 values (two
+// 16-byte loads) into 16 codes (one 16-byte store), code = clamp(rne(x /
+// scale), -127, 127) in fp32 with the IEEE division (a NaN value gives 0).
+__device__ __forceinline__ uint32_t quant4(uint32_t lo, uint32_t hi, float scale) {
+  const float x[4] = {__uint_as_float(lo << 16), __uint_as_float(lo & 0xFFFF0000u),
+                      __uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u)};
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float r = rintf(__fdiv_rn(x[i], scale));
+    r = (r == r) ? fminf(fmaxf(r, -127.f), 127.f) : 0.f;
+    w |= ((uint32_t)(int)r & 0xFFu) << (8 * i);
+  }
+  return w;
+}
+
+__global__ void __launch_bounds__(256) write_int8_kernel(
+    const uint16_t* __restrict__ k, int64_t k_stride, const uint16_t* __restrict__ v,
+    int64_t v_stride, int8_t* __restrict__ kc, int8_t* __restrict__ vc, int64_t num_slots,
+    int row_vecs, const int64_t* __restrict__ slots, int64_t n_tokens, float k_scale,
+    float v_scale, int* err) {
+  // row_vecs = 16-code vectors per token row = num_kv_heads * 128 / 16
+  const int64_t per_token = 2 * (int64_t)row_vecs;
+  const int64_t total = n_tokens * per_token;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int rem = (int)(i - t * per_token);
+    const bool is_v = rem >= row_vecs;
+    const int vec = is_v ? rem - row_vecs : rem;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (rem == 0) atomicOr(err, PKV_DEV_ERR_SLOT_RANGE);
+      continue;
+    }
+    const uint16_t* src = (is_v ? v + t * v_stride : k + t * k_stride) + (int64_t)vec * 16;
+    int8_t* dst = (is_v ? vc : kc) + slot * (int64_t)row_vecs * 16 + (int64_t)vec * 16;
+    const float sc = is_v ? v_scale : k_scale;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+    *reinterpret_cast<uint4*>(dst) =
+        make_uint4(quant4(a.x, a.y, sc), quant4(a.z, a.w, sc), quant4(b.x, b.y, sc),
+                   quant4(b.z, b.w, sc));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_write_int8(const uint16_t* k, int64_t k_stride, const uint16_t* v,
+                              int64_t v_stride, int8_t* kc, int8_t* vc, int64_t num_blocks,
+                              int hkv, const int64_t* slots, int64_t n_tokens, float k_scale,
+                              float v_scale, int* err, int sms, cudaStream_t st) {
+  const int row_vecs = hkv * kHeadSize / 16;
+  const int64_t total = n_tokens * 2 * (int64_t)row_vecs;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  write_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(k, k_stride, v, v_stride, kc, vc,
+                                                          num_blocks * kBlockSize, row_vecs,
+                                                          slots, n_tokens, k_scale, v_scale, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,
                          uint16_t* kc, uint16_t* vc, int64_t num_blocks, int hkv,

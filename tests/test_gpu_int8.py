@@ -1,0 +1,105 @@
+"""int8 KV cache on the GPU against the float64 oracle: the quantising write
+bit for bit (codes, clamp, NaN), and decode-path attention over the codes
+(every head grouping, splits, multi-token decode) within the tolerance;
+requests too long for the decode path are reported and left unwritten."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_05_gb300 as pkv
+from paged_kv_attention_05_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import DeviceStep, assert_close  # noqa: E402
+
+KS, VS = 0.03, 0.04   # |x| > 127 * scale (about 3.8 and 5.1 for N(0, 1) data) saturates
+
+
+def _history_codes(step):
+    """The bf16 history caches as int8 codes (stale NaN slots become 0)."""
+    nb, bs, hkv, d = step.key_cache.shape
+    k8 = np.zeros((nb, bs, hkv, d), dtype=np.int8)
+    v8 = np.zeros_like(k8)
+    flat_k = step.key_cache.reshape(nb * bs, hkv, d)
+    flat_v = step.value_cache.reshape(nb * bs, hkv, d)
+    assert oracle.write_int8(flat_k, flat_v, k8, v8, np.arange(nb * bs, dtype=np.int64),
+                             KS, VS) == 0
+    return k8, v8
+
+
+def run_int8(step, what, expect_err=0):
+    k8, v8 = _history_codes(step)
+    rk, rv = k8.copy(), v8.copy()
+    assert oracle.write_int8(step.k, step.v, rk, rv, step.slot_mapping, KS, VS) == 0
+    ref, err = oracle.attention_int8(step.q, rk, rv, KS, VS, step.query_start_loc,
+                                     step.seq_lens, step.block_table, step.num_reqs, step.scale)
+    assert err == 0
+    ds = DeviceStep(step)
+    dk, dv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pkv.pkv_write_int8(ds.k, ds.v, dk, dv, ds.slot_mapping, KS, VS)
+    assert pkv.pkv_get_error() == 0
+    assert np.array_equal(dk.cpu().numpy(), rk) and np.array_equal(dv.cpu().numpy(), rv), \
+        "int8 write differs from the oracle's codes"
+    pkv.pkv_attention_int8(ds.q, dk, dv, KS, VS, ds.qsl, ds.seq_lens, ds.block_table,
+                           step.num_reqs, step.scale, ds.out)
+    assert pkv.pkv_get_error() == expect_err
+    got = ds.out_f64()
+    return ds, got, ref
+
+
+def _check_all(step, got, ref, what):
+    n = int(step.query_start_loc[-1])
+    assert_close(got[:n], ref[:n], what)
+    assert np.isnan(got[n:]).all()
+
+
+def test_int8_write_codes_clamp_and_nan():
+    step = W.build(W.custom([20, 0, 37], [5, 33, 1], 8, 2, seed=41, pad_tokens=3))
+    # plant special values in the new rows: NaN -> 0, +-inf and large -> +-127
+    step.k[0, 0, :4] = W.bf16_bits(np.array([np.nan, np.inf, -np.inf, 1e3], dtype=np.float32))
+    step.v[1, 1, 5:8] = W.bf16_bits(np.array([-1e3, 127.5 * 0.04, -0.02], dtype=np.float32))
+    k8, v8 = _history_codes(step)
+    rk, rv = k8.copy(), v8.copy()
+    assert oracle.write_int8(step.k, step.v, rk, rv, step.slot_mapping, KS, VS) == 0
+    ds = DeviceStep(step)
+    dk, dv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pkv.pkv_write_int8(ds.k, ds.v, dk, dv, ds.slot_mapping, KS, VS)
+    assert pkv.pkv_get_error() == 0
+    assert np.array_equal(dk.cpu().numpy(), rk) and np.array_equal(dv.cpu().numpy(), rv)
+    s0 = int(step.slot_mapping[0])
+    assert rk[s0 // 16, s0 % 16, 0, :4].tolist() == [0, 127, -127, 127]
+
+
+@pytest.mark.parametrize("hq,hkv,qn", [(8, 8, 1), (32, 8, 1), (32, 1, 1), (64, 2, 1),
+                                       (8, 8, 4), (16, 4, 2), (12, 4, 5)])
+def test_int8_decode(hq, hkv, qn):
+    ctx = [0, 1, 15, 16, 63, 200, 1023, 2100, 5000]
+    step = W.build(W.custom(ctx, [qn] * len(ctx), hq, hkv, seed=hq * 7 + hkv + qn))
+    ds, got, ref = run_int8(step, "int8 decode")
+    _check_all(step, got, ref, "int8 decode hq=%d hkv=%d qn=%d" % (hq, hkv, qn))
+
+
+def test_int8_long_requests_split_and_merge():
+    step = W.build(W.custom([9000, 3, 16384], [1, 1, 1], 32, 8, seed=43))
+    ds, got, ref = run_int8(step, "int8 split")
+    _check_all(step, got, ref, "int8 split decode")
+
+
+def test_int8_prefill_class_requests_are_reported_and_skipped():
+    step = W.build(W.custom([100, 0, 50], [1, 40, 2], 8, 2, seed=44))
+    ds, got, ref = run_int8(step, "int8 mixed", expect_err=pkv.DEV_ERR_BITS["INT8_PREFILL"])
+    q = step.query_start_loc
+    for r, ok in ((0, True), (1, False), (2, True)):
+        rows = slice(int(q[r]), int(q[r + 1]))
+        if ok:
+            assert_close(got[rows], ref[rows], "int8 decode rows of request %d" % r)
+        else:
+            assert np.isnan(got[rows]).all(), "rows of the skipped request were written"
+
+
+def test_int8_mha_decode_subset_full_lengths():
+    step = W.build(W.subset(W.spec("mha_decode"), 24))
+    ds, got, ref = run_int8(step, "int8 mha_decode subset")
+    _check_all(step, got, ref, "int8 mha_decode subset")
