@@ -61,14 +61,14 @@ def metric_work(spec):
     return float(spec.num_tokens)
 
 
-def decode_algorithmic_bytes(spec):
+def decode_algorithmic_bytes(spec, kv_elem_bytes=2):
     """Algorithmic bytes of one decode-kernel launch: every decode request's
-    K and V rows once per KV head, its query rows read and output rows
-    written (bf16)."""
+    K and V rows once per KV head (bf16, or int8 codes), its query rows read
+    and output rows written (bf16)."""
     b = 0
     for c, n in zip(spec.ctx, spec.q_len):
         if n == 1:
-            b += (c + 1) * spec.hkv * spec.head_size * 2 * 2
+            b += (c + 1) * spec.hkv * spec.head_size * kv_elem_bytes * 2
             b += 2 * spec.hq * spec.head_size * 2
     return b
 
@@ -229,6 +229,9 @@ def main():
     ap.add_argument("--with-prepare", action="store_true",
                     help="start each step with pkv_prepare_step (positions, seq_lens, slot "
                          "mapping and block table computed on the device)")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
+                    help="int8: the step writes and reads an int8 KV cache (one scale per "
+                         "cache; decode workloads only)")
     ap.add_argument("--reqs", type=int, default=0,
                     help="first N requests of the workload only, with a pool sized for them "
                          "(a small case of the same kernel shapes, e.g. for profiling)")
@@ -240,6 +243,10 @@ def main():
     spec = W.spec(args.config)
     if args.reqs:
         spec = W.subset(spec, args.reqs)
+    int8 = args.kv_dtype == "int8"
+    if int8 and any(n != 1 for n in spec.q_len):
+        raise SystemExit("--kv-dtype int8 runs decode workloads only (mha_decode, gqa_decode, "
+                         "mqa_long_decode)")
     if args.impl == "reference":
         run_reference(args, spec, rank)
         return
@@ -273,6 +280,17 @@ def main():
     out = torch.empty((rows, s.hq, d), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     pkv.pkv_reserve_workspace(s.num_reqs, rows, step.block_table.shape[1], s.hq, s.hkv)
+    KS, VS = 0.03, 0.03  # int8 scales: codes saturate beyond about 3.8 sigma
+    if int8:
+        # the history as int8 codes, quantised once by the library's own write
+        nb = key_cache.shape[0]
+        kc8 = torch.empty(key_cache.shape, dtype=torch.int8, device="cuda")
+        vc8 = torch.empty_like(kc8)
+        all_slots = torch.arange(nb * s.block_size, dtype=torch.int64, device="cuda")
+        pkv.pkv_write_int8(key_cache.view(-1, s.hkv, d), value_cache.view(-1, s.hkv, d), kc8,
+                           vc8, all_slots, KS, VS)
+        pkv.pkv_get_error()
+        key_cache = value_cache = all_slots = None  # the bf16 history is no longer needed
 
     if args.with_prepare:
         num_computed = torch.tensor(s.ctx, dtype=torch.int32, device="cuda")
@@ -283,6 +301,11 @@ def main():
         if args.with_prepare:
             pkv.pkv_prepare_step(qsl, num_computed, persistent_bt, s.num_reqs, rows, positions,
                                  seq_lens, slot_mapping, block_table, stream=stream)
+        if int8:
+            pkv.pkv_write_int8(k, v, kc8, vc8, slot_mapping, KS, VS, stream=stream)
+            pkv.pkv_attention_int8(q, kc8, vc8, KS, VS, qsl, seq_lens, block_table, s.num_reqs,
+                                   s.scale, out, stream=stream)
+            return
         pkv.pkv_write(k, v, key_cache, value_cache, slot_mapping, stream=stream)
         pkv.pkv_attention(q, key_cache, value_cache, qsl, seq_lens, block_table, s.num_reqs,
                           s.scale, out, stream=stream)
@@ -321,6 +344,8 @@ def main():
     ms_per_step = ms / args.steps
     name, unit = metric_of(spec)
     work = metric_work(spec)
+    if int8:  # one byte per cached element instead of two
+        name, work = name + " (int8 cache)", work / 2
     value = whole_job_value(work, world, ms_per_step / 1e3)
 
     # end to end through the public API with host buffers: pinned host inputs
@@ -375,8 +400,8 @@ def main():
                 "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
                 "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
     else:
-        algo = decode_algorithmic_bytes(spec) if dominant == "decode" else \
-            2 * s.num_tokens * s.hkv * d * 2 * 2
+        algo = decode_algorithmic_bytes(spec, 1 if int8 else 2) if dominant == "decode" else \
+            2 * s.num_tokens * s.hkv * d * 2 * (1.5 if int8 else 2)
         peak = peaks.get("hbm_gbs")
         roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
                 "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
@@ -389,23 +414,26 @@ def main():
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dominant
     roof["avg_launch_ms"] = avg_ms
-    traffic = profiled_traffic(dominant, spec.name, srcs)
+    traffic = profiled_traffic(dominant, spec.name + ("_int8" if int8 else ""), srcs)
     roof["traffic"] = traffic
 
     rec = {"metric": name, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "int8 cache, bf16 math" if int8 else "bf16", "data": "synthetic",
            "config": {"workload": spec.name, "requests": s.num_reqs, "query_tokens": s.num_tokens,
                       "step": ("prepare + " if args.with_prepare else "") + "write + attention",
                       "num_heads": s.hq, "num_kv_heads": s.hkv, "head_size": d,
-                      "block_size": s.block_size, "kv_bytes_per_step": s.kv_bytes(),
+                      "block_size": s.block_size,
+                      "kv_bytes_per_step": s.kv_bytes() // (2 if int8 else 1),
+                      "kv_dtype": args.kv_dtype,
                       "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB)" %
                             (s.kv_bytes() / 1e9),
                       "parallelism": "replica per GPU (dp%d)" % world},
            "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
            "roofline": roof}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not int8:
         rec["cpu_baseline"] = cpu_baseline(step)
     if rank == 0:
         print(json.dumps(rec))
