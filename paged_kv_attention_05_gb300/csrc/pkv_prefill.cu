@@ -77,10 +77,12 @@ enum {
   B_OE = 20,  // [2] O_x read by the epilogue
   B_IF = 22,  // [2] item slot published
   B_IE = 24,  // [2] item slot released
-  kNumBars = 26
+  B_XP = 26,  // [4] exchange between the two softmax warps of a row quarter
+  kNumBars = 30
 };
 constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 item slots
-constexpr int kOffCtl = kOffItems + 2 * 48;        // TMEM address, abort flag
+constexpr int kOffXch = kOffItems + 2 * 48;        // [4 quarters][2 slots][2 halves][32] floats
+constexpr int kOffCtl = kOffXch + 4 * 2 * 2 * 32 * 4;  // TMEM address, abort flag
 constexpr int kSmemBytes = kOffCtl + 16 + 1024;    // + alignment slack
 
 struct Item {
@@ -204,10 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(B_PF + x), 4);  // one arrival per softmax warp of the tile
-      mbar_init(bar(B_OE + x), 4);
+      mbar_init(bar(B_PF + x), 8);  // one arrival per softmax warp (each writes half of P)
+      mbar_init(bar(B_OE + x), 8);
       mbar_init(bar(B_IE + x), 1 + 8);  // MMA thread + one lane of each softmax warp
     }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_XP + i), 2);
     ctl[1] = 0;
     fence_barrier_init();
   }
@@ -388,13 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(B_SF + x));
         s_cnt[x]++;
       };
-      // O_x (+)= P_x V_c  (P_x: bf16 pairs in the first 64 columns of S_x)
+      // O_x (+)= P_x V_c  (P_x: bf16 pairs, keys 0-63 in columns 0-31 and keys
+      // 64-127 in columns 64-95 of S_x: each half where its own scores were)
       auto issue_pv = [&](int x, uint32_t c, bool acc) {
         const uint64_t db = (c & 1) ? dv1 : dv0;
         const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(d, pa + kk * 8, db + ((kk * 16 * 128) >> 4), id_o, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, pa + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 16 * 128) >> 4), id_o,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
       for (uint32_t it_cnt = 0; ok; ++it_cnt) {
@@ -457,173 +462,211 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------- softmax + epilogue, one row per thread -------------------
-    const int x = (warp - 2) >> 2;           // 0: tile a (warps 2-5), 1: tile b (warps 6-9)
-    const int row = (warp & 3) * 32 + lane;  // == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + x * 128 + lane_off, t_o = tmem + 256 + x * 128 + lane_off;
+    // ------------- softmax + epilogue: two warps per row, a column half each -------------
+    // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its 32 rows, one per
+    // thread) and key columns 64 * hf .. 64 * hf + 63, hf = (w - 2) / 4, of
+    // both query tiles of the item in turn; both warps of a row quarter (w and
+    // w + 4) sit on the same SM sub-partition and work on the same tile at the
+    // same time, so each tile's softmax takes half as long.  The warps of a
+    // quarter exchange per-row values (the need for a max pass, the partial
+    // maxima, the partial sums) through shared memory and a two-arrival
+    // mbarrier, whose waits are bounded like every other.
+    const int hf = (warp - 2) >> 2;
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;  // == TMEM lane
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + kOffXch);
     const float sl2 = a.scale * kLog2e;
-    uint32_t s_cnt = 0, o_cnt = 0;
-    for (uint32_t it_cnt = 0;; ++it_cnt) {
+    uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, x_cnt = 0;
+    bool ok = true;
+    // this lane's value out, the other warp's value for the same row back
+    auto exchange = [&](float v) -> float {
+      const int sl = x_cnt & 1;  // two slots: a slot is rewritten only after both read it
+      xch[((qd * 2 + sl) * 2 + hf) * 32 + lane] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_XP + qd));
+      if (!mbar_wait_warp(bar(B_XP + qd), x_cnt & 1, abort, ws.err)) ok = false;
+      x_cnt++;
+      return xch[((qd * 2 + sl) * 2 + (1 - hf)) * 32 + lane];
+    };
+    for (uint32_t it_cnt = 0; ok; ++it_cnt) {
       const int slot = it_cnt & 1;
       if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
       const Item it = items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_IE + slot));
       if (it.r < 0) break;
-      if (x == 1 && it.hb < 0) continue;  // single-tile item: warps of tile b idle
-      const int h = x == 0 ? it.ha : it.hb;
+      const int nx = it.hb >= 0 ? 2 : 1;
       const int qrow = it.qt * kPreTileQ + row;  // row inside the request
       const bool valid_row = qrow < it.n;
       const int qpos = valid_row ? it.ctx + qrow : 0;  // last visible key
-      float m_used = -INFINITY, l_sum = 0.f;
-      bool ok = true;
-      for (int j = 0; j < it.nkv; ++j) {
-        if (!mbar_wait_warp(bar(B_SF + x), s_cnt++ & 1, abort, ws.err)) {
+      float m_used[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+      for (int j = 0; j < it.nkv && ok; ++j) {
+        const int lim = qpos - j * kTileK - 64 * hf;  // my columns <= lim are visible
+        const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+        for (int x = 0; x < nx && ok; ++x) {
+          if (!mbar_wait_warp(bar(B_SF + x), s_cnt[x]++ & 1, abort, ws.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t t_s = tmem + x * 128 + 64 * hf + lane_off;
+          // my 64 scores of the row in registers (one wait), then P in place
+          float sv[64];
+          auto load_scores = [&]() {
+            PKV_LD32(t_s + 0, (sv + 0));
+            PKV_LD32(t_s + 32, (sv + 32));
+            tmem_wait_ld();
+            if (masked) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+            }
+          };
+          // p = exp2(s * scale * log2(e) - m) two columns at a time (packed
+          // fp32 pairs for the multiply-add and the sums); the bf16 pairs are
+          // packed over sv[0..31] (sv[2i], sv[2i+1] read before sv[i] is written)
+          float rs[4];
+          auto exp_pack = [&](float m) {
+            rs[0] = rs[1] = rs[2] = rs[3] = 0.f;
+            const float nm = -m;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x0, x1;
+              fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
+              sv[i] = __uint_as_float(pack_bf16(p0, p1));
+            }
+          };
+          load_scores();
+          float alpha = 1.f;
+          bool resc = false;
+          // After the first tile, P is computed with the running max straight
+          // away: no p exceeds 2^8 (the rescale threshold) while a half-row
+          // sum does not, so the max pass is taken only when some half-row's
+          // sum does (or is not finite) in either warp of the quarter.
+          bool need_max = j == 0;
+          if (!need_max) {
+            exp_pack(m_used[x]);
+            const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+            const float mine = (tot <= 256.f) ? 0.f : 1.f;
+            const float other = exchange(mine);
+            if (!ok) break;
+            need_max = __any_sync(0xffffffffu, mine + other > 0.f);
+            if (need_max) load_scores();
+          }
+          if (need_max) {
+            // the row maximum over both halves: three-input max chains, then
+            // the other warp's half through the exchange
+            float mx[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
+#pragma unroll
+            for (int i = 12; i < 60; i += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[60 + k]);
+            const float pm = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
+            const float po = exchange(pm);
+            if (!ok) break;
+            // (both warps form the same value: the halves in a fixed order)
+            const float mt = (hf == 0 ? fmaxf(pm, po) : fmaxf(po, pm)) * sl2;
+            resc = mt > m_used[x] + kRescaleThreshold;
+            if (resc) {
+              alpha = fast_exp2(m_used[x] - mt);  // 0 on the first tile
+              m_used[x] = mt;
+            }
+            exp_pack(m_used[x]);
+          }
+          PKV_ST32(t_s, (sv + 0));  // P half: 32 packed columns where my scores began
+          l_part[x] = l_part[x] * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+            // PV(j-1) is complete (S(j) is, and one thread's MMAs finish in
+            // order); each warp rescales its own 64 output columns
+            const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              float ov[32];
+              PKV_LD32(t_o + ch * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+              PKV_ST32(t_o + ch * 32, ov);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_PF + x));
+        }
+      }
+      if (!ok) break;
+      // epilogue, tile by tile: O / l in bf16, this warp's 64 columns.  Each
+      // 32-column chunk of the warp's 32 rows goes through the warp's staging
+      // area in shared memory, so that each global store writes whole 64-byte
+      // row pieces (8 rows x 4 lanes) instead of 32 scattered 16-byte pieces.
+      for (int x = 0; x < nx && ok; ++x) {
+        const float lo = exchange(l_part[x]);
+        if (!ok) break;
+        const float l = hf == 0 ? l_part[x] + lo : lo + l_part[x];  // the same in both warps
+        if (!mbar_wait_warp(bar(B_OF + x), o_cnt[x]++ & 1, abort, ws.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int lim = qpos - j * kTileK;  // columns <= lim are visible
-        const bool masked = !__all_sync(0xffffffffu, lim >= kTileK - 1);
-        // the row's 128 scores in registers (one wait), then P in place
-        float sv[128];
-        auto load_scores = [&]() {
-          PKV_LD32(t_s + 0, (sv + 0));
-          PKV_LD32(t_s + 32, (sv + 32));
-          PKV_LD32(t_s + 64, (sv + 64));
-          PKV_LD32(t_s + 96, (sv + 96));
+        const float inv = 1.f / l;
+        const int h = x == 0 ? it.ha : it.hb;
+        // (the thread index passes through an opaque move so that the staging
+        // addresses below are computed here, not kept live across the loop)
+        int ti;
+        asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
+        const int ln = ti & 31;
+        const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
+        const int row_base = it.qt * kPreTileQ + qd * 32;  // the warp's first row
+        uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize + 64 * hf;
+        const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
+        // the next chunk's TMEM load is in flight while this one is staged
+        float ov[2][32];
+        PKV_LD32(t_o, ov[0]);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
           tmem_wait_ld();
-          if (masked) {
+          if (ch < 1) PKV_LD32(t_o + 32, ov[1]);
+          const float* o = ov[ch];
+          // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
+          // that eight lanes of a store phase hit eight different bank groups
 #pragma unroll
-            for (int i = 0; i < 128; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
+            v.y = pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+            v.z = pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+            v.w = pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                             stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
           }
-        };
-        // p = exp2(s * scale * log2(e) - m) two columns at a time (packed fp32
-        // pairs for the multiply-add and the row sums); the bf16 pairs are
-        // packed over sv[0..63] (sv[2i], sv[2i+1] are read before sv[i] is written)
-        float rs[4];
-        auto exp_pack = [&](float m) {
-          rs[0] = rs[1] = rs[2] = rs[3] = 0.f;
-          const float nm = -m;
+          __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            float x0, x1;
-            fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
-            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
-            sv[i] = __uint_as_float(pack_bf16(p0, p1));
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (ln >> 2), c = ln & 3;
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
+                         : "memory");
+            const int qr = row_base + rr;
+            if (qr < it.n)
+              *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
           }
-        };
-        load_scores();
-        float alpha = 1.f;
-        bool resc = false;
-        // After the first tile, P is computed with the running max straight
-        // away: no p exceeds 2^8 (the rescale threshold) while the row sum
-        // does not, so the max pass is needed only when some row's sum does
-        // (or is not finite); then the warp reloads the scores and takes it.
-        bool fast = j > 0;
-        if (fast) {
-          exp_pack(m_used);
-          const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
-          fast = __all_sync(0xffffffffu, tot <= 256.f);
-          if (!fast) load_scores();
+          __syncwarp();
         }
-        if (!fast) {
-          // row maximum: four chains of three-input max (two scores per step)
-          float mx[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
-#pragma unroll
-          for (int i = 12; i < 124; i += 8)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[124 + k]);
-          const float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-          resc = mt > m_used + kRescaleThreshold;
-          if (resc) {
-            alpha = fast_exp2(m_used - mt);  // 0 on the first tile
-            m_used = mt;
-          }
-          exp_pack(m_used);
-        }
-        PKV_ST32(t_s + 0, (sv + 0));
-        PKV_ST32(t_s + 32, (sv + 32));
-        l_sum = l_sum * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // PV(j-1) is complete (S(j) is, and one thread's MMAs finish in order)
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float ov[32];
-            PKV_LD32(t_o + ch * 32, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-            PKV_ST32(t_o + ch * 32, ov);
-          }
-        }
-        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PF + x));
+        if (lane == 0) mbar_arrive(bar(B_OE + x));
       }
-      if (!ok) break;
-      // epilogue: O / l in bf16 to the output rows.  Each 32-column chunk of
-      // the warp's 32 rows goes through the warp's staging area in shared
-      // memory, so that each global store writes whole 64-byte row pieces
-      // (8 rows x 4 lanes) instead of 32 scattered 16-byte pieces.
-      if (!mbar_wait_warp(bar(B_OF + x), o_cnt++ & 1, abort, ws.err)) break;
-      tc_fence_after();
-      const float inv = 1.f / l_sum;
-      // (the thread index passes through an opaque move so that the staging
-      // addresses below are computed here, not kept live across the loop)
-      int ti;
-      asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
-      const int ln = ti & 31;
-      const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
-      const int row_base = it.qt * kPreTileQ + (warp & 3) * 32;  // the warp's first row
-      uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize;
-      // the next chunk's TMEM load is in flight while this one is staged
-      float ov[2][32];
-      PKV_LD32(t_o, ov[0]);
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        tmem_wait_ld();
-        if (ch < 3) PKV_LD32(t_o + (ch + 1) * 32, ov[(ch + 1) & 1]);
-        const float* o = ov[ch & 1];
-        // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
-        // that eight lanes of a store phase hit eight different bank groups
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 v;
-          v.x = pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
-          v.y = pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
-          v.z = pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
-          v.w = pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                           stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
-                       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                       : "memory");
-        }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = i * 8 + (ln >> 2), c = ln & 3;
-          uint4 v;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
-                       : "memory");
-          const int qr = row_base + rr;
-          if (qr < it.n)
-            *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
-        }
-        __syncwarp();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OE + x));
     }
   }
 
