@@ -120,12 +120,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
          | ((128u >> 4) << 24);            // M
 }
 
+// The MMA role runs on a whole converged warp, so that operands are
+// warp-uniform values; one elected lane (the lowest, the same every time, so
+// that its commits track all its MMAs) issues each instruction.
 // D (TMEM) (+)= A (shared) * B (shared)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -133,14 +136,16 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                        uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          bar)
       : "memory");
 }
 
@@ -369,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
+    // (the whole warp runs this, in step; see mma_ss)
+    {
       const uint32_t id_s = idesc_bf16(false), id_o = idesc_bf16(true);
       uint32_t tile_cnt = 0, s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
       // Operand descriptors of every buffer, built once: a descriptor's low
@@ -404,15 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (uint32_t it_cnt = 0; ok; ++it_cnt) {
         const int slot = it_cnt & 1;
-        if (!mbar_wait_inl(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+        if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
         const Item it = items[slot];
-        mbar_arrive(bar(B_IE + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IE + slot));
         if (it.r < 0) break;
         const int nx = it.hb >= 0 ? 2 : 1;
         for (int x = 0; x < nx && ok; ++x)
-          ok = mbar_wait_inl(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
+          ok = mbar_wait_warp(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
         const uint32_t c0 = tile_cnt;
-        if (!ok || !mbar_wait_inl(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
+        if (!ok || !mbar_wait_warp(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
         tc_fence_after();
         for (int x = 0; x < nx; ++x) issue_s(x, c0);
         mma_commit(bar(B_KE + c0 % kStages));
@@ -421,14 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < it.nkv && ok; ++j) {
           const uint32_t c = c0 + j;
           const bool more = j + 1 < it.nkv;
-          if (!mbar_wait_inl(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
+          if (!mbar_wait_warp(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
             ok = false;
             break;
           }
           for (int x = 0; x < nx; ++x) {
-            if (!mbar_wait_inl(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
+            if (!mbar_wait_warp(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
                 (j == 0 && o_cnt[x] > 0 &&
-                 !mbar_wait_inl(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err))) {
+                 !mbar_wait_warp(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err))) {
               ok = false;
               break;
             }
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (x == nx - 1) mma_commit(bar(B_VE + c % kStages));  // every PV of V_c issued
             if (more) {
               // the next K tile is waited for only now, with PV_x already queued
-              if (x == 0 && !mbar_wait_inl(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1,
+              if (x == 0 && !mbar_wait_warp(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1,
                                            abort, ws.err)) {
                 ok = false;
                 break;
