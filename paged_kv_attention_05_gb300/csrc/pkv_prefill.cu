@@ -496,13 +496,94 @@ __global__ void __launch_bounds__(kThreads, 1)
       x_cnt++;
       return xch[((qd * 2 + sl) * 2 + (1 - hf)) * 32 + lane];
     };
+    // The epilogue of an item (O / l in bf16 to its output rows) is split in
+    // two around the next item's first softmax step, tile by tile: first O_x
+    // is read out of TMEM (normalised and packed to bf16 in registers) and
+    // released, so that the next item's first P.V can follow its first P
+    // without waiting for the stores; then, after that softmax step, the
+    // packed rows are written out.  The last item's epilogue runs whole.
+    bool pending = false;
+    Item pv_it{};                      // the item whose epilogue is pending
+    float pv_l[2] = {0.f, 0.f};        // its partial row sums (this warp's half)
+    uint32_t held[32];                 // one tile's O half of the row, bf16 pairs
+    // read O_x of the pending item, release it
+    auto take_o = [&](int x) {
+      const float lo = exchange(pv_l[x]);
+      if (!ok) return;
+      const float l = hf == 0 ? pv_l[x] + lo : lo + pv_l[x];  // the same in both warps
+      if (!mbar_wait_warp(bar(B_OF + x), o_cnt[x]++ & 1, abort, ws.err)) {
+        ok = false;
+        return;
+      }
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
+      float ov[64];
+      PKV_LD32(t_o, (ov + 0));
+      PKV_LD32(t_o + 32, (ov + 32));
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) held[i] = pack_bf16(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_OE + x));
+    };
+    // write the held rows: each 32-column chunk of the warp's 32 rows goes
+    // through the warp's staging area in shared memory, so that each global
+    // store writes whole 64-byte row pieces (8 rows x 4 lanes) instead of 32
+    // scattered 16-byte pieces
+    auto store_o = [&](int x) {
+      const int h = x == 0 ? pv_it.ha : pv_it.hb;
+      // (the thread index passes through an opaque move so that the staging
+      // addresses below are computed here, not kept live across the loop)
+      int ti;
+      asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
+      const int ln = ti & 31;
+      const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
+      const int row_base = pv_it.qt * kPreTileQ + qd * 32;  // the warp's first row
+      uint16_t* obase =
+          a.out + (int64_t)pv_it.q0 * a.out_stride + (int64_t)h * kHeadSize + 64 * hf;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
+        // that eight lanes of a store phase hit eight different bank groups
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                           stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
+                       "r"(held[ch * 16 + 4 * k]), "r"(held[ch * 16 + 4 * k + 1]),
+                       "r"(held[ch * 16 + 4 * k + 2]), "r"(held[ch * 16 + 4 * k + 3])
+                       : "memory");
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = i * 8 + (ln >> 2), c = ln & 3;
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
+                       : "memory");
+          const int qr = row_base + rr;
+          if (qr < pv_it.n)
+            *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
+        }
+        __syncwarp();
+      }
+    };
     for (uint32_t it_cnt = 0; ok; ++it_cnt) {
       const int slot = it_cnt & 1;
       if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
       const Item it = items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_IE + slot));
-      if (it.r < 0) break;
+      if (it.r < 0) {
+        // no next item: the pending epilogue runs whole
+        for (int x = 0; pending && x < (pv_it.hb >= 0 ? 2 : 1) && ok; ++x) {
+          take_o(x);
+          if (ok) store_o(x);
+        }
+        break;
+      }
       const int nx = it.hb >= 0 ? 2 : 1;
       const int qrow = it.qt * kPreTileQ + row;  // row inside the request
       const bool valid_row = qrow < it.n;
@@ -512,6 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = qpos - j * kTileK - 64 * hf;  // my columns <= lim are visible
         const bool masked = !__all_sync(0xffffffffu, lim >= 63);
         for (int x = 0; x < nx && ok; ++x) {
+          if (j == 0 && pending) {
+            take_o(x);
+            if (!ok) break;
+          }
           if (!mbar_wait_warp(bar(B_SF + x), s_cnt[x]++ & 1, abort, ws.err)) {
             ok = false;
             break;
@@ -606,74 +691,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_PF + x));
+          if (j == 0 && pending) store_o(x);  // the previous item's rows of tile x
         }
       }
       if (!ok) break;
-      // epilogue, tile by tile: O / l in bf16, this warp's 64 columns.  Each
-      // 32-column chunk of the warp's 32 rows goes through the warp's staging
-      // area in shared memory, so that each global store writes whole 64-byte
-      // row pieces (8 rows x 4 lanes) instead of 32 scattered 16-byte pieces.
-      for (int x = 0; x < nx && ok; ++x) {
-        const float lo = exchange(l_part[x]);
-        if (!ok) break;
-        const float l = hf == 0 ? l_part[x] + lo : lo + l_part[x];  // the same in both warps
-        if (!mbar_wait_warp(bar(B_OF + x), o_cnt[x]++ & 1, abort, ws.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float inv = 1.f / l;
-        const int h = x == 0 ? it.ha : it.hb;
-        // (the thread index passes through an opaque move so that the staging
-        // addresses below are computed here, not kept live across the loop)
-        int ti;
-        asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
-        const int ln = ti & 31;
-        const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
-        const int row_base = it.qt * kPreTileQ + qd * 32;  // the warp's first row
-        uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize + 64 * hf;
-        const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
-        // the next chunk's TMEM load is in flight while this one is staged
-        float ov[2][32];
-        PKV_LD32(t_o, ov[0]);
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          tmem_wait_ld();
-          if (ch < 1) PKV_LD32(t_o + 32, ov[1]);
-          const float* o = ov[ch];
-          // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
-          // that eight lanes of a store phase hit eight different bank groups
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
-            v.y = pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
-            v.z = pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
-            v.w = pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                             stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
-                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = i * 8 + (ln >> 2), c = ln & 3;
-            uint4 v;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
-                         : "memory");
-            const int qr = row_base + rr;
-            if (qr < it.n)
-              *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
-          }
-          __syncwarp();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OE + x));
-      }
+      pending = true;
+      pv_it = it;
+      pv_l[0] = l_part[0];
+      pv_l[1] = l_part[1];
     }
   }
 
