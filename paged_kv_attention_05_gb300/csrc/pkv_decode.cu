@@ -45,6 +45,7 @@ namespace {
 using namespace dev;
 
 constexpr int kWarps = 8;
+constexpr int kCombineThreads = 128;  // merge kernel: 4 warps, one split pair row each
 constexpr int kThreads = kWarps * 32;
 constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2 KB)
 constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   using C = Cfg<MT, Q8>;
+  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -456,36 +458,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge of split results: one (split pair, query row) per CTA iteration, one
-// output column per thread; the weights exp2(m_s - max) renormalise the
-// splits' running sums and outputs (the same online-softmax identity the
-// decode loop uses between pages).  Rows are (query token, head in group);
-// pairs with fewer rows than the largest skip the rest.
-__global__ void __launch_bounds__(kHeadSize) combine_kernel(AttnArgs a, Workspace ws) {
+// Merge of split results: one (split pair, query row) per warp, four output
+// columns per lane, the splits merged in one pass with the online-softmax
+// identity the decode loop uses between pages (a running max M; the sum and
+// the output so far are scaled by exp2(M_old - M_new) when it grows).  A
+// split that saw no key of the row (m = -inf: only later splits of a
+// multi-token row) contributes nothing; the first split always holds key 0.
+// Rows are (query token, head in group); pairs with fewer rows than the
+// largest skip the rest.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {
   const int G = a.hq / a.hkv;
   const int max_rows = ws.hdr->max_rows;
   const int n_items = ws.hdr->n_pairs * max_rows;
-  const int d = threadIdx.x;
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kWarpsPerBlock = kCombineThreads / 32;
+  for (int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
+       item += gridDim.x * kWarpsPerBlock) {
     const SplitPair sp = ws.pairs[item / max_rows];
     const int row = item % max_rows;
     const int q0 = a.qsl[sp.r];
     const int rows = (a.qsl[sp.r + 1] - q0) * G;
     if (row >= rows) continue;
     const float* ml = ws.part_ml + ((int64_t)sp.first + row) * 2;
-    const float* po = ws.part_o + ((int64_t)sp.first + row) * kHeadSize + d;
-    float M = -INFINITY;
-    for (int s = 0; s < sp.nsplit; ++s) M = fmaxf(M, __ldcg(ml + (int64_t)s * rows * 2));
-    float acc = 0.f, lsum = 0.f;
+    const float* po = ws.part_o + ((int64_t)sp.first + row) * kHeadSize + 4 * lane;
+    float M = -INFINITY, lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
     for (int s = 0; s < sp.nsplit; ++s) {
       const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + (int64_t)s * rows * 2));
-      const float f = fast_exp2(v.x - M);  // a split that saw no key of this row has m = -inf
-      lsum += f * v.y;
-      acc += f * __ldcg(po + (int64_t)s * rows * kHeadSize);
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(po + (int64_t)s * rows * kHeadSize));
+      const float Mn = fmaxf(M, v.x);
+      const float fo = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+      const float fn = v.x == -INFINITY ? 0.f : fast_exp2(v.x - Mn);
+      lsum = lsum * fo + v.y * fn;
+      acc.x = acc.x * fo + o.x * fn;
+      acc.y = acc.y * fo + o.y * fn;
+      acc.z = acc.z * fo + o.z * fn;
+      acc.w = acc.w * fo + o.w * fn;
+      M = Mn;
     }
-    a.out[(int64_t)(q0 + row / G) * a.out_stride + (int64_t)(sp.g * G + row % G) * kHeadSize + d] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(acc / lsum));
+    const float inv = 1.f / lsum;
+    uint16_t* orow = a.out + (int64_t)(q0 + row / G) * a.out_stride +
+                     (int64_t)(sp.g * G + row % G) * kHeadSize + 4 * lane;
+    *reinterpret_cast<uint2*>(orow) =
+        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
   }
 }
 
@@ -526,7 +542,7 @@ cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaS
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
-  combine_kernel<<<sms * 8, kHeadSize, 0, st>>>(a, ws);
+  combine_kernel<<<sms * 8, kCombineThreads, 0, st>>>(a, ws);
   return cudaGetLastError();
 }
 

@@ -193,6 +193,7 @@ __device__ __forceinline__ void tmem_wait_st() {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
+  if (ws.hdr->n_pre_entries == 0) return;  // a batch without prefill work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
