@@ -164,25 +164,42 @@ def whole_job_value(work_per_rank, world, seconds_max):
     return work_per_rank * world / seconds_max
 
 
-def cpu_baseline(step, sample_reqs=None):
-    """The float64 oracle on the host cores over (a sample of) the same step."""
+def cpu_baseline(step, sample_reqs=None, target_s=None):
+    """The float64 oracle on the host cores over (a sample of) the same step:
+    write + attention for the first sample_reqs requests (all by default),
+    repeated until about target_s seconds of CPU work when that is given."""
     import oracle
     spec = step.spec
     R = spec.num_reqs if sample_reqs is None else min(sample_reqs, spec.num_reqs)
     kc, vc = step.key_cache, step.value_cache
-    t0 = time.perf_counter()
-    oracle.write(step.k, step.v, kc, vc, step.slot_mapping)
     qsl = step.query_start_loc[:R + 1]
-    oracle.attention(step.q, kc, vc, qsl, step.seq_lens[:R], step.block_table[:R], R,
-                     step.scale)
-    dt = time.perf_counter() - t0
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.write(step.k, step.v, kc, vc, step.slot_mapping)
+        oracle.attention(step.q, kc, vc, qsl, step.seq_lens[:R], step.block_table[:R], R,
+                         step.scale)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if target_s is None or dt >= target_s:
+            break
     sub = W.StepSpec(spec.name, spec.ctx[:R], spec.q_len[:R], spec.hq, spec.hkv,
                      spec.num_blocks, spec.seed)
-    work = metric_work(sub)
+    work = metric_work(sub) * reps
     return {"value": work / dt, "unit": metric_of(spec)[1], "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": "%d of %d requests, one step (write + attention), %.1f s" %
-                      (R, spec.num_reqs, dt)}
+            "sample": "%d of %d requests, write + attention, %d pass%s, %.1f s" %
+                      (R, spec.num_reqs, reps, "" if reps == 1 else "es", dt)}
+
+
+def cpu_baseline_bounded(step, target_s=10.0):
+    """cpu_baseline on a sample sized for about target_s seconds: the whole
+    batch (repeated) when one pass is short, else the first requests."""
+    spec = step.spec
+    n_probe = min(2, spec.num_reqs)
+    probe = cpu_baseline(step, sample_reqs=n_probe)
+    per_req = float(probe["sample"].split(", ")[-1].rstrip(" s")) / n_probe
+    reqs = max(1, min(spec.num_reqs, int(target_s / max(per_req, 1e-9))))
+    return cpu_baseline(step, sample_reqs=reqs, target_s=target_s)
 
 
 def run_reference(args, spec, rank):
@@ -434,7 +451,7 @@ def main():
            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
            "roofline": roof}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not int8:
-        rec["cpu_baseline"] = cpu_baseline(step)
+        rec["cpu_baseline"] = cpu_baseline_bounded(step)
     if rank == 0:
         print(json.dumps(rec))
     if dist is not None:
