@@ -172,28 +172,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       s_off_q[kPlanThreads] = tot_q;
     }
     __syncthreads();
-    for (int i = tid; i < tot_u; i += kPlanThreads) {
-      const int lo = find_owner(s_off_u, i);
-      const int rem = i - s_off_u[lo];
+    // decode units and split pairs: one warp per request (a request's entries
+    // are contiguous), lanes over its entries, so that consecutive lanes
+    // write consecutive entries with no search for the owner
+    for (int lo = tid >> 5; lo < kPlanThreads && base + lo < a.num_reqs;
+         lo += kPlanThreads / 32) {
+      const int ln = tid & 31;
+      const int cnt_u = s_off_u[lo + 1] - s_off_u[lo];
+      if (cnt_u == 0) continue;
       const int L = s_len[lo], qn = s_n[lo];
       const int nsplit = (L + chunk - 1) / chunk;
-      const int sp = rem / a.hkv, g = rem - sp * a.hkv;
-      const int64_t idx = (int64_t)unit_carry + i;
-      if (idx >= ws.max_units) break;
-      // two 16-byte stores per unit: consecutive threads fill consecutive units
-      int4* dst = reinterpret_cast<int4*>(ws.units + idx);
-      dst[0] = make_int4(base + lo, g, L - qn, nsplit);
-      dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
-                         nsplit > 1 ? s_off_p[lo] + (g * nsplit + sp) * qn * G : -1, qn);
-    }
-    for (int i = tid; i < tot_q; i += kPlanThreads) {
-      const int lo = find_owner(s_off_q, i);
-      const int g = i - s_off_q[lo];
-      const int nsplit = (s_len[lo] + chunk - 1) / chunk;
-      const int64_t idx = (int64_t)pair_carry + i;
-      if (idx >= ws.max_pairs) break;
-      *reinterpret_cast<int4*>(ws.pairs + idx) =
-          make_int4(base + lo, g, s_off_p[lo] + g * nsplit * s_n[lo] * G, nsplit);
+      for (int rem = ln; rem < cnt_u; rem += 32) {
+        const int sp = rem / a.hkv, g = rem - sp * a.hkv;
+        const int64_t idx = (int64_t)unit_carry + s_off_u[lo] + rem;
+        if (idx >= ws.max_units) break;
+        // two 16-byte stores per unit
+        int4* dst = reinterpret_cast<int4*>(ws.units + idx);
+        dst[0] = make_int4(base + lo, g, L - qn, nsplit);
+        dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
+                           nsplit > 1 ? s_off_p[lo] + (g * nsplit + sp) * qn * G : -1, qn);
+      }
+      const int cnt_q = s_off_q[lo + 1] - s_off_q[lo];
+      for (int g = ln; g < cnt_q; g += 32) {
+        const int64_t idx = (int64_t)pair_carry + s_off_q[lo] + g;
+        if (idx >= ws.max_pairs) break;
+        *reinterpret_cast<int4*>(ws.pairs + idx) =
+            make_int4(base + lo, g, s_off_p[lo] + g * nsplit * qn * G, nsplit);
+      }
     }
     for (int i = tid; i < tot_t; i += kPlanThreads) {
       const int lo = find_owner(s_off_t, i);
