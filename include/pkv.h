@@ -146,6 +146,46 @@ int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t n
                   float scale, void* out, int64_t out_row_stride, void* stream);
 
 /*
+ * pkv_plan / pkv_attention_planned — one step plan serving every layer.
+ *
+ * "Tour: One forward pass", stop 5: one attention-metadata object is built per
+ * step and shared by all layers; stop 7: the 32-layer loop.  pkv_attention
+ * builds its plan (the work lists: decode units, split pairs, prefill tiles)
+ * on every call; pkv_plan builds it once per step and pkv_attention_planned
+ * runs one layer on it, so a step of L layers pays for one plan.
+ *
+ * pkv_plan(q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens,
+ *          block_table_width, num_reqs, stream): the metadata arguments of
+ *   pkv_attention, with its checks.  The plan is a snapshot: the work lists
+ *   hold every request's query rows and lengths, and no later call reads
+ *   query_start_loc or seq_lens again.  The plan lives in this device's
+ *   workspace (grown here if needed, so reserve it before a graph capture)
+ *   and replaces the previous one; pkv_attention, pkv_attention_int8 and a
+ *   workspace reallocation (a call needing more room, pkv_reserve_workspace)
+ *   replace or drop it too.  Requests whose metadata fail a check are
+ *   reported in the error word when the plan kernel runs.
+ *
+ * pkv_attention_planned(q, q_row_stride, num_heads, key_cache, value_cache,
+ *          num_blocks, block_size, num_kv_heads, head_size, block_table,
+ *          scale, out, out_row_stride, stream): pkv_attention for the current
+ *   plan: the same result as a pkv_attention call with the plan's metadata
+ *   and these buffers (q and out hold the plan's q_rows rows; block_table is
+ *   read again, so a layer may point at its own table of the same width).
+ *   num_heads and num_kv_heads must equal the plan's; with no valid plan on
+ *   the current device the call returns PKV_ERR_ARG.  Calls are stream
+ *   ordered: the plan must be enqueued before, on the same stream (or one
+ *   ordered after it).
+ */
+int pkv_plan(int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
+             const int32_t* query_start_loc, const int32_t* seq_lens, int64_t block_table_width,
+             int32_t num_reqs, void* stream);
+int pkv_attention_planned(const void* q, int64_t q_row_stride, int32_t num_heads,
+                          const void* key_cache, const void* value_cache, int64_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t head_size,
+                          const int32_t* block_table, float scale, void* out,
+                          int64_t out_row_stride, void* stream);
+
+/*
  * pkv_prepare_step — the step-side metadata the two calls read, computed on
  * the device from the request state (no host round trip).
  *

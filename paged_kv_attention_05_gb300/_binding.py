@@ -18,7 +18,8 @@ DEV_ERR_BITS = {
 
 EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
            "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
-           "pkv_launch_count", "pkv_prepare_step", "pkv_write_int8", "pkv_attention_int8"]
+           "pkv_launch_count", "pkv_prepare_step", "pkv_write_int8", "pkv_attention_int8",
+           "pkv_plan", "pkv_attention_planned"]
 TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine", "prepare"]
 
 
@@ -53,6 +54,11 @@ def load():
     L.pkv_attention_int8.restype = ctypes.c_int
     L.pkv_attention_int8.argtypes = [vp, i64, i64, i32, vp, vp, f32, f32, i64, i32, i32, i32, vp,
                                      vp, vp, i64, i32, f32, vp, i64, vp]
+    L.pkv_plan.restype = ctypes.c_int
+    L.pkv_plan.argtypes = [i64, i32, i32, vp, vp, i64, i32, vp]
+    L.pkv_attention_planned.restype = ctypes.c_int
+    L.pkv_attention_planned.argtypes = [vp, i64, i32, vp, vp, i64, i32, i32, i32, vp, f32, vp,
+                                        i64, vp]
     L.pkv_reserve_workspace.restype = ctypes.c_int
     L.pkv_reserve_workspace.argtypes = [i32, i64, i64, i32, i32]
     L.pkv_get_error.restype = ctypes.c_int
@@ -221,6 +227,43 @@ def pkv_attention_int8(q, key_cache, value_cache, k_scale, v_scale, query_start_
                                      block_table.data_ptr(), bt_width, int(num_reqs),
                                      float(scale), out.data_ptr(), _rows3(out, "out"),
                                      _stream(stream)))
+
+
+def pkv_plan(q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens, block_table_width,
+             num_reqs, stream=None):
+    """Builds one step plan on the current device, for pkv_attention_planned
+    calls (one per layer) that follow it; see include/pkv.h."""
+    import torch
+    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens")):
+        _require(t, torch.int32, n)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
+                              seq_lens.numel() < int(num_reqs)):
+        raise ValueError("metadata shorter than num_reqs")
+    _check(load().pkv_plan(int(q_rows), int(num_heads), int(num_kv_heads),
+                           query_start_loc.data_ptr(), seq_lens.data_ptr(),
+                           int(block_table_width), int(num_reqs), _stream(stream)))
+
+
+def pkv_attention_planned(q, key_cache, value_cache, block_table, scale, out, stream=None):
+    """One layer's attention on the current step plan (pkv_plan)."""
+    import torch
+    for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"), (out, "out")):
+        _require(t, torch.bfloat16, n)
+    _require(block_table, torch.int32, "block_table")
+    if not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous")
+    nb, bs, hkv, d = _caches(key_cache, value_cache, torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [rows, num_heads, head_size]")
+    rows, hq, _ = q.shape
+    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+        raise ValueError("out must hold [rows, num_heads * head_size]")
+    _check(load().pkv_attention_planned(q.data_ptr(), _rows3(q, "q"), hq, key_cache.data_ptr(),
+                                        value_cache.data_ptr(), nb, bs, hkv, d,
+                                        block_table.data_ptr(), float(scale), out.data_ptr(),
+                                        _rows3(out, "out"), _stream(stream)))
 
 
 def pkv_reserve_workspace(max_reqs, max_q_rows, block_table_width, num_heads, num_kv_heads):

@@ -2,6 +2,7 @@
 // per-device workspace and error word, and the kernel launches.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -22,6 +23,12 @@ struct DeviceState {
   int* err = nullptr;  // device error word
   void* ws = nullptr;  // workspace
   size_t ws_bytes = 0;
+  // the step plan held in the workspace (pkv_plan / pkv_attention): its
+  // geometry and the carve of the workspace it was written with
+  bool plan_valid = false;
+  int64_t plan_q_rows = 0, plan_bt_width = 0;
+  int plan_hq = 0, plan_hkv = 0, plan_reqs = 0;
+  Sizes plan_sizes{};
 };
 
 std::mutex g_mu;
@@ -116,6 +123,7 @@ int ensure_workspace(DeviceState* s, const Sizes& z, cudaStream_t st, Workspace*
     if (s->ws) cudaFree(s->ws);
     s->ws = nullptr;
     s->ws_bytes = 0;
+    s->plan_valid = false;  // the plan lived in the old workspace
     const size_t grow = need + need / 4;
     e = cudaMalloc(&s->ws, grow);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
@@ -129,6 +137,7 @@ int ensure_workspace(DeviceState* s, const Sizes& z, cudaStream_t st, Workspace*
 }
 
 int check_geometry(int32_t block_size, int32_t hkv, int32_t head_size) {
+  if (hkv > 32767) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d > 32767", hkv);
   if (block_size != kBlockSize)
     return fail(PKV_ERR_UNSUPPORTED, "block_size %d (only %d)", block_size, kBlockSize);
   if (head_size != kHeadSize)
@@ -271,6 +280,116 @@ extern "C" int pkv_write_int8(const void* k, int64_t k_row_stride, const void* v
 
 namespace {
 
+// The checks of the step metadata shared by pkv_plan and the attention calls.
+int check_meta(int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
+               const int32_t* query_start_loc, const int32_t* seq_lens,
+               int64_t block_table_width, int32_t num_reqs) {
+  if (num_kv_heads <= 0) return fail(PKV_ERR_ARG, "num_kv_heads %d", num_kv_heads);
+  if (num_heads <= 0 || num_heads % num_kv_heads)
+    return fail(PKV_ERR_UNSUPPORTED, "num_heads %d is not a multiple of num_kv_heads %d",
+                num_heads, num_kv_heads);
+  if (num_heads / num_kv_heads > kMaxGroup)
+    return fail(PKV_ERR_UNSUPPORTED, "num_heads / num_kv_heads = %d > %d",
+                num_heads / num_kv_heads, kMaxGroup);
+  if (num_reqs < 0 || q_rows < 0 || block_table_width < 0)
+    return fail(PKV_ERR_ARG, "negative size");
+  if (num_reqs == 0 || q_rows == 0) return PKV_OK;
+  if (!query_start_loc || !seq_lens) return fail(PKV_ERR_ARG, "null pointer argument");
+  if (block_table_width < 1) return fail(PKV_ERR_ARG, "block_table_width < 1");
+  if (block_table_width > kMaxBtWidth)
+    return fail(PKV_ERR_UNSUPPORTED, "block_table_width %lld > %d (longest supported request is "
+                "%d keys)", (long long)block_table_width, kMaxBtWidth, kMaxBtWidth * kBlockSize);
+  return PKV_OK;
+}
+
+// Builds the step plan into the device workspace (state lock held).
+int plan_locked(DeviceState* s, int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
+                const int32_t* query_start_loc, const int32_t* seq_lens,
+                int64_t block_table_width, int32_t num_reqs, int kv_int8, cudaStream_t st) {
+  const Sizes z = sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads);
+  Workspace ws;
+  int rc = ensure_workspace(s, z, st, &ws);
+  if (rc) return rc;
+  AttnArgs a{};
+  a.q_rows = q_rows;
+  a.hq = num_heads;
+  a.hkv = num_kv_heads;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.bt_width = block_table_width;
+  a.num_reqs = num_reqs;
+  a.kv_int8 = kv_int8;
+  const int workers = decode_workers(num_heads / num_kv_heads, s->sms);
+  cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  // an int8 plan leaves prefill-class requests out: it cannot serve a bf16 call
+  s->plan_valid = !kv_int8;
+  s->plan_q_rows = q_rows;
+  s->plan_bt_width = block_table_width;
+  s->plan_hq = num_heads;
+  s->plan_hkv = num_kv_heads;
+  s->plan_reqs = num_reqs;
+  s->plan_sizes = z;
+  return PKV_OK;
+}
+
+// Runs the attention kernels of the plan held in the workspace (state lock
+// held; the plan's geometry is the caller's).
+int run_locked(DeviceState* s, const void* q, int64_t q_row_stride, const void* key_cache,
+               const void* value_cache, int64_t num_blocks, const int32_t* block_table,
+               float scale, void* out, int64_t out_row_stride, int kv_int8, float k_scale,
+               float v_scale, cudaStream_t st) {
+  Workspace ws = carve_workspace(s->ws, s->plan_sizes, s->err);
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_stride = q_row_stride;
+  a.q_rows = s->plan_q_rows;
+  a.hq = s->plan_hq;
+  a.kc = static_cast<const uint16_t*>(key_cache);
+  a.vc = static_cast<const uint16_t*>(value_cache);
+  a.num_blocks = num_blocks;
+  a.hkv = s->plan_hkv;
+  a.qsl = nullptr;  // the kernels read the plan's snapshot of the metadata
+  a.seq_lens = nullptr;
+  a.bt = block_table;
+  a.bt_width = s->plan_bt_width;
+  a.num_reqs = s->plan_reqs;
+  a.scale = scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_stride = out_row_stride;
+  a.kv_int8 = kv_int8;
+  a.k_scale = kv_int8 ? k_scale : 1.f;
+  a.v_scale = kv_int8 ? v_scale : 1.f;
+  cudaError_t e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (!kv_int8) {  // an int8 call has no prefill work (the plan reports such requests)
+    e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  }
+  return PKV_OK;
+}
+
+// The checks of the buffers an attention call reads and writes.
+int check_buffers(const void* q, int64_t q_row_stride, int32_t num_heads, const void* key_cache,
+                  const void* value_cache, int64_t num_blocks, const int32_t* block_table,
+                  float scale, void* out, int64_t out_row_stride) {
+  if (num_blocks < 1) return fail(PKV_ERR_ARG, "num_blocks %lld < 1", (long long)num_blocks);
+  if (!q || !key_cache || !value_cache || !block_table || !out)
+    return fail(PKV_ERR_ARG, "null pointer argument");
+  const int64_t row = (int64_t)num_heads * kHeadSize;
+  if (q_row_stride < row || out_row_stride < row)
+    return fail(PKV_ERR_ARG, "q/out row stride below num_heads * head_size (%lld)",
+                (long long)row);
+  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
+      (q_row_stride % 8) || (out_row_stride % 8))
+    return fail(PKV_ERR_ALIGN, "q/out/caches must be 16-byte aligned with row strides * 2 a "
+                               "multiple of 16 bytes");
+  if (!(scale == scale)) return fail(PKV_ERR_ARG, "scale is NaN");
+  return PKV_OK;
+}
+
 // pkv_attention and pkv_attention_int8: kv_int8 = 0 for bf16 caches, 1 for
 // int8 codes with the two scales (decode-class requests only).
 int attention_common(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
@@ -283,31 +402,14 @@ int attention_common(const void* q, int64_t q_row_stride, int64_t q_rows, int32_
   g_msg[0] = 0;
   int rc = check_geometry(block_size, num_kv_heads, head_size);
   if (rc) return rc;
-  if (num_heads <= 0 || num_heads % num_kv_heads)
-    return fail(PKV_ERR_UNSUPPORTED, "num_heads %d is not a multiple of num_kv_heads %d",
-                num_heads, num_kv_heads);
-  if (num_heads / num_kv_heads > kMaxGroup)
-    return fail(PKV_ERR_UNSUPPORTED, "num_heads / num_kv_heads = %d > %d",
-                num_heads / num_kv_heads, kMaxGroup);
-  if (num_reqs < 0 || q_rows < 0 || block_table_width < 0)
-    return fail(PKV_ERR_ARG, "negative size");
+  rc = check_meta(q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens,
+                  block_table_width, num_reqs);
+  if (rc) return rc;
   if (num_blocks < 1) return fail(PKV_ERR_ARG, "num_blocks %lld < 1", (long long)num_blocks);
   if (num_reqs == 0 || q_rows == 0) return PKV_OK;
-  if (!q || !key_cache || !value_cache || !query_start_loc || !seq_lens || !block_table || !out)
-    return fail(PKV_ERR_ARG, "null pointer argument");
-  if (block_table_width < 1) return fail(PKV_ERR_ARG, "block_table_width < 1");
-  if (block_table_width > kMaxBtWidth)
-    return fail(PKV_ERR_UNSUPPORTED, "block_table_width %lld > %d (longest supported request is "
-                "%d keys)", (long long)block_table_width, kMaxBtWidth, kMaxBtWidth * kBlockSize);
-  const int64_t row = (int64_t)num_heads * kHeadSize;
-  if (q_row_stride < row || out_row_stride < row)
-    return fail(PKV_ERR_ARG, "q/out row stride below num_heads * head_size (%lld)",
-                (long long)row);
-  if (!aligned16(q) || !aligned16(out) || !aligned16(key_cache) || !aligned16(value_cache) ||
-      (q_row_stride % 8) || (out_row_stride % 8))
-    return fail(PKV_ERR_ALIGN, "q/out/caches must be 16-byte aligned with row strides * 2 a "
-                               "multiple of 16 bytes");
-  if (!(scale == scale)) return fail(PKV_ERR_ARG, "scale is NaN");
+  rc = check_buffers(q, q_row_stride, num_heads, key_cache, value_cache, num_blocks, block_table,
+                     scale, out, out_row_stride);
+  if (rc) return rc;
   if (kv_int8 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
     return fail(PKV_ERR_ARG, "k_scale and v_scale must be finite and positive");
 
@@ -316,47 +418,73 @@ int attention_common(const void* q, int64_t q_row_stride, int64_t q_rows, int32_
   rc = current_state(&s);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  Workspace ws;
-  rc = ensure_workspace(s, sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads),
-                        st, &ws);
+  rc = plan_locked(s, q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens,
+                   block_table_width, num_reqs, kv_int8, st);
   if (rc) return rc;
-
-  AttnArgs a;
-  a.q = static_cast<const uint16_t*>(q);
-  a.q_stride = q_row_stride;
-  a.q_rows = q_rows;
-  a.hq = num_heads;
-  a.kc = static_cast<const uint16_t*>(key_cache);
-  a.vc = static_cast<const uint16_t*>(value_cache);
-  a.num_blocks = num_blocks;
-  a.hkv = num_kv_heads;
-  a.qsl = query_start_loc;
-  a.seq_lens = seq_lens;
-  a.bt = block_table;
-  a.bt_width = block_table_width;
-  a.num_reqs = num_reqs;
-  a.scale = scale;
-  a.out = static_cast<uint16_t*>(out);
-  a.out_stride = out_row_stride;
-  a.kv_int8 = kv_int8;
-  a.k_scale = kv_int8 ? k_scale : 1.f;
-  a.v_scale = kv_int8 ? v_scale : 1.f;
-
-  const int workers = decode_workers(num_heads / num_kv_heads, s->sms);
-  cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-  e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if (!kv_int8) {  // an int8 call has no prefill work (the plan reports such requests)
-    e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  }
-  return PKV_OK;
+  return run_locked(s, q, q_row_stride, key_cache, value_cache, num_blocks, block_table, scale,
+                    out, out_row_stride, kv_int8, k_scale, v_scale, st);
 }
 
 }  // namespace
+
+extern "C" int pkv_plan(int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
+                        const int32_t* query_start_loc, const int32_t* seq_lens,
+                        int64_t block_table_width, int32_t num_reqs, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_meta(q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens,
+                      block_table_width, num_reqs);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc) return rc;
+  if (num_reqs == 0 || q_rows == 0) {  // an empty step: nothing to plan, nothing to run
+    s->plan_valid = true;
+    s->plan_q_rows = q_rows;
+    s->plan_reqs = 0;
+    s->plan_hq = num_heads;
+    s->plan_hkv = num_kv_heads;
+    s->plan_bt_width = block_table_width;
+    return PKV_OK;
+  }
+  return plan_locked(s, q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens,
+                     block_table_width, num_reqs, 0, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_attention_planned(const void* q, int64_t q_row_stride, int32_t num_heads,
+                                     const void* key_cache, const void* value_cache,
+                                     int64_t num_blocks, int32_t block_size,
+                                     int32_t num_kv_heads, int32_t head_size,
+                                     const int32_t* block_table, float scale, void* out,
+                                     int64_t out_row_stride, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_geometry(block_size, num_kv_heads, head_size);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* s = nullptr;
+  rc = current_state(&s);
+  if (rc) return rc;
+  if (!s->plan_valid)
+    return fail(PKV_ERR_ARG, "no step plan on this device (call pkv_plan or pkv_attention first)");
+  if (num_heads != s->plan_hq || num_kv_heads != s->plan_hkv)
+    return fail(PKV_ERR_ARG, "num_heads %d / num_kv_heads %d differ from the plan's %d / %d",
+                num_heads, num_kv_heads, s->plan_hq, s->plan_hkv);
+  if (s->plan_reqs == 0 || s->plan_q_rows == 0) return PKV_OK;
+  rc = check_buffers(q, q_row_stride, num_heads, key_cache, value_cache, num_blocks, block_table,
+                     scale, out, out_row_stride);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the decode and prefill kernels take work from two cursors in the plan
+  // header, which the plan kernel zeroes; a further run of the same plan
+  // zeroes them again first (a stream-ordered memset, graph-capturable)
+  PlanHeader* hdr = carve_workspace(s->ws, s->plan_sizes, s->err).hdr;
+  static_assert(offsetof(PlanHeader, pre_counter) == offsetof(PlanHeader, dec_counter) + 4,
+                "adjacent cursors");
+  cudaError_t e = cudaMemsetAsync(&hdr->dec_counter, 0, 2 * sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cursor reset");
+  return run_locked(s, q, q_row_stride, key_cache, value_cache, num_blocks, block_table, scale,
+                    out, out_row_stride, 0, 1.f, 1.f, st);
+}
 
 extern "C" int pkv_attention(const void* q, int64_t q_row_stride, int64_t q_rows,
                              int32_t num_heads, const void* key_cache, const void* value_cache,

@@ -163,6 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= n_units || *abort) break;
     const DecUnit un = ws.units[u];
+    const int ug = un.gq & 0xFFFF;  // KV head
+    const int uqn = un.gq >> 16;    // query tokens of the request
     const int k0 = un.k0, k1 = un.k1;
     const int p0 = k0 / kBlockSize;
     const int npages = (k1 + kBlockSize - 1) / kBlockSize - p0;
@@ -187,14 +189,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the query rows of this KV head by TMA: for each of the unit's qn query
     // tokens, its G heads (g*G ..), at rows token * G .. token * G + G - 1
-    const int qn = un.qn, nrows = qn * G;
+    const int qn = uqn, nrows = qn * G;
     if (lane == 0) {
       fence_async_smem();  // the previous unit's reads of the buffer are done
       mbar_expect_tx(q_bar, 2 * nrows * 128);
-      const int q0 = a.qsl[un.r];
+      const int q0 = un.q0;
       for (int i = 0; i < qn; ++i) {
-        tma_load_3d(qbuf + i * G * 128, &tm_q, q_bar, 0, un.g * G, q0 + i);
-        tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, un.g * G, q0 + i);
+        tma_load_3d(qbuf + i * G * 128, &tm_q, q_bar, 0, ug * G, q0 + i);
+        tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, ug * G, q0 + i);
       }
     }
     // last visible key + 1 of the two rows this thread holds in each tile:
@@ -224,13 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = wbase + s * C::kStageBytes;
         mbar_expect_tx(full_bar(s), C::kStageBytes);
         if (Q8) {
-          tma_load_4d(st, &tm_k, full_bar(s), 0, un.g, 0, blk);
-          tma_load_4d(st + kPage8 / 2, &tm_v, full_bar(s), 0, un.g, 0, blk);
+          tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
+          tma_load_4d(st + kPage8 / 2, &tm_v, full_bar(s), 0, ug, 0, blk);
         } else {
-          tma_load_4d(st, &tm_k, full_bar(s), 0, un.g, 0, blk);
-          tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, un.g, 0, blk);
-          tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, un.g, 0, blk);
-          tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, un.g, 0, blk);
+          tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
+          tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, ug, 0, blk);
+          tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, ug, 0, blk);
+          tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, ug, 0, blk);
         }
       }
     };
@@ -420,12 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
       const int ra = mt * 16 + gid, rb = ra + 8;  // rows: token * G + head in group
       if (un.nsplit == 1) {
-        const int q0 = a.qsl[un.r];
+        const int q0 = un.q0;
         // row -> out[q0 + row / G][g * G + row % G]
         uint16_t* oa = a.out + (int64_t)(q0 + ra / G) * a.out_stride +
-                       (int64_t)(un.g * G + ra % G) * kHeadSize;
+                       (int64_t)(ug * G + ra % G) * kHeadSize;
         uint16_t* ob = a.out + (int64_t)(q0 + rb / G) * a.out_stride +
-                       (int64_t)(un.g * G + rb % G) * kHeadSize;
+                       (int64_t)(ug * G + rb % G) * kHeadSize;
         const float i0 = o_scale / l0, i1 = o_scale / l1;
 #pragma unroll
         for (int dn = 0; dn < 16; ++dn) {
@@ -476,8 +478,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Wo
        item += gridDim.x * kWarpsPerBlock) {
     const SplitPair sp = ws.pairs[item / max_rows];
     const int row = item % max_rows;
-    const int q0 = a.qsl[sp.r];
-    const int rows = (a.qsl[sp.r + 1] - q0) * G;
+    const int q0 = sp.q0;
+    const int rows = sp.qn * G;
     if (row >= rows) continue;
     const float* ml = ws.part_ml + ((int64_t)sp.first + row) * 2;
     const float* po = ws.part_o + ((int64_t)sp.first + row) * kHeadSize + 4 * lane;

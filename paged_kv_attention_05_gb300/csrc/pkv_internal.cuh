@@ -22,23 +22,33 @@ constexpr int kPreTileQ = 128;   // query rows per prefill tile
 // Query rows a decode unit can carry (query tokens x heads of one KV head).
 __host__ __device__ constexpr int dec_rows_cap(int group) { return group <= 16 ? 16 : 32; }
 
-// One decode work unit: request r with qn query tokens (ctx keys before the
-// first one), KV head g, keys [k0, k1) of the request.  Split results occupy
-// partial rows part .. part + qn * G - 1 (row = token * G + head in group).
+// The work lists are a snapshot of the request metadata taken by the plan
+// kernel: the attention kernels read query_start_loc and seq_lens only
+// through them, so a plan can serve several layers (and later changes of the
+// metadata arrays cannot send a kernel out of bounds).
+
+// One decode work unit (32 bytes): request r with qn query tokens starting at
+// row q0 (ctx keys before the first one), KV head g, keys [k0, k1) of the
+// request; gq = g | qn << 16.  Split results occupy partial rows part .. part
+// + qn * G - 1 (row = token * G + head in group).
 struct __align__(16) DecUnit {
-  int r, g, ctx, nsplit, k0, k1, part, qn;
+  int r, gq, ctx, nsplit, k0, k1, part, q0;
 };
 
-// One prefill work entry: request r, 128-row query tile qt; nkv = number of
-// 128-key tiles it reads (work estimate used for longest-first ordering).
+// One prefill work entry: request r (n query rows from q0, seq_len L),
+// 128-row query tile qt; nkv = number of 128-key tiles it reads (the work
+// estimate used for longest-first ordering).
 struct __align__(16) PreEntry {
-  int r, qt, nkv, pad;
+  int r, qt, nkv, q0;
+  int n, L, pad0, pad1;
 };
 
 // A (request, KV head) whose keys were split over several decode units: split
-// s keeps its qn * G partial rows from first + s * qn * G.
+// s keeps its qn * G partial rows from first + s * qn * G; the request's
+// rows start at q0.
 struct __align__(16) SplitPair {
   int r, g, first, nsplit;
+  int q0, qn, pad0, pad1;
 };
 
 // Header of the step plan, written by the plan kernel each call.

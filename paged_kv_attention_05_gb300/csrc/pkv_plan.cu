@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // finding its request by binary search over the chunk's offsets
   __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1], s_off_q[kPlanThreads + 1];
   __shared__ int s_off_p[kPlanThreads], s_len[kPlanThreads], s_n[kPlanThreads];
+  __shared__ int s_q0[kPlanThreads];
   __shared__ int s_max_rows;
   if (tid == 0) s_max_rows = 0;
   __syncthreads();
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     s_off_p[tid] = part_carry + off_p;
     s_len[tid] = ri.L;
     s_n[tid] = ri.n;
+    s_q0[tid] = ri.q0;
     if (tid == 0) {
       s_off_u[kPlanThreads] = tot_u;
       s_off_t[kPlanThreads] = tot_t;
@@ -188,16 +190,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
         if (idx >= ws.max_units) break;
         // two 16-byte stores per unit
         int4* dst = reinterpret_cast<int4*>(ws.units + idx);
-        dst[0] = make_int4(base + lo, g, L - qn, nsplit);
+        dst[0] = make_int4(base + lo, g | (qn << 16), L - qn, nsplit);
         dst[1] = make_int4(sp * chunk, min(L, (sp + 1) * chunk),
-                           nsplit > 1 ? s_off_p[lo] + (g * nsplit + sp) * qn * G : -1, qn);
+                           nsplit > 1 ? s_off_p[lo] + (g * nsplit + sp) * qn * G : -1, s_q0[lo]);
       }
       const int cnt_q = s_off_q[lo + 1] - s_off_q[lo];
       for (int g = ln; g < cnt_q; g += 32) {
         const int64_t idx = (int64_t)pair_carry + s_off_q[lo] + g;
         if (idx >= ws.max_pairs) break;
-        *reinterpret_cast<int4*>(ws.pairs + idx) =
-            make_int4(base + lo, g, s_off_p[lo] + g * nsplit * qn * G, nsplit);
+        int4* dst = reinterpret_cast<int4*>(ws.pairs + idx);
+        dst[0] = make_int4(base + lo, g, s_off_p[lo] + g * nsplit * qn * G, nsplit);
+        dst[1] = make_int4(s_q0[lo], qn, 0, 0);
       }
     }
     for (int i = tid; i < tot_t; i += kPlanThreads) {
@@ -209,8 +212,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       const int64_t idx = (int64_t)pre_carry + i;
       if (idx >= ws.max_pre) break;
       const int last_row = min(kPreTileQ * (t + 1), n);
-      *reinterpret_cast<int4*>(ws.pre + idx) =
-          make_int4(base + lo, t, (ctx + last_row + kPreTileQ - 1) / kPreTileQ, 0);
+      int4* dst = reinterpret_cast<int4*>(ws.pre + idx);
+      dst[0] = make_int4(base + lo, t, (ctx + last_row + kPreTileQ - 1) / kPreTileQ, s_q0[lo]);
+      dst[1] = make_int4(n, s_len[lo], 0, 0);
     }
     unit_carry += tot_u;
     part_carry += tot_p;

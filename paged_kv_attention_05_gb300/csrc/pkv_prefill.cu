@@ -235,25 +235,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
     // Global loads are issued one step before their values are needed: the
-    // next item's cursor and entry while the current item is being issued,
-    // its request's lengths after the current item's first tile, and each
-    // tile's block ids one tile ahead; a load only stalls at its first use.
+    // next item's cursor and entry (which carries its request's lengths)
+    // while the current item is being issued, and each tile's block ids one
+    // tile ahead; a load only stalls at its first use.
     uint32_t tile_cnt = 0, vt_uses[kStages] = {0, 0}, qx_cnt[2] = {0, 0};
     int w_nxt = 0;
     if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
     w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
-    PreEntry e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : PreEntry{-1, 0, 0, 0};
-    int q0_nxt = 0, q1_nxt = 0, L_nxt = 0;
-    if (e_nxt.r >= 0) {
-      q0_nxt = a.qsl[e_nxt.r];
-      q1_nxt = a.qsl[e_nxt.r + 1];
-      L_nxt = a.seq_lens[e_nxt.r];
-    }
+    const PreEntry none{-1, 0, 0, 0, 0, 0, 0, 0};
+    PreEntry e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
     for (uint32_t it_cnt = 0;; ++it_cnt) {
       const int slot = it_cnt & 1;
       const int w = w_nxt;
       const PreEntry e = e_nxt;
-      const int q0 = q0_nxt, q1 = q1_nxt, Lr = L_nxt;
+      const int q0 = e.q0, q1 = e.q0 + e.n, Lr = e.L;
       if (it_cnt >= 2 &&
           !mbar_wait_warp(bar(B_IE + slot), ((it_cnt >> 1) - 1) & 1, abort, ws.err))
         break;
@@ -286,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next item's cursor and entry (consumed after this item)
       if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
       w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
-      e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : PreEntry{-1, 0, 0, 0};
+      e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
       const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
       const int row0 = it.q0 + it.qt * kPreTileQ;
       // Q tiles, once the previous item's last S has read them
@@ -319,11 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         int blk = blk_nxt;
         if (j + 1 < it.nkv && lane < tile_pages(j + 1))
           blk_nxt = __ldg(btrow + ((key0 + kTileK) >> 4) + lane);
-        if (j == 0 && e_nxt.r >= 0) {  // the next item's request lengths
-          q0_nxt = a.qsl[e_nxt.r];
-          q1_nxt = a.qsl[e_nxt.r + 1];
-          L_nxt = a.seq_lens[e_nxt.r];
-        }
         if (c >= (uint32_t)kStages &&
             !mbar_wait_warp(bar(B_KE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
           ok = false;
