@@ -108,3 +108,38 @@ def test_python_binding_requires_cuda_tensors():
         pkv.pkv_write(k, k, kc, kc, sm)
     with pytest.raises(TypeError):
         pkv.pkv_write(k.float(), k, kc, kc, sm)
+
+
+def test_int8_and_plan_calls_reject_bad_arguments_on_host(lib):
+    ct = ctypes
+    i64, i32, f32, vp = ct.c_int64, ct.c_int32, ct.c_float, ct.c_void_p
+    lib.pkv_write_int8.restype = ct.c_int
+    lib.pkv_write_int8.argtypes = [vp, i64, vp, i64, vp, vp, f32, f32, i64, i32, i32, i32, vp, i64,
+                                   vp]
+    lib.pkv_attention_int8.restype = ct.c_int
+    lib.pkv_attention_int8.argtypes = [vp, i64, i64, i32, vp, vp, f32, f32, i64, i32, i32, i32,
+                                       vp, vp, vp, i64, i32, f32, vp, i64, vp]
+    lib.pkv_plan.restype = ct.c_int
+    lib.pkv_plan.argtypes = [i64, i32, i32, vp, vp, i64, i32, vp]
+    lib.pkv_attention_planned.restype = ct.c_int
+    lib.pkv_attention_planned.argtypes = [vp, i64, i32, vp, vp, i64, i32, i32, i32, vp, f32, vp,
+                                          i64, vp]
+    # int8 write: scales must be finite and positive; geometry as pkv_write
+    w8 = lambda ks, vs, bs=16: lib.pkv_write_int8(FAKE, 1024, FAKE, 1024, FAKE, FAKE, ks, vs, 10,
+                                                  bs, 8, 128, FAKE, 4, None)
+    assert w8(0.0, 0.1) == -1 and w8(0.1, float("nan")) == -1 and w8(-1.0, 0.1) == -1
+    assert w8(float("inf"), 0.1) == -1 and w8(0.1, 0.1, bs=8) == -2
+    # int8 attention: the same checks as pkv_attention, plus the scales
+    a8 = lambda ks, vs, hq=32: lib.pkv_attention_int8(FAKE, 4096, 4, hq, FAKE, FAKE, ks, vs, 10,
+                                                      16, 8, 128, FAKE, FAKE, FAKE, 4, 2, 0.088,
+                                                      FAKE, 4096, None)
+    assert a8(0.0, 0.1) == -1 and a8(0.1, 0.1, hq=30) == -2
+    # the plan: metadata checks of pkv_attention
+    pl = lambda hq=32, hkv=8, w=4, R=2, qsl=FAKE: lib.pkv_plan(4, hq, hkv, qsl, FAKE, w, R, None)
+    assert pl(hq=30) == -2 and pl(hkv=0) == -1 and pl(R=-1) == -1 and pl(qsl=None) == -1
+    assert pl(w=40000) == -2
+    # a planned call: geometry checked before the device is looked at
+    ap = lambda bs=16, d=128, hkv=8: lib.pkv_attention_planned(FAKE, 4096, 32, FAKE, FAKE, 10, bs,
+                                                               hkv, d, FAKE, 0.088, FAKE, 4096,
+                                                               None)
+    assert ap(bs=32) == -2 and ap(d=64) == -2 and ap(hkv=40000) == -2
