@@ -30,14 +30,18 @@
 //               (MN-major), O accumulating in TMEM; tcgen05.commit drives the
 //               mbarriers.  Because one thread's MMAs complete in order, S(j+1)
 //               being ready also means PV(j) is done;
-//   warps 2-5   softmax for tile a, warps 6-9 for tile b, one query row per
-//               thread (TMEM lane = 32 * (warp % 4) + lane = row): scores -> causal/length mask (only
-//               on tiles that cross the diagonal) -> running max in the log2
-//               domain -> exp2 -> row sum -> bf16 P back into TMEM.  The two
-//               warpgroups alternate with the tensor pipe.  O is rescaled in
-//               TMEM only when a row's max grows by more than 2^8 (exact,
-//               rare).  At the end of an item the same warps divide by the row
-//               sum and write the bf16 rows to global memory.
+//   warps 2-9   softmax, two warps per row quarter (one per 64-key half of
+//               the scores), one query row per thread (TMEM lane = 32 *
+//               (warp % 4) + lane = row), both query tiles in turn: scores ->
+//               causal/length mask (only on tiles that cross the diagonal) ->
+//               running max in the log2 domain -> exp2 -> row sum -> bf16 P
+//               back into TMEM.  O is rescaled in TMEM only when a row's max
+//               grows by more than 2^8 (exact, rare).  At the end of an item
+//               each warp leaves its partial row sums in shared memory;
+//   warps 10-13 epilogue: once O_x is final, read it out of TMEM in two
+//               64-column halves, divide by the row sum, release O_x to the
+//               next item's first P.V and write the bf16 rows to global memory
+//               through a per-warp staging area (whole 64-byte row pieces).
 // Every mbarrier wait is bounded; on expiry the kernel records
 // PKV_DEV_ERR_TIMEOUT, stops issuing work, frees its TMEM and returns.
 #include "pkv_device.cuh"
@@ -47,7 +51,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 320;                     // 10 warps
+constexpr int kThreads = 448;                     // 14 warps
 constexpr int kStages = 2;
 constexpr int kTileK = 128;                       // keys per KV tile
 constexpr int kHalfBytes = 128 * 128;             // 128 rows x 64 bf16
@@ -61,8 +65,9 @@ constexpr int kOffQ = 0;                          // Q_a | Q_b
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kStageWarp = 32 * 64;               // epilogue staging: 32 rows x 64 bytes
-constexpr int kOffStage = kOffV + kStages * kTileBytes;  // one staging area per softmax warp
-constexpr int kOffBar = kOffStage + 8 * kStageWarp;
+constexpr int kOffStage = kOffV + kStages * kTileBytes;  // one staging area per epilogue warp
+constexpr int kOffLsum = kOffStage + 4 * kStageWarp;  // [2 items][2 tiles][2 halves][128 rows]
+constexpr int kOffBar = kOffLsum + 2 * 2 * 2 * 128 * 4;
 enum {
   B_QF = 0,   // [2] Q tile loaded
   B_QE = 2,   // [2] Q tile consumed by the item's last S
@@ -78,7 +83,8 @@ enum {
   B_IF = 22,  // [2] item slot published
   B_IE = 24,  // [2] item slot released
   B_XP = 26,  // [4] exchange between the two softmax warps of a row quarter
-  kNumBars = 30
+  B_LF = 30,  // [2] row sums of tile x written for the epilogue
+  kNumBars = 32
 };
 constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 item slots
 constexpr int kOffXch = kOffItems + 2 * 48;        // [4 quarters][2 slots][2 halves][32] floats
@@ -183,6 +189,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])                              \
       : "memory")
 
+#define PKV_LD16(taddr, v)                                                                     \
+  asm volatile(                                                                                \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15}, [%16];\n"                                                                     \
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),   \
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]),            \
+        "=f"(v[13]), "=f"(v[14]), "=f"(v[15])                                                  \
+      : "r"(taddr))
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
@@ -213,8 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_PF + x), 8);  // one arrival per softmax warp (each writes half of P)
-      mbar_init(bar(B_OE + x), 8);
-      mbar_init(bar(B_IE + x), 1 + 8);  // MMA thread + one lane of each softmax warp
+      mbar_init(bar(B_OE + x), 4);  // one arrival per epilogue warp
+      mbar_init(bar(B_LF + x), 8);  // one arrival per softmax warp
+      mbar_init(bar(B_IE + x), 1 + 8 + 4);  // MMA warp, softmax warps, epilogue warps
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_XP + i), 2);
     ctl[1] = 0;
@@ -459,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ------------- softmax + epilogue: two warps per row, a column half each -------------
+  } else if (warp < 10) {
+    // ------------------- softmax: two warps per row, a column half each -------------------
     // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its 32 rows, one per
     // thread) and key columns 64 * hf .. 64 * hf + 63, hf = (w - 2) / 4, of
     // both query tiles of the item in turn; both warps of a row quarter (w and
@@ -487,94 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       x_cnt++;
       return xch[((qd * 2 + sl) * 2 + (1 - hf)) * 32 + lane];
     };
-    // The epilogue of an item (O / l in bf16 to its output rows) is split in
-    // two around the next item's first softmax step, tile by tile: first O_x
-    // is read out of TMEM (normalised and packed to bf16 in registers) and
-    // released, so that the next item's first P.V can follow its first P
-    // without waiting for the stores; then, after that softmax step, the
-    // packed rows are written out.  The last item's epilogue runs whole.
-    bool pending = false;
-    Item pv_it{};                      // the item whose epilogue is pending
-    float pv_l[2] = {0.f, 0.f};        // its partial row sums (this warp's half)
-    uint32_t held[32];                 // one tile's O half of the row, bf16 pairs
-    // read O_x of the pending item, release it
-    auto take_o = [&](int x) {
-      const float lo = exchange(pv_l[x]);
-      if (!ok) return;
-      const float l = hf == 0 ? pv_l[x] + lo : lo + pv_l[x];  // the same in both warps
-      if (!mbar_wait_warp(bar(B_OF + x), o_cnt[x]++ & 1, abort, ws.err)) {
-        ok = false;
-        return;
-      }
-      tc_fence_after();
-      const float inv = 1.f / l;
-      const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
-      float ov[64];
-      PKV_LD32(t_o, (ov + 0));
-      PKV_LD32(t_o + 32, (ov + 32));
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) held[i] = pack_bf16(ov[2 * i] * inv, ov[2 * i + 1] * inv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OE + x));
-    };
-    // write the held rows: each 32-column chunk of the warp's 32 rows goes
-    // through the warp's staging area in shared memory, so that each global
-    // store writes whole 64-byte row pieces (8 rows x 4 lanes) instead of 32
-    // scattered 16-byte pieces
-    auto store_o = [&](int x) {
-      const int h = x == 0 ? pv_it.ha : pv_it.hb;
-      // (the thread index passes through an opaque move so that the staging
-      // addresses below are computed here, not kept live across the loop)
-      int ti;
-      asm volatile("mov.b32 %0, %1;\n" : "=r"(ti) : "r"(tid));
-      const int ln = ti & 31;
-      const uint32_t stg = sbase + kOffStage + ((ti >> 5) - 2) * kStageWarp;
-      const int row_base = pv_it.qt * kPreTileQ + qd * 32;  // the warp's first row
-      uint16_t* obase =
-          a.out + (int64_t)pv_it.q0 * a.out_stride + (int64_t)h * kHeadSize + 64 * hf;
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
-        // that eight lanes of a store phase hit eight different bank groups
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                           stg + ln * 64 + ((k ^ ((ln >> 1) & 3)) << 4)),
-                       "r"(held[ch * 16 + 4 * k]), "r"(held[ch * 16 + 4 * k + 1]),
-                       "r"(held[ch * 16 + 4 * k + 2]), "r"(held[ch * 16 + 4 * k + 3])
-                       : "memory");
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int rr = i * 8 + (ln >> 2), c = ln & 3;
-          uint4 v;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
-                       : "memory");
-          const int qr = row_base + rr;
-          if (qr < pv_it.n)
-            *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + ch * 32 + c * 8) = v;
-        }
-        __syncwarp();
-      }
-    };
+    float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
     for (uint32_t it_cnt = 0; ok; ++it_cnt) {
       const int slot = it_cnt & 1;
       if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
       const Item it = items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_IE + slot));
-      if (it.r < 0) {
-        // no next item: the pending epilogue runs whole
-        for (int x = 0; pending && x < (pv_it.hb >= 0 ? 2 : 1) && ok; ++x) {
-          take_o(x);
-          if (ok) store_o(x);
-        }
-        break;
-      }
+      if (it.r < 0) break;
       const int nx = it.hb >= 0 ? 2 : 1;
       const int qrow = it.qt * kPreTileQ + row;  // row inside the request
       const bool valid_row = qrow < it.n;
@@ -584,10 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = qpos - j * kTileK - 64 * hf;  // my columns <= lim are visible
         const bool masked = !__all_sync(0xffffffffu, lim >= 63);
         for (int x = 0; x < nx && ok; ++x) {
-          if (j == 0 && pending) {
-            take_o(x);
-            if (!ok) break;
-          }
           if (!mbar_wait_warp(bar(B_SF + x), s_cnt[x]++ & 1, abort, ws.err)) {
             ok = false;
             break;
@@ -682,14 +614,105 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_PF + x));
-          if (j == 0 && pending) store_o(x);  // the previous item's rows of tile x
         }
       }
       if (!ok) break;
-      pending = true;
-      pv_it = it;
-      pv_l[0] = l_part[0];
-      pv_l[1] = l_part[1];
+      // this warp's partial row sums of the item, for the epilogue warps
+      for (int x = 0; x < nx; ++x) {
+        lsum[(((it_cnt & 1) * 2 + x) * 2 + hf) * 128 + row] = l_part[x];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_LF + x));
+      }
+    }
+  } else {
+    // ------------------ epilogue: one warp per TMEM lane quarter ------------------
+    // Warp w (10..13) owns rows 32 * (w % 4) .. + 31 of both output tiles.  When
+    // O_x is final (its last P.V done) and both partial row sums are in, the
+    // warp reads the 128-column row block out of TMEM in two halves,
+    // normalises them and packs them to bf16 in registers, and releases O_x as
+    // soon as the second half is read (the next item's first P.V may then
+    // overwrite it); each 32-column chunk goes out through the warp's staging
+    // area in shared memory, so that each global store writes whole 64-byte
+    // row pieces (8 rows x 4 lanes).
+    // The softmax warps never wait for this work.
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;  // == TMEM lane
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const float* lsum = reinterpret_cast<const float*>(smem + kOffLsum);
+    const uint32_t stg = sbase + kOffStage + (warp - 10) * kStageWarp;
+    uint32_t o_cnt[2] = {0, 0};
+    for (uint32_t it_cnt = 0;; ++it_cnt) {
+      const int slot = it_cnt & 1;
+      if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+      const Item it = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IE + slot));
+      if (it.r < 0) break;
+      const int nx = it.hb >= 0 ? 2 : 1;
+      bool ok = true;
+      for (int x = 0; x < nx && ok; ++x) {
+        const uint32_t par = o_cnt[x]++ & 1;
+        if (!mbar_wait_warp(bar(B_OF + x), par, abort, ws.err) ||
+            !mbar_wait_warp(bar(B_LF + x), par, abort, ws.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* ls = lsum + ((it_cnt & 1) * 2 + x) * 2 * 128;
+        const float inv = 1.f / (ls[row] + ls[128 + row]);  // the two column halves' sums
+        const uint32_t t_o = tmem + 256 + x * 128 + lane_off;
+        const int h = x == 0 ? it.ha : it.hb;
+        const int row_base = it.qt * kPreTileQ + qd * 32;  // the warp's first row
+        uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize;
+        // two 64-column halves; O_x is released once the second half is in
+        // registers (the first half is already on its way out by then)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t held[32];  // 64 outputs of the row, bf16 pairs
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float ov[16];
+            PKV_LD16(t_o + half * 64 + ch * 16, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              held[ch * 8 + i] = pack_bf16(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+          }
+          if (half == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_OE + x));
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            // this lane's row: 16-byte piece k at slot k ^ ((lane >> 1) & 3), so
+            // that eight lanes of a store phase hit eight different bank groups
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                               stg + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)),
+                           "r"(held[cc * 16 + 4 * k]), "r"(held[cc * 16 + 4 * k + 1]),
+                           "r"(held[cc * 16 + 4 * k + 2]), "r"(held[cc * 16 + 4 * k + 3])
+                           : "memory");
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = i * 8 + (lane >> 2), c = lane & 3;
+              uint4 v;
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                           : "r"(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
+                           : "memory");
+              const int qr = row_base + rr;
+              if (qr < it.n)
+                *reinterpret_cast<uint4*>(obase + (int64_t)qr * a.out_stride + half * 64 +
+                                          cc * 32 + c * 8) = v;
+            }
+            __syncwarp();
+          }
+        }
+      }
+      if (!ok) break;
     }
   }
 
