@@ -437,7 +437,7 @@ def main():
     rec = {"metric": name, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
-           "dtype": "int8 cache, bf16 math" if int8 else "bf16", "data": "synthetic",
+           "dtype": "int8 cache, fp16 math" if int8 else "bf16", "data": "synthetic",
            "config": {"workload": spec.name, "requests": s.num_reqs, "query_tokens": s.num_tokens,
                       "step": ("prepare + " if args.with_prepare else "") + "write + attention",
                       "num_heads": s.hq, "num_kv_heads": s.hkv, "head_size": d,

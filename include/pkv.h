@@ -239,8 +239,11 @@ int pkv_write_int8(const void* k, int64_t k_row_stride, const void* v, int64_t v
 /*
  * pkv_attention_int8 — pkv_attention over int8 caches written by
  * pkv_write_int8: the same formula with K_j = k_scale * code and V_j =
- * v_scale * code.  The codes are widened to bf16 exactly on chip; k_scale is
- * folded into the softmax scale and v_scale into the output.
+ * v_scale * code.  The products run on fp16 operands: the codes are exact
+ * fp16 integers, the query is multiplied by scale * log2(e) * k_scale and
+ * rounded to fp16 (so |q| * scale * k_scale * 1.4427 must stay below 65504,
+ * the fp16 range; a larger product gives inf), the probabilities are fp16,
+ * accumulation is fp32, and v_scale is applied to the output.
  *
  * Requests on the decode path only: a request whose query_len * (num_heads /
  * num_kv_heads) is at most 16 (32 when the group is larger than 16) —

@@ -319,7 +319,7 @@ int plan_locked(DeviceState* s, int64_t q_rows, int32_t num_heads, int32_t num_k
   a.bt_width = block_table_width;
   a.num_reqs = num_reqs;
   a.kv_int8 = kv_int8;
-  const int workers = decode_workers(num_heads / num_kv_heads, s->sms);
+  const int workers = decode_workers(num_heads / num_kv_heads, kv_int8, s->sms);
   cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   // an int8 plan leaves prefill-class requests out: it cannot serve a bf16 call

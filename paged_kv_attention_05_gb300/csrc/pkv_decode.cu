@@ -37,6 +37,8 @@
 //     several writes (max, sum, unnormalised output) in fp32 to the workspace,
 //     and the combine kernel merges the splits afterwards.  Every mbarrier wait
 //     is bounded.
+// The int8-cache variant of the decode kernel is in pkv_decode_i8.cu; it
+// shares the plan, the work units and the combine kernel below.
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -51,18 +53,12 @@ constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2
 constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
 constexpr int kIdRegs = kMaxChunk / kBlockSize / 32;  // block ids per lane per unit
 
-// int8 caches: one 2 KB box of 16 slots x 128 codes per page and K/V, so a
-// stage is 4 KB; the warp widens each page into a bf16 page (kPage) in the
-// layout the bf16 path reads, and the rest of the math is shared.
-constexpr int kPage8 = 2 * kBlockSize * 128;
-
-template <int MT, bool Q8>
+template <int MT>
 struct Cfg {
-  static constexpr int kStages = Q8 ? (MT == 1 ? 4 : 3) : (MT == 1 ? 3 : 2);
-  static constexpr int kStageBytes = Q8 ? kPage8 : kPage;
-  static constexpr int kScratch = Q8 ? kPage : 0;      // the widened bf16 page
+  static constexpr int kStages = MT == 1 ? 3 : 2;
+  static constexpr int kStageBytes = kPage;
   static constexpr int kQHalf = MT * 16 * 128;        // query rows x one 64-dim half
-  static constexpr int kWarpBytes = kStages * kStageBytes + kScratch + 2 * kQHalf;
+  static constexpr int kWarpBytes = kStages * kStageBytes + 2 * kQHalf;
   static constexpr int kBarsPerWarp = kStages + 1;     // page stages, query
   static constexpr int kOffBar = kWarps * kWarpBytes;
   static constexpr int kOffCtl = kOffBar + kWarps * kBarsPerWarp * 8;
@@ -99,26 +95,11 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok_lo, int valid)
   return v & (lo | hi);
 }
 
-// Four int8 codes (one 32-bit word) to four bf16 values (two packed words),
-// exactly: each code c, offset by 128, becomes the low mantissa byte of the
-// float 2^23 + 128 + c, from which 2^23 + 128 is subtracted.
-__device__ __forceinline__ uint2 i8x4_to_bf16x4(uint32_t w) {
-  const uint32_t u = w ^ 0x80808080u;
-  float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540));
-  float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541));
-  float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542));
-  float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543));
-  constexpr float kBias = 8388736.0f;  // 2^23 + 128
-  padd2(f0, f1, f0, f1, -kBias, -kBias);
-  padd2(f2, f3, f2, f3, -kBias, -kBias);
-  return make_uint2(pack_bf16(f0, f1), pack_bf16(f2, f3));
-}
-
-template <int MT, bool Q8>
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
-  using C = Cfg<MT, Q8>;
+  using C = Cfg<MT>;
   if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -127,8 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = a.hq / a.hkv;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t wbase = sbase + warp * C::kWarpBytes;        // this warp's page stages
-  const uint32_t scratch = wbase + C::kStages * C::kStageBytes;  // widened page (int8 caches)
-  const uint32_t qbuf = scratch + C::kScratch;                  // and query rows
+  const uint32_t qbuf = wbase + C::kStages * C::kStageBytes;  // and query rows
   const uint32_t bars = sbase + C::kOffBar + warp * C::kBarsPerWarp * 8;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   const uint32_t q_bar = bars + 8u * C::kStages;
@@ -150,9 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
-  // int8 caches: S = k_scale * (q . codes), O = v_scale * (P . codes)
-  const float sl2 = a.scale * kLog2e * (Q8 ? a.k_scale : 1.f);
-  const float o_scale = Q8 ? a.v_scale : 1.f;
+  const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
   uint32_t page_cnt = 0;
@@ -225,15 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_async_smem();
         const uint32_t st = wbase + s * C::kStageBytes;
         mbar_expect_tx(full_bar(s), C::kStageBytes);
-        if (Q8) {
-          tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
-          tma_load_4d(st + kPage8 / 2, &tm_v, full_bar(s), 0, ug, 0, blk);
-        } else {
-          tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
-          tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, ug, 0, blk);
-          tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, ug, 0, blk);
-          tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, ug, 0, blk);
-        }
+        tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
+        tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, ug, 0, blk);
+        tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, ug, 0, blk);
+        tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, ug, 0, blk);
       }
     };
     for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
@@ -271,36 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int pos0 = k0 + p * kBlockSize;
       const int valid = k1 - pos0;  // keys of this page inside the unit
-      uint32_t st = wbase + s * C::kStageBytes;
-      if (Q8) {
-        // widen the int8 page (K rows, then V rows: 16 slots x 128 codes,
-        // 128-byte swizzle) into the bf16 page: 256 16-byte pieces of codes,
-        // 8 per lane, each giving two 16-byte pieces of bf16 values
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int pc = lane + 32 * i;
-          const int mat = pc >> 7, row = (pc >> 3) & 15, j = pc & 7;  // j: codes 16j..16j+15
-          uint4 w;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                       : "r"(st + mat * (kPage8 / 2) + row * 128 + ((j ^ (row & 7)) << 4)));
-          const uint2 b0 = i8x4_to_bf16x4(w.x), b1 = i8x4_to_bf16x4(w.y);
-          const uint2 b2 = i8x4_to_bf16x4(w.z), b3 = i8x4_to_bf16x4(w.w);
-          const uint32_t box = scratch + (mat * 2 + (j >> 2)) * kBox;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                           box + sw128(row, (j & 3) * 2)),
-                       "r"(b0.x), "r"(b0.y), "r"(b1.x), "r"(b1.y)
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
-                           box + sw128(row, (j & 3) * 2 + 1)),
-                       "r"(b2.x), "r"(b2.y), "r"(b3.x), "r"(b3.y)
-                       : "memory");
-        }
-        __syncwarp();
-        // the stage is free again: its next page can be on its way already
-        if (p + C::kStages < npages) issue_page(p + C::kStages);
-        st = scratch;
-      }
+      const uint32_t st = wbase + s * C::kStageBytes;
 
       // S = Q K^T for the page's 16 keys (two n-tiles of 8)
       float sacc[MT][2][4];
@@ -407,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (!Q8 && p + C::kStages < npages) issue_page(p + C::kStages);
+      if (p + C::kStages < npages) issue_page(p + C::kStages);
     }
     if (!ok) break;
     page_cnt += npages;
@@ -428,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (int64_t)(ug * G + ra % G) * kHeadSize;
         uint16_t* ob = a.out + (int64_t)(q0 + rb / G) * a.out_stride +
                        (int64_t)(ug * G + rb % G) * kHeadSize;
-        const float i0 = o_scale / l0, i1 = o_scale / l1;
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
         for (int dn = 0; dn < 16; ++dn) {
           const int col = dn * 8 + tig * 2;
@@ -444,10 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col = dn * 8 + tig * 2;
           if (ra < nrows)
             *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
-                make_float2(o[mt][dn][0] * o_scale, o[mt][dn][1] * o_scale);
+                make_float2(o[mt][dn][0], o[mt][dn][1]);
           if (rb < nrows)
             *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
-                make_float2(o[mt][dn][2] * o_scale, o[mt][dn][3] * o_scale);
+                make_float2(o[mt][dn][2], o[mt][dn][3]);
         }
         if (tig == 0) {
           if (ra < nrows)
@@ -507,40 +451,36 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Wo
   }
 }
 
-template <int MT, bool Q8>
+template <int MT>
 cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
-  using C = Cfg<MT, Q8>;
+  using C = Cfg<MT>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT, Q8>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int G = a.hq / a.hkv;
   CUtensorMap tq, tk, tv;
-  const bool maps = make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) &&
-                    (Q8 ? make_cache_map_i8(&tk, a.kc, a.num_blocks, a.hkv) &&
-                              make_cache_map_i8(&tv, a.vc, a.num_blocks, a.hkv)
-                        : make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) &&
-                              make_cache_map(&tv, a.vc, a.num_blocks, a.hkv));
-  if (!maps) return cudaErrorInvalidValue;
-  decode_kernel<MT, Q8><<<sms, kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
+  if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) ||
+      !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
+      !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
+    return cudaErrorInvalidValue;
+  decode_kernel<MT><<<sms, kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_workers(int group, int sms) {
-  (void)group;
-  return sms * kWarps;
+int decode_workers(int group, int kv_int8, int sms) {
+  return sms * (kv_int8 ? decode_i8_warps(group) : kWarps);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   const int G = a.hq / a.hkv;
-  if (a.kv_int8)
-    return G <= 16 ? launch_mt<1, true>(a, ws, sms, st) : launch_mt<2, true>(a, ws, sms, st);
-  return G <= 16 ? launch_mt<1, false>(a, ws, sms, st) : launch_mt<2, false>(a, ws, sms, st);
+  if (a.kv_int8) return launch_decode_i8(a, ws, sms, st);
+  return G <= 16 ? launch_mt<1>(a, ws, sms, st) : launch_mt<2>(a, ws, sms, st);
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {

@@ -152,10 +152,13 @@ cudaError_t launch_prepare(const PrepArgs& p, int sms, cudaStream_t st);
 
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st);
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
+// the decode path over int8 caches (pkv_decode_i8.cu)
+cudaError_t launch_decode_i8(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
-// Independent decode workers (warp groups) the decode grid runs for a head
-// grouping; the plan sizes its split chunks for this many.
-int decode_workers(int group, int sms);
+// Independent decode workers (warps) the decode grid runs for a head grouping
+// and cache type; the plan sizes its split chunks for this many.
+int decode_workers(int group, int kv_int8, int sms);
+int decode_i8_warps(int group);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
 }  // namespace pkv

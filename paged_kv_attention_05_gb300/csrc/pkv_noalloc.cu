@@ -144,7 +144,7 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
   a.kv_int8 = 0;
   a.k_scale = a.v_scale = 1.f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((e = launch_plan(a, ws, decode_workers(group, sms), st)) != cudaSuccess ||
+  if ((e = launch_plan(a, ws, decode_workers(group, 0, sms), st)) != cudaSuccess ||
       (e = launch_decode(a, ws, sms, st)) != cudaSuccess ||
       (e = launch_combine(a, ws, sms, st)) != cudaSuccess ||
       (e = launch_prefill(a, ws, sms, st)) != cudaSuccess)
