@@ -284,9 +284,6 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
       const uint4 vB = lds128(st + kBox8 + sw128(2 * tig + 1, gid));
       const uint4 vC = lds128(st + kBox8 + sw128(2 * tig + 8, gid));
       const uint4 vD = lds128(st + kBox8 + sw128(2 * tig + 9, gid));
-      __syncwarp();
-      // the stage is free again: its next page can be on its way already
-      if (p + C::kStages < npages) issue_page(p + C::kStages);
 
       // S = Q K^T (log2 domain) for the page's 16 keys (two n-tiles of 8)
       float sacc[MT][2][4];
@@ -319,6 +316,11 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
           mma_f16(sacc[mt][1], qf, b10, b11);
         }
       }
+
+      // the stage's codes are all in registers: its next page can be on its
+      // way (issued here, behind the S MMAs, whose latency hides the branch)
+      __syncwarp();
+      if (p + C::kStages < npages) issue_page(p + C::kStages);
 
       // online softmax in the log2 domain, keys >= the row's limit masked;
       // the output is rescaled only when a row's maximum grows by more than 2^8
