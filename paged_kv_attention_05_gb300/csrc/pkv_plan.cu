@@ -13,6 +13,11 @@
 //   * prefill entries (request, 128-row query tile) for requests with more
 //     than one query token, ordered longest first;
 //   * a header with the counts, the split size and zeroed scheduler cursors.
+// The kernel runs a few CTAs: each one reads the whole metadata and forms
+// every offset (the scans are cheap and the same in every CTA), then writes
+// its share of the entries — one request per warp of the grid — so that a
+// batch of hundreds of requests and tens of thousands of units is not
+// written by a single SM.
 // "vLLM MHA Code Path: From QKV to Paged KV Cache", section "Prefill and
 // decode share an interface": the phase of a request is told apart only by
 // its query and sequence lengths, which is what this kernel does.
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
     if (r < a.num_reqs) ri = classify(a, r);
-    if (ri.bad) atomicOr(ws.err, ri.bad);
+    if (ri.bad && blockIdx.x == 0) atomicOr(ws.err, ri.bad);
     int units = 0, parts = 0, tiles = 0, pairs = 0;
     if (ri.kind == 1) {
       const int nsplit = (ri.L + chunk - 1) / chunk;
@@ -174,11 +179,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       s_off_q[kPlanThreads] = tot_q;
     }
     __syncthreads();
-    // decode units and split pairs: one warp per request (a request's entries
-    // are contiguous), lanes over its entries, so that consecutive lanes
-    // write consecutive entries with no search for the owner
-    for (int lo = tid >> 5; lo < kPlanThreads && base + lo < a.num_reqs;
-         lo += kPlanThreads / 32) {
+    // decode units and split pairs: one warp of the grid per request (a
+    // request's entries are contiguous), lanes over its entries, so that
+    // consecutive lanes write consecutive entries with no search for the owner
+    for (int lo = blockIdx.x * (kPlanThreads / 32) + (tid >> 5);
+         lo < kPlanThreads && base + lo < a.num_reqs; lo += gridDim.x * (kPlanThreads / 32)) {
       const int ln = tid & 31;
       const int cnt_u = s_off_u[lo + 1] - s_off_u[lo];
       if (cnt_u == 0) continue;
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
         dst[1] = make_int4(s_q0[lo], qn, 0, 0);
       }
     }
-    for (int i = tid; i < tot_t; i += kPlanThreads) {
+    for (int i = blockIdx.x * kPlanThreads + tid; i < tot_t; i += gridDim.x * kPlanThreads) {
       const int lo = find_owner(s_off_t, i);
       // a request's query tiles from the last (most keys) to the first, so
       // that the persistent prefill grid starts with the longest items
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     pair_carry += tot_q;
     __syncthreads();  // the chunk's offsets are reused by the next chunk
   }
-  if (tid == 0) {
+  if (blockIdx.x == 0 && tid == 0) {
     ws.hdr->n_dec_units = (int)min((int64_t)unit_carry, ws.max_units);
     ws.hdr->n_pre_entries = (int)min((int64_t)pre_carry, ws.max_pre);
     ws.hdr->dec_counter = 0;
@@ -236,7 +241,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
 }  // namespace
 
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st) {
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(a, ws, dec_grid);
+  // one warp per request of the first 1024-request chunk, at most 16 CTAs
+  const int warps = kPlanThreads / 32;
+  const int grid = a.num_reqs <= warps ? 1 : (a.num_reqs >= 16 * warps ? 16 : (a.num_reqs + warps - 1) / warps);
+  plan_kernel<<<grid, kPlanThreads, 0, st>>>(a, ws, dec_grid);
   return cudaGetLastError();
 }
 
