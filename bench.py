@@ -422,7 +422,8 @@ def main():
         peak = peaks.get("hbm_gbs")
         roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
                 "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
-        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % dominant,
+        kfile = "decode_i8" if (int8 and dominant == "decode") else dominant
+        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % kfile,
                 "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
                 "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
     if roof["peak"] is None:

@@ -28,31 +28,50 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Exclusive block-wide prefix sum of one int per thread (1024 threads).
-__device__ int block_exclusive_scan(int x, int* total, int* smem32) {
+// Exclusive block-wide prefix sums of four ints per thread (1024 threads),
+// the four scans sharing their barriers.
+__device__ int4 block_exclusive_scan4(int4 x, int4* total, int4* smem33) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = x;
+  int4 incl = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    const int y0 = __shfl_up_sync(0xffffffffu, incl.x, o);
+    const int y1 = __shfl_up_sync(0xffffffffu, incl.y, o);
+    const int y2 = __shfl_up_sync(0xffffffffu, incl.z, o);
+    const int y3 = __shfl_up_sync(0xffffffffu, incl.w, o);
+    if (lane >= o) {
+      incl.x += y0;
+      incl.y += y1;
+      incl.z += y2;
+      incl.w += y3;
+    }
   }
-  if (lane == 31) smem32[warp] = incl;
+  if (lane == 31) smem33[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = smem32[lane];
-    int wi = w;
+    const int4 w = smem33[lane];
+    int4 wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
+      const int y0 = __shfl_up_sync(0xffffffffu, wi.x, o);
+      const int y1 = __shfl_up_sync(0xffffffffu, wi.y, o);
+      const int y2 = __shfl_up_sync(0xffffffffu, wi.z, o);
+      const int y3 = __shfl_up_sync(0xffffffffu, wi.w, o);
+      if (lane >= o) {
+        wi.x += y0;
+        wi.y += y1;
+        wi.z += y2;
+        wi.w += y3;
+      }
     }
-    smem32[lane] = wi - w;  // exclusive warp offsets
-    if (lane == 31) smem32[32] = wi;
+    smem33[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);  // exclusive
+    if (lane == 31) smem33[32] = wi;
   }
   __syncthreads();
-  const int res = smem32[warp] + incl - x;
-  *total = smem32[32];
+  const int4 wo = smem33[warp];
+  const int4 res = make_int4(wo.x + incl.x - x.x, wo.y + incl.y - x.y, wo.z + incl.z - x.z,
+                             wo.w + incl.w - x.w);
+  *total = smem33[32];
   __syncthreads();
   return res;
 }
@@ -104,14 +123,17 @@ __device__ ReqInfo classify(const AttnArgs& a, int r) {
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspace ws,
                                                             int dec_grid) {
-  __shared__ int smem32[33];
+  __shared__ int4 smem33[33];
   __shared__ long long red[32];
   const int tid = threadIdx.x;
 
-  // pass 1: total decode keys, to size the split-KV chunk
+  // pass 1: total decode keys, to size the split-KV chunk (a thread keeps its
+  // first request's classification for pass 2)
   long long dec_keys = 0;
+  ReqInfo first{0, 0, 0, 0, 0};
   for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
     ReqInfo ri = classify(a, r);
+    if (r == tid) first = ri;
     if (ri.kind == 1) dec_keys += ri.L;
   }
 #pragma unroll
@@ -149,7 +171,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
-    if (r < a.num_reqs) ri = classify(a, r);
+    if (r < a.num_reqs) ri = base == 0 ? first : classify(a, r);
     if (ri.bad && blockIdx.x == 0) atomicOr(ws.err, ri.bad);
     int units = 0, parts = 0, tiles = 0, pairs = 0;
     if (ri.kind == 1) {
@@ -161,11 +183,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     } else if (ri.kind == 2) {
       tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
     }
-    int tot_u, tot_p, tot_t, tot_q;
-    const int off_u = block_exclusive_scan(units, &tot_u, smem32);
-    const int off_p = block_exclusive_scan(parts, &tot_p, smem32);
-    const int off_t = block_exclusive_scan(tiles, &tot_t, smem32);
-    const int off_q = block_exclusive_scan(pairs, &tot_q, smem32);
+    int4 tot;
+    const int4 off = block_exclusive_scan4(make_int4(units, parts, tiles, pairs), &tot, smem33);
+    const int off_u = off.x, off_p = off.y, off_t = off.z, off_q = off.w;
+    const int tot_u = tot.x, tot_p = tot.y, tot_t = tot.z, tot_q = tot.w;
     s_off_u[tid] = off_u;
     s_off_t[tid] = off_t;
     s_off_q[tid] = off_q;
