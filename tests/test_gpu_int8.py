@@ -73,7 +73,8 @@ def test_int8_write_codes_clamp_and_nan():
 
 
 @pytest.mark.parametrize("hq,hkv,qn", [(8, 8, 1), (32, 8, 1), (32, 1, 1), (64, 2, 1),
-                                       (8, 8, 4), (16, 4, 2), (12, 4, 5)])
+                                       (48, 2, 1), (20, 1, 1), (8, 8, 4), (16, 4, 2),
+                                       (12, 4, 5), (8, 1, 2)])
 def test_int8_decode(hq, hkv, qn):
     ctx = [0, 1, 15, 16, 63, 200, 1023, 2100, 5000]
     step = W.build(W.custom(ctx, [qn] * len(ctx), hq, hkv, seed=hq * 7 + hkv + qn))
@@ -103,3 +104,11 @@ def test_int8_mha_decode_subset_full_lengths():
     step = W.build(W.subset(W.spec("mha_decode"), 24))
     ds, got, ref = run_int8(step, "int8 mha_decode subset")
     _check_all(step, got, ref, "int8 mha_decode subset")
+
+
+@pytest.mark.parametrize("name", ["mha_decode", "gqa_decode", "mqa_long_decode"])
+def test_int8_decode_full_size(name):
+    """The bench's decode workloads at full size, every output row checked."""
+    step = W.build(W.spec(name))
+    ds, got, ref = run_int8(step, "int8 " + name)
+    _check_all(step, got, ref, "int8 " + name)
