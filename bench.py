@@ -73,6 +73,17 @@ def decode_algorithmic_bytes(spec, kv_elem_bytes=2):
     return b
 
 
+def step_bytes(spec, kv_elem_bytes=2):
+    """Algorithmic bytes of a whole step (write + attention): every request's
+    K and V rows once per KV head, the query rows read and output rows
+    written, and the write's new K/V rows read (bf16) and stored."""
+    d = spec.head_size
+    kv = sum(c + n for c, n in zip(spec.ctx, spec.q_len)) * spec.hkv * d * kv_elem_bytes * 2
+    qo = 2 * spec.num_tokens * spec.hq * d * 2
+    wr = spec.num_tokens * spec.hkv * d * 2 * (2 + kv_elem_bytes)
+    return kv + qo + wr
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -434,6 +445,15 @@ def main():
     roof["avg_launch_ms"] = avg_ms
     traffic = profiled_traffic(dominant, spec.name + ("_int8" if int8 else ""), srcs)
     roof["traffic"] = traffic
+    # the whole step against its own floor: max(bytes / copy bandwidth,
+    # flops / bf16 peak), both algorithmic
+    sb, sf = step_bytes(spec, 1 if int8 else 2), causal_flops(spec)
+    bw = peaks.get("hbm_gbs") or 6800.0
+    tf = peaks.get("bf16_tflops") or 1900.0
+    floor_ms = max(sb / (bw * 1e9), sf / (tf * 1e12)) * 1e3
+    step_roof = {"bytes": sb, "flops": sf, "floor_ms": floor_ms,
+                 "bound": "hbm" if sb / (bw * 1e9) >= sf / (tf * 1e12) else "tensor",
+                 "frac": floor_ms / ms_per_step}
 
     rec = {"metric": name, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -450,7 +470,7 @@ def main():
                       "parallelism": "replica per GPU (dp%d)" % world},
            "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
-           "roofline": roof}
+           "roofline": roof, "step_roofline": step_roof}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not int8:
         rec["cpu_baseline"] = cpu_baseline_bounded(step)
     if rank == 0:

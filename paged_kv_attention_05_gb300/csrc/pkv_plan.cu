@@ -6,12 +6,14 @@
 // metadata (no device-to-host copy, so a step can be captured in a CUDA
 // graph): one small kernel reads query_start_loc and seq_lens on the device,
 // checks them, and writes
-//   * decode units (request, KV head, key range) for requests with one query
-//     token, split along the keys so that the persistent decode grid has
-//     several units per CTA (split-KV; the split results are merged by the
-//     last unit of each (request, KV head) to finish);
-//   * prefill entries (request, 128-row query tile) for requests with more
-//     than one query token, ordered longest first;
+//   * decode units (request, KV head, key range) for requests whose query
+//     tokens x heads of a KV head fit one decode unit's rows (single-token
+//     and short multi-token steps), split along the keys so that the
+//     persistent decode grid has several units per worker (split-KV);
+//   * split pairs: the (request, KV head) pairs whose splits the combine
+//     kernel merges afterwards;
+//   * prefill entries (request, 128-row query tile) for longer requests,
+//     ordered longest first;
 //   * a header with the counts, the split size and zeroed scheduler cursors.
 // The kernel runs a few CTAs: each one reads the whole metadata and forms
 // every offset (the scans are cheap and the same in every CTA), then writes
