@@ -459,13 +459,8 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
 template <int MT>
 cudaError_t launch_i8(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   using C = Cfg8<MT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_i8_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<bool> attr[kMaxAttrDevices];
+  if (cudaError_t e = smem_attr_once(decode_i8_kernel<MT>, C::kSmem, attr)) return e;
   const int G = a.hq / a.hkv;
   CUtensorMap tq, tk, tv;
   if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) ||

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -86,6 +88,22 @@ struct Sizes {
 Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv);
 size_t workspace_bytes(const Sizes& z);
 Workspace carve_workspace(void* base, const Sizes& z, int* err);
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (each device holds its own copy of the kernel and
+// of the attribute); `done` is the kernel's own flag array.
+constexpr int kMaxAttrDevices = 64;
+template <typename Kernel>
+cudaError_t smem_attr_once(Kernel* kernel, int bytes, std::atomic<bool>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,

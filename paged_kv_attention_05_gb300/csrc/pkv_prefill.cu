@@ -728,13 +728,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<bool> attr[kMaxAttrDevices];
+  if (cudaError_t e = smem_attr_once(prefill_kernel, kSmemBytes, attr)) return e;
   CUtensorMap tq, tk, tv;
   if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, 1, kPreTileQ) ||
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
