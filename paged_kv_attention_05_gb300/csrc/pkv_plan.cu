@@ -129,27 +129,53 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   __shared__ long long red[32];
   const int tid = threadIdx.x;
 
-  // pass 1: total decode keys, to size the split-KV chunk (a thread keeps its
-  // first request's classification for pass 2)
+  // pass 1: total decode keys, decode requests and their longest length, to
+  // size the split-KV chunk (a thread keeps its first request's
+  // classification for pass 2)
   long long dec_keys = 0;
+  int dec_reqs = 0, dec_lmax = 0;
   ReqInfo first{0, 0, 0, 0, 0};
   for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
     ReqInfo ri = classify(a, r);
     if (r == tid) first = ri;
-    if (ri.kind == 1) dec_keys += ri.L;
+    if (ri.kind == 1) {
+      dec_keys += ri.L;
+      dec_reqs += 1;
+      dec_lmax = max(dec_lmax, ri.L);
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
-  if ((tid & 31) == 0) red[tid >> 5] = dec_keys;
+  for (int o = 16; o > 0; o >>= 1) {
+    dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
+    dec_reqs += __shfl_xor_sync(0xffffffffu, dec_reqs, o);
+    dec_lmax = max(dec_lmax, __shfl_xor_sync(0xffffffffu, dec_lmax, o));
+  }
+  __shared__ int red_n[32], red_l[32];
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = dec_keys;
+    red_n[tid >> 5] = dec_reqs;
+    red_l[tid >> 5] = dec_lmax;
+  }
   __syncthreads();
   if (tid < 32) {
     long long x = red[tid];
+    int n = red_n[tid], l = red_l[tid];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (tid == 0) red[0] = x;
+    for (int o = 16; o > 0; o >>= 1) {
+      x += __shfl_xor_sync(0xffffffffu, x, o);
+      n += __shfl_xor_sync(0xffffffffu, n, o);
+      l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+    }
+    if (tid == 0) {
+      red[0] = x;
+      red_n[0] = n;
+      red_l[0] = l;
+    }
   }
   __syncthreads();
   const long long total_keys = red[0];
+  const long long dec_pairs = (long long)red_n[0] * a.hkv;  // (request, KV head) pairs
+  const int lmax = red_l[0];
   // aim for about four units per decode worker (dec_grid = workers), in
   // whole 64-key tiles, at most kMaxChunk keys; at least kMinChunk keys, and
   // at least 32 keys per query head of the group, so that a split's partial
@@ -158,7 +184,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   want = (want + kDecTile - 1) / kDecTile * kDecTile;
   const int G = a.hq / a.hkv;
   const int lo_chunk = max(kMinChunk, 32 * G);
-  const int chunk = (int)(want < lo_chunk ? lo_chunk : (want > kMaxChunk ? kMaxChunk : want));
+  int chunk = (int)(want < lo_chunk ? lo_chunk : (want > kMaxChunk ? kMaxChunk : want));
+  // When even the longest request's splits, times the pairs, fit one wave of
+  // workers, the step takes one unit's time: give every pair as many splits
+  // as the wave has room for (units of at most that many keys, kMinChunk at
+  // least), so that the wave is full and each unit short.
+  if (dec_pairs > 0 && dec_pairs * ((lmax + chunk - 1) / chunk) <= dec_grid) {
+    const long long per_pair = dec_grid / dec_pairs;
+    long long c = (lmax + per_pair - 1) / per_pair;
+    c = (c + kDecTile - 1) / kDecTile * kDecTile;
+    if (c < kMinChunk) c = kMinChunk;
+    if (c < chunk) chunk = (int)c;
+  }
 
   // pass 2: per-request offsets (block scans), then the work lists written
   // cooperatively: consecutive threads write consecutive entries, each
