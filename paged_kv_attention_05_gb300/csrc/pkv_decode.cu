@@ -46,15 +46,15 @@ namespace {
 
 using namespace dev;
 
-constexpr int kWarps = 8;
 constexpr int kCombineThreads = 128;  // merge kernel: 4 warps, one split pair row each
-constexpr int kThreads = kWarps * 32;
 constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2 KB)
 constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
 constexpr int kIdRegs = kMaxChunk / kBlockSize / 32;  // block ids per lane per unit
 
 template <int MT>
 struct Cfg {
+  static constexpr int kWarps = 8;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kStages = MT == 1 ? 3 : 2;
   static constexpr int kStageBytes = kPage;
   static constexpr int kQHalf = MT * 16 * 128;        // query rows x one 64-dim half
@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok_lo, int valid)
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   using C = Cfg<MT>;
@@ -462,14 +462,15 @@ cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  decode_kernel<MT><<<sms, kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
+  decode_kernel<MT><<<sms, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 int decode_workers(int group, int kv_int8, int sms) {
-  return sms * (kv_int8 ? decode_i8_warps(group) : kWarps);
+  return sms * (kv_int8 ? decode_i8_warps(group)
+                        : (group <= 16 ? Cfg<1>::kWarps : Cfg<2>::kWarps));
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
