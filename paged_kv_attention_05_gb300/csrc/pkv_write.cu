@@ -7,11 +7,12 @@
 // rows carry PAD_SLOT_ID = -1.
 //
 // GB300 layout of the work: the copy is pure HBM traffic (read 2 rows, write
-// 2 rows per token), so each thread moves 16-byte vectors and consecutive
-// threads move consecutive 16-byte pieces of one token's contiguous
-// [num_kv_heads * 128] row: every warp issues fully coalesced 512-byte
-// transactions on both sides.  The grid is a multiple of the SM count and
-// strides over (token, K/V, 16-byte piece).
+// 2 rows per token), so a warp moves one 2 KB piece of a token's contiguous
+// [num_kv_heads * 128] K row and the same piece of its V row: the slot is
+// read once, the lanes take consecutive 16-byte vectors, four of each row per
+// lane, all loads issued before the stores (fully coalesced 512-byte
+// transactions, and enough bytes in flight per SM to cover HBM latency).  The
+// grid is a multiple of the SM count and strides over (token, piece).
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -25,25 +26,46 @@ __global__ void __launch_bounds__(256) write_kernel(const uint16_t* __restrict__
                                                     int row_vecs, const int64_t* __restrict__ slots,
                                                     int64_t n_tokens, int* err) {
   // row_vecs = 16-byte vectors per token row = num_kv_heads * 128 * 2 / 16
-  const int64_t per_token = 2 * (int64_t)row_vecs;
-  const int64_t total = n_tokens * per_token;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / per_token;
-    const int rem = (int)(i - t * per_token);
-    const bool is_v = rem >= row_vecs;
-    const int vec = is_v ? rem - row_vecs : rem;
+  constexpr int kUnroll = 4;
+  constexpr int kPiece = 32 * kUnroll;  // vectors of a row one warp moves
+  const int pieces = (row_vecs + kPiece - 1) / kPiece;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t units = n_tokens * pieces;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < units;
+       w += nwarps) {
+    const int64_t t = w / pieces;
+    const int base = (int)(w - t * pieces) * kPiece;
     const int64_t slot = __ldg(slots + t);
     if (slot < 0) continue;  // padding token
     if (slot >= num_slots) {
-      if (rem == 0) atomicOr(err, PKV_DEV_ERR_SLOT_RANGE);
+      if (lane == 0 && base == 0) atomicOr(err, PKV_DEV_ERR_SLOT_RANGE);
       continue;
     }
     // cache row of this slot: [block][offset] == slot * row (contiguous pool)
-    const uint16_t* src = (is_v ? v + t * v_stride : k + t * k_stride) + (int64_t)vec * 8;
-    uint16_t* dst = (is_v ? vc : kc) + slot * (int64_t)row_vecs * 8 + (int64_t)vec * 8;
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
-    *reinterpret_cast<uint4*>(dst) = val;
+    const uint4* ks = reinterpret_cast<const uint4*>(k + t * k_stride);
+    const uint4* vs = reinterpret_cast<const uint4*>(v + t * v_stride);
+    uint4* kd = reinterpret_cast<uint4*>(kc + slot * (int64_t)row_vecs * 8);
+    uint4* vd = reinterpret_cast<uint4*>(vc + slot * (int64_t)row_vecs * 8);
+    {
+      uint4 kv[kUnroll], vv[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int e = base + u * 32 + lane;
+        if (e < row_vecs) {
+          kv[u] = __ldg(ks + e);
+          vv[u] = __ldg(vs + e);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int e = base + u * 32 + lane;
+        if (e < row_vecs) {
+          kd[e] = kv[u];
+          vd[e] = vv[u];
+        }
+      }
+    }
   }
 }
 
@@ -118,9 +140,9 @@ cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,
                          const int64_t* slots, int64_t n_tokens, int* err, int sms,
                          cudaStream_t st) {
   const int row_vecs = hkv * kHeadSize * 2 / 16;
-  const int64_t total = n_tokens * 2 * (int64_t)row_vecs;
   const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t units = n_tokens * ((row_vecs + 127) / 128);  // a warp per 128-vector piece
+  int64_t blocks = (units + threads / 32 - 1) / (threads / 32);
   const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread CTAs per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
