@@ -362,9 +362,10 @@ int run_locked(DeviceState* s, const void* q, int64_t q_row_stride, const void* 
   a.v_scale = kv_int8 ? v_scale : 1.f;
   cudaError_t e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if (!kv_int8) {  // an int8 call has no prefill work (the plan reports such requests)
+  if (kv_int8) {  // an int8 call has no prefill work (the plan reports such requests)
+    e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  } else {  // the prefill kernel merges the split results first
     e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }

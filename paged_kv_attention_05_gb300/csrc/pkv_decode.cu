@@ -35,10 +35,12 @@
 //     the fragments, so stale or NaN cache slots never reach the product.
 //   * A unit that covers a whole request writes the bf16 output; one split of
 //     several writes (max, sum, unnormalised output) in fp32 to the workspace,
-//     and the combine kernel merges the splits afterwards.  Every mbarrier wait
-//     is bounded.
+//     and the merge of the splits (pkv_combine.cuh) runs afterwards: first
+//     thing in the prefill kernel's launch for bf16 calls, in the combine
+//     kernel below for int8 calls.  Every mbarrier wait is bounded.
 // The int8-cache variant of the decode kernel is in pkv_decode_i8.cu; it
-// shares the plan, the work units and the combine kernel below.
+// shares the plan, the work units and the merge.
+#include "pkv_combine.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -404,51 +406,9 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   }
 }
 
-// Merge of split results: one (split pair, query row) per warp, four output
-// columns per lane, the splits merged in one pass with the online-softmax
-// identity the decode loop uses between pages (a running max M; the sum and
-// the output so far are scaled by exp2(M_old - M_new) when it grows).  A
-// split that saw no key of the row (m = -inf: only later splits of a
-// multi-token row) contributes nothing; the first split always holds key 0.
-// Rows are (query token, head in group); pairs with fewer rows than the
-// largest skip the rest.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {
-  const int G = a.hq / a.hkv;
-  const int max_rows = ws.hdr->max_rows;
-  const int n_items = ws.hdr->n_pairs * max_rows;
-  const int lane = threadIdx.x & 31;
   constexpr int kWarpsPerBlock = kCombineThreads / 32;
-  for (int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
-       item += gridDim.x * kWarpsPerBlock) {
-    const SplitPair sp = ws.pairs[item / max_rows];
-    const int row = item % max_rows;
-    const int q0 = sp.q0;
-    const int rows = sp.qn * G;
-    if (row >= rows) continue;
-    const float* ml = ws.part_ml + ((int64_t)sp.first + row) * 2;
-    const float* po = ws.part_o + ((int64_t)sp.first + row) * kHeadSize + 4 * lane;
-    float M = -INFINITY, lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s = 0; s < sp.nsplit; ++s) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + (int64_t)s * rows * 2));
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(po + (int64_t)s * rows * kHeadSize));
-      const float Mn = fmaxf(M, v.x);
-      const float fo = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
-      const float fn = v.x == -INFINITY ? 0.f : fast_exp2(v.x - Mn);
-      lsum = lsum * fo + v.y * fn;
-      acc.x = acc.x * fo + o.x * fn;
-      acc.y = acc.y * fo + o.y * fn;
-      acc.z = acc.z * fo + o.z * fn;
-      acc.w = acc.w * fo + o.w * fn;
-      M = Mn;
-    }
-    const float inv = 1.f / lsum;
-    uint16_t* orow = a.out + (int64_t)(q0 + row / G) * a.out_stride +
-                     (int64_t)(sp.g * G + row % G) * kHeadSize + 4 * lane;
-    *reinterpret_cast<uint2*>(orow) =
-        make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
-  }
+  combine_splits(a, ws, blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), gridDim.x * kWarpsPerBlock);
 }
 
 template <int MT>

@@ -5,7 +5,7 @@
 // K_j = k_scale * code and V_j = v_scale * code, the int8 KV cache that the
 // closing note of the deep dive's paged_attention section names as a decode
 // speed-up.  Work units, split-KV partial results and the merge are those of
-// the bf16 path (same plan, same combine kernel).
+// the bf16 path (same plan, same merge of the splits).
 //
 // GB300 design.  A page of one KV head is 4 KB of codes (16 slots x 128 for K,
 // the same for V), loaded by TMA into a per-warp ring of 3 pages (one 2 KB box

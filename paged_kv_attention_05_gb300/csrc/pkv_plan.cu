@@ -10,8 +10,8 @@
 //     tokens x heads of a KV head fit one decode unit's rows (single-token
 //     and short multi-token steps), split along the keys so that the
 //     persistent decode grid has several units per worker (split-KV);
-//   * split pairs: the (request, KV head) pairs whose splits the combine
-//     kernel merges afterwards;
+//   * split pairs: the (request, KV head) pairs whose splits are merged
+//     afterwards (pkv_combine.cuh);
 //   * prefill entries (request, 128-row query tile) for longer requests,
 //     ordered longest first;
 //   * a header with the counts, the split size and zeroed scheduler cursors.

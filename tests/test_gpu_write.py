@@ -18,7 +18,7 @@ def _expected_caches(step):
     return kc, vc
 
 
-@pytest.mark.parametrize("name", ["tiny_mixed", "mixed_chunked", "gqa_decode"])
+@pytest.mark.parametrize("name", ["tiny_mixed", "mixed_chunked", "gqa_decode", "large_prefill"])
 def test_write_bit_exact_whole_cache(name):
     step = W.build(W.spec(name))
     ek, ev = _expected_caches(step)
@@ -29,8 +29,10 @@ def test_write_bit_exact_whole_cache(name):
     assert torch.equal(ds.value_cache.view(torch.int16), to_dev(ev).view(torch.int16))
 
 
-@pytest.mark.parametrize("hkv", [1, 2, 8, 32])
+@pytest.mark.parametrize("hkv", [1, 2, 5, 8, 32, 48])
 def test_write_small_ragged_with_pads(hkv):
+    """Rows of 1 to 48 KV heads: a part of a warp's 2 KB piece, one piece,
+    several, and a last piece partly filled."""
     spec = W.custom([3, 17, 0], [5, 1, 33], 2 * hkv, hkv, seed=100 + hkv, pad_tokens=7)
     step = W.build(spec)
     ek, ev = _expected_caches(step)
