@@ -197,25 +197,64 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     if (c < chunk) chunk = (int)c;
   }
 
+  // Units are listed roughly longest first, in five classes: every request's
+  // full chunks, then the last (shorter) pieces by length quarter, longest
+  // quarter first, so that the tail of the dynamic schedule is made of short
+  // units.  cls_total[c] = units of class c over all requests.
+  auto last_class = [&](int L) {  // 1..4: quarter of the chunk the last piece fills
+    const int rem = L % chunk;
+    return rem == 0 ? 0 : 4 - min(3, (rem - 1) * 4 / chunk);
+  };
+  int4 cnt_a = make_int4(0, 0, 0, 0);  // full, last quarters 4/4, 3/4, 2/4
+  int cnt_b = 0;                       // last quarter 1/4
+  for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
+    const ReqInfo ri = r == tid ? first : classify(a, r);
+    if (ri.kind != 1) continue;
+    cnt_a.x += (ri.L / chunk) * a.hkv;
+    const int c = last_class(ri.L);
+    if (c == 1) cnt_a.y += a.hkv;
+    if (c == 2) cnt_a.z += a.hkv;
+    if (c == 3) cnt_a.w += a.hkv;
+    if (c == 4) cnt_b += a.hkv;
+  }
+  int4 cls_a;
+  int cls_b;
+  {
+    int4 t4;
+    block_exclusive_scan4(cnt_a, &t4, smem33);
+    int4 t5;
+    block_exclusive_scan4(make_int4(cnt_b, 0, 0, 0), &t5, smem33);
+    cls_a = t4;
+    cls_b = t5.x;
+  }
+  // first index of each class in the unit list
+  const int cls_base[5] = {0, cls_a.x, cls_a.x + cls_a.y, cls_a.x + cls_a.y + cls_a.z,
+                           cls_a.x + cls_a.y + cls_a.z + cls_a.w};
+  (void)cls_b;
+
   // pass 2: per-request offsets (block scans), then the work lists written
   // cooperatively: consecutive threads write consecutive entries, each
   // finding its request by binary search over the chunk's offsets
   __shared__ int s_off_u[kPlanThreads + 1], s_off_t[kPlanThreads + 1], s_off_q[kPlanThreads + 1];
+  __shared__ int s_off_f[kPlanThreads], s_off_l[kPlanThreads];  // full chunks, last piece
   __shared__ int s_off_p[kPlanThreads], s_len[kPlanThreads], s_n[kPlanThreads];
   __shared__ int s_q0[kPlanThreads];
   __shared__ int s_max_rows;
   if (tid == 0) s_max_rows = 0;
   __syncthreads();
   int unit_carry = 0, part_carry = 0, pre_carry = 0, pair_carry = 0;
+  int cls_carry[5] = {0, 0, 0, 0, 0};
   for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
     if (r < a.num_reqs) ri = base == 0 ? first : classify(a, r);
     if (ri.bad && blockIdx.x == 0) atomicOr(ws.err, ri.bad);
-    int units = 0, parts = 0, tiles = 0, pairs = 0;
+    int units = 0, parts = 0, tiles = 0, pairs = 0, fulls = 0, lcls = 0;
     if (ri.kind == 1) {
       const int nsplit = (ri.L + chunk - 1) / chunk;
       units = nsplit * a.hkv;
+      fulls = (ri.L / chunk) * a.hkv;
+      lcls = last_class(ri.L);
       parts = nsplit > 1 ? units * ri.n * G : 0;  // partial rows
       pairs = nsplit > 1 ? a.hkv : 0;
       if (nsplit > 1) atomicMax(&s_max_rows, ri.n * G);
@@ -226,6 +265,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     const int4 off = block_exclusive_scan4(make_int4(units, parts, tiles, pairs), &tot, smem33);
     const int off_u = off.x, off_p = off.y, off_t = off.z, off_q = off.w;
     const int tot_u = tot.x, tot_p = tot.y, tot_t = tot.z, tot_q = tot.w;
+    // offsets inside the classes: full chunks, and the last piece's quarter
+    const int lu = units - fulls;  // a.hkv or 0
+    int4 tot2, tot3;
+    const int4 off2 = block_exclusive_scan4(
+        make_int4(fulls, lcls == 1 ? lu : 0, lcls == 2 ? lu : 0, lcls == 3 ? lu : 0), &tot2, smem33);
+    const int4 off3 = block_exclusive_scan4(make_int4(lcls == 4 ? lu : 0, 0, 0, 0), &tot3, smem33);
+    s_off_f[tid] = cls_base[0] + cls_carry[0] + off2.x;
+    {
+      const int ofs = lcls == 1 ? off2.y : (lcls == 2 ? off2.z : (lcls == 3 ? off2.w : off3.x));
+      s_off_l[tid] = lcls == 0 ? 0 : cls_base[lcls] + cls_carry[lcls] + ofs;
+    }
     s_off_u[tid] = off_u;
     s_off_t[tid] = off_t;
     s_off_q[tid] = off_q;
@@ -248,10 +298,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       const int cnt_u = s_off_u[lo + 1] - s_off_u[lo];
       if (cnt_u == 0) continue;
       const int L = s_len[lo], qn = s_n[lo];
-      const int nsplit = (L + chunk - 1) / chunk;
+      const int nsplit = (L + chunk - 1) / chunk, nfull = L / chunk;
       for (int rem = ln; rem < cnt_u; rem += 32) {
         const int sp = rem / a.hkv, g = rem - sp * a.hkv;
-        const int64_t idx = (int64_t)unit_carry + s_off_u[lo] + rem;
+        const int64_t idx = sp < nfull ? (int64_t)s_off_f[lo] + rem : (int64_t)s_off_l[lo] + g;
         if (idx >= ws.max_units) break;
         // two 16-byte stores per unit
         int4* dst = reinterpret_cast<int4*>(ws.units + idx);
@@ -282,6 +332,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       dst[1] = make_int4(n, s_len[lo], 0, 0);
     }
     unit_carry += tot_u;
+    cls_carry[0] += tot2.x;
+    cls_carry[1] += tot2.y;
+    cls_carry[2] += tot2.z;
+    cls_carry[3] += tot2.w;
+    cls_carry[4] += tot3.x;
     part_carry += tot_p;
     pre_carry += tot_t;
     pair_carry += tot_q;

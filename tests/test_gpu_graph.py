@@ -4,6 +4,8 @@ host synchronisation, so the layers of a step ("Tour: One forward pass",
 stop 7: the 32-layer loop; stop 5: one attention metadata object shared by
 all layers) can be captured and replayed.  Replays must reproduce the eager
 results exactly (same kernels, same inputs)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -62,22 +64,50 @@ def test_capture_layers_in_a_cuda_graph_and_replay():
         assert_close(ds.out_f64()[:n], ref[:n], "graph layer %d" % l)
 
 
+_REFUSAL_SCRIPT = r"""
+import sys
+sys.path[:0] = [sys.argv[1], sys.argv[2]]
+import torch
+import paged_kv_attention_05_gb300 as pkv
+from paged_kv_attention_05_gb300 import workloads as W
+from gpu_util import DeviceStep
+spec = W.custom([5000], [1], 32, 1, seed=616)   # MQA, long: a big partial buffer
+ds = DeviceStep(W.build(spec))
+ds.write()
+ds.attention()   # eager first: the device state and a small workspace exist
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+stream = torch.cuda.Stream()
+big = 4096   # far more requests than this process reserved for
+qsl = torch.zeros(big + 1, dtype=torch.int32, device="cuda")
+sl = torch.zeros(big, dtype=torch.int32, device="cuda")
+# the widest block table: 4096 x 2048 split units alone need 256 MiB
+bt = torch.zeros((big, 32768), dtype=torch.int32, device="cuda")
+torch.cuda.synchronize()
+try:
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            pkv.pkv_attention(ds.q, ds.key_cache, ds.value_cache, qsl, sl, bt, big,
+                              ds.step.scale, ds.out, stream=stream)
+except pkv.PkvError as e:
+    torch.cuda.synchronize()
+    print("refused:", e)
+    sys.exit(0)
+print("not refused")
+sys.exit(1)
+"""
+
+
 def test_capture_without_reserved_workspace_is_refused_cleanly():
     """A capture that would need a larger workspace fails on the host with an
-    error (no allocation inside capture), not with a broken graph."""
-    spec = W.custom([5000], [1], 32, 1, seed=616)   # MQA, long: a big partial buffer
-    ds = DeviceStep(W.build(spec))
-    g = torch.cuda.CUDAGraph()
-    stream = torch.cuda.Stream()
-    big = 4096   # far more requests than any earlier call reserved for
-    qsl = torch.zeros(big + 1, dtype=torch.int32, device="cuda")
-    sl = torch.zeros(big, dtype=torch.int32, device="cuda")
-    # the widest block table: 4096 x 2048 split units alone need 256 MiB
-    bt = torch.zeros((big, 32768), dtype=torch.int32, device="cuda")
-    torch.cuda.synchronize()
-    with pytest.raises(pkv.PkvError):
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                pkv.pkv_attention(ds.q, ds.key_cache, ds.value_cache, qsl, sl, bt, big,
-                                  ds.step.scale, ds.out, stream=stream)
-    torch.cuda.synchronize()
+    error (no allocation inside capture), not with a broken graph.  Run in a
+    fresh process: the workspace only grows, so an earlier test's reservation
+    in this process could already cover the request."""
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    r = subprocess.run([sys.executable, "-c", _REFUSAL_SCRIPT, root, here],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "refused:" in r.stdout
