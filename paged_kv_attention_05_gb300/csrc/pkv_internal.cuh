@@ -15,7 +15,7 @@ namespace pkv {
 constexpr int kHeadSize = 128;   // elements per head row
 constexpr int kBlockSize = 16;   // tokens per cache block (page)
 constexpr int kMaxGroup = 32;    // query heads per KV head handled by one decode unit
-constexpr int kDecTile = 64;     // tokens per decode pipeline stage (4 pages)
+constexpr int kDecTile = 64;     // split-KV chunks are whole multiples of this many keys
 constexpr int kMinChunk = 256;   // smallest split-KV chunk (tokens)
 constexpr int kMaxChunk = 2048;  // largest split-KV chunk (tokens)
 constexpr int kMaxBtWidth = 32768;  // block-table entries per request (524,288 keys) at most
