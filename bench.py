@@ -352,10 +352,11 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
+    # The timed region: K steps, no per-launch events (recording an event
+    # between two launches holds the next one back by a few microseconds,
+    # which lengthens short steps by up to a third).
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    pkv.pkv_trace_read()
-    pkv.pkv_trace_enable(True)
     launches0 = pkv.pkv_launch_count()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -366,6 +367,14 @@ def main():
     e1.record(stream)
     barrier()
     launches = pkv.pkv_launch_count() - launches0
+    # The per-kernel durations behind the roofline: the same K steps again,
+    # with CUDA events recorded around each launch on its stream.
+    pkv.pkv_trace_read()
+    pkv.pkv_trace_enable(True)
+    barrier()
+    for _ in range(args.steps):
+        one_step()
+    barrier()
     pkv.pkv_trace_enable(False)
     trace = pkv.pkv_trace_read()
     clk = clocks.stop()
@@ -521,6 +530,8 @@ def main():
                       "parallelism": "replica per GPU (dp%d)" % world},
            "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
+           "kernel_timing": "CUDA events around each launch, in a second pass of the same K "
+                            "steps right after the timed one (which records none)",
            "roofline": roof, "step_roofline": step_roof}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not int8:
         rec["cpu_baseline"] = cpu_baseline_bounded(step)
