@@ -198,39 +198,45 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   }
 
   // Units are listed roughly longest first, in five classes: every request's
-  // full chunks, then the last (shorter) pieces by length quarter, longest
-  // quarter first, so that the tail of the dynamic schedule is made of short
-  // units.  cls_total[c] = units of class c over all requests.
-  auto last_class = [&](int L) {  // 1..4: quarter of the chunk the last piece fills
+  // full chunks, then the last (shorter) pieces by the quarter of a chunk
+  // they fill, longest first, so that the tail of the dynamic schedule is
+  // made of short units.  cls_base[c] = first unit of class c.
+  auto last_class = [&](int L) {  // 0: no last piece; 1..4 longest to shortest
     const int rem = L % chunk;
     return rem == 0 ? 0 : 4 - min(3, (rem - 1) * 4 / chunk);
   };
-  int4 cnt_a = make_int4(0, 0, 0, 0);  // full, last quarters 4/4, 3/4, 2/4
-  int cnt_b = 0;                       // last quarter 1/4
+  int4 cnt = make_int4(0, 0, 0, 0);  // units of classes 0..3 of this thread's requests
+                                     // (class 4 comes last: its count is not needed)
   for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
     const ReqInfo ri = r == tid ? first : classify(a, r);
     if (ri.kind != 1) continue;
-    cnt_a.x += (ri.L / chunk) * a.hkv;
+    cnt.x += (ri.L / chunk) * a.hkv;
     const int c = last_class(ri.L);
-    if (c == 1) cnt_a.y += a.hkv;
-    if (c == 2) cnt_a.z += a.hkv;
-    if (c == 3) cnt_a.w += a.hkv;
-    if (c == 4) cnt_b += a.hkv;
+    if (c == 1) cnt.y += a.hkv;
+    if (c == 2) cnt.z += a.hkv;
+    if (c == 3) cnt.w += a.hkv;
   }
-  int4 cls_a;
-  int cls_b;
-  {
-    int4 t4;
-    block_exclusive_scan4(cnt_a, &t4, smem33);
-    int4 t5;
-    block_exclusive_scan4(make_int4(cnt_b, 0, 0, 0), &t5, smem33);
-    cls_a = t4;
-    cls_b = t5.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt.x += __shfl_xor_sync(0xffffffffu, cnt.x, o);
+    cnt.y += __shfl_xor_sync(0xffffffffu, cnt.y, o);
+    cnt.z += __shfl_xor_sync(0xffffffffu, cnt.z, o);
+    cnt.w += __shfl_xor_sync(0xffffffffu, cnt.w, o);
   }
-  // first index of each class in the unit list
-  const int cls_base[5] = {0, cls_a.x, cls_a.x + cls_a.y, cls_a.x + cls_a.y + cls_a.z,
-                           cls_a.x + cls_a.y + cls_a.z + cls_a.w};
-  (void)cls_b;
+  if ((tid & 31) == 0) smem33[tid >> 5] = cnt;
+  __syncthreads();
+  int4 cls = make_int4(0, 0, 0, 0);
+#pragma unroll 4
+  for (int w = 0; w < kPlanThreads / 32; ++w) {  // (every thread, the same order)
+    const int4 v = smem33[w];
+    cls.x += v.x;
+    cls.y += v.y;
+    cls.z += v.z;
+    cls.w += v.w;
+  }
+  __syncthreads();  // smem33 is reused by the scans
+  const int cls_base[5] = {0, cls.x, cls.x + cls.y, cls.x + cls.y + cls.z,
+                           cls.x + cls.y + cls.z + cls.w};
 
   // pass 2: per-request offsets (block scans), then the work lists written
   // cooperatively: consecutive threads write consecutive entries, each
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     const int4 off = block_exclusive_scan4(make_int4(units, parts, tiles, pairs), &tot, smem33);
     const int off_u = off.x, off_p = off.y, off_t = off.z, off_q = off.w;
     const int tot_u = tot.x, tot_p = tot.y, tot_t = tot.z, tot_q = tot.w;
-    // offsets inside the classes: full chunks, and the last piece's quarter
+    // offsets inside the classes: full chunks, and the last piece's class
     const int lu = units - fulls;  // a.hkv or 0
     int4 tot2, tot3;
     const int4 off2 = block_exclusive_scan4(
