@@ -114,3 +114,12 @@ def test_shared_prefix_blocks():
     for r in range(1, 4):
         step.block_table[r, :shared] = step.block_table[0, :shared]
     run_and_check(step, "shared prefix")
+
+
+def test_decode_longest_request():
+    """A request at the longest supported length (a block-table row of 32,768
+    blocks, 524,288 keys: the most splits of one request, all merged) next to
+    a short one."""
+    ctx = [32768 * 16 - 1, 40]
+    step = W.build(W.custom(ctx, [1, 1], 8, 1, seed=71, num_blocks=32768 + 8, bt_width=32768))
+    run_and_check(step, "longest request decode")

@@ -151,3 +151,10 @@ def test_prefill_scores_growing_along_the_keys():
             else:
                 step.k[step.query_start_loc[r] + pos - ctx, :, :] = kv[None, :]
     run_and_check(step, "growing scores")
+
+
+def test_prefill_chunk_after_long_context():
+    """A 200-row chunk continuing a 32,768-token cached prompt: items of 258
+    key tiles, the steady state of the prefill kernel, next to a decode."""
+    step = W.build(W.custom([32768, 900], [200, 1], 8, 2, seed=73))
+    run_and_check(step, "prefill after a long context")
