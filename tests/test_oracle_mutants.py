@@ -37,6 +37,24 @@ MUTANTS = [
     ("write-v-from-k", "value_cache[dst] = v[", "value_cache[dst] = k[", None),
     ("write-head-stride", "int64_t dst = ((block * block_size + offset) * hkv + h) * d + e;",
      "int64_t dst = ((block * block_size + offset) * hkv) * d + e;", None),
+    ("query-row-ignores-request-start",
+     "const uint16_t *qrow = q + (q0 + i) * q_row_stride + (int64_t)h * d;",
+     "const uint16_t *qrow = q + i * q_row_stride + (int64_t)h * d;", None),
+    ("query-head-uses-kv-head",
+     "const uint16_t *qrow = q + (q0 + i) * q_row_stride + (int64_t)h * d;",
+     "const uint16_t *qrow = q + (q0 + i) * q_row_stride + (int64_t)g * d;", None),
+    ("key-head-zero", "int64_t krow = ((block * block_size + offset) * hkv + g) * d;",
+     "int64_t krow = ((block * block_size + offset) * hkv + 0) * d;", None),
+    ("key-offset-zero", "int64_t offset = j % block_size;", "int64_t offset = 0;", 0),
+    ("key-excludes-itself", "for (int64_t j = 0; j <= last; ++j) {",
+     "for (int64_t j = 0; j < last; ++j) {", 0),
+    ("output-row-ignores-request-start",
+     "double *orow = out + ((int64_t)query_start_loc[r] + i) * out_row_stride +",
+     "double *orow = out + (i) * out_row_stride +", None),
+    ("bt-width-check-strict", "if (nb > bt_width) return ORC_ERR_BT_WIDTH;",
+     "if (nb >= bt_width) return ORC_ERR_BT_WIDTH;", None),
+    ("block-id-check-dropped", "if (id < 0 || id >= num_blocks) return ORC_ERR_BLOCK_ID;", "",
+     None),
     ("int8-truncates", "float r = rintf(x / scale);", "float r = truncf(x / scale);", None),
     ("int8-rounds-half-up", "float r = rintf(x / scale);", "float r = floorf(x / scale + 0.5f);",
      None),
