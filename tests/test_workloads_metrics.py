@@ -86,3 +86,18 @@ def test_metric_units_and_floor(name):
         assert t_bytes > t_flops
     if name == "large_prefill":
         assert t_flops > t_bytes
+
+
+@pytest.mark.parametrize("name", W.CONFIG_NAMES)
+@pytest.mark.parametrize("elem", [2, 1])
+def test_timed_steps_read_from_hbm(name, elem):
+    # the timed loop rotates through enough copies of a step's inputs that the
+    # rotation is at least four L2s, so no step finds its K/V still in L2
+    b = _bench()
+    sb = b.step_bytes(W.spec(name), elem)
+    n = b.l2_copies(sb)
+    assert n * sb >= 4 * 129e6 and (n == 1 or (n - 1) * sb < 4 * 129e6)
+    if name in ("mha_decode", "gqa_decode", "large_prefill"):
+        assert n == 1
+    if name == "tiny_mixed":
+        assert n > 40
