@@ -19,21 +19,25 @@
 // every offset (the scans are cheap and the same in every CTA), then writes
 // its share of the entries — one request per warp of the grid — so that a
 // batch of hundreds of requests and tens of thousands of units is not
-// written by a single SM.
+// written by a single SM.  A CTA has as many threads as the batch has
+// requests (rounded up to a warp, at most 1024): the plan's cost is a chain
+// of block-wide barriers and scans, so a small batch plans with one warp.
 // "vLLM MHA Code Path: From QKV to Paged KV Cache", section "Prefill and
 // decode share an interface": the phase of a request is told apart only by
 // its query and sequence lengths, which is what this kernel does.
+#include <algorithm>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;  // the most threads of a plan CTA
 
-// Exclusive block-wide prefix sums of four ints per thread (1024 threads),
-// the four scans sharing their barriers.
+// Exclusive block-wide prefix sums of four ints per thread (any whole number
+// of warps up to 32), the four scans sharing their barriers.
 __device__ int4 block_exclusive_scan4(int4 x, int4* total, int4* smem33) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int4 incl = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -51,7 +55,7 @@ __device__ int4 block_exclusive_scan4(int4 x, int4* total, int4* smem33) {
   if (lane == 31) smem33[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int4 w = smem33[lane];
+    const int4 w = lane < nw ? smem33[lane] : make_int4(0, 0, 0, 0);
     int4 wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -78,10 +82,10 @@ __device__ int4 block_exclusive_scan4(int4 x, int4* total, int4* smem33) {
   return res;
 }
 
-// Last index i in [0, kPlanThreads) with off[i] <= x: the request that owns
-// entry x when off[] holds the exclusive prefix sums of per-request counts.
-__device__ __forceinline__ int find_owner(const int* off, int x) {
-  int lo = 0, hi = kPlanThreads - 1;
+// Last index i in [0, n) with off[i] <= x: the request that owns entry x
+// when off[] holds the exclusive prefix sums of per-request counts.
+__device__ __forceinline__ int find_owner(const int* off, int n, int x) {
+  int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (off[mid] <= x) lo = mid; else hi = mid - 1;
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
                                                             int dec_grid) {
   __shared__ int4 smem33[33];
   __shared__ long long red[32];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
 
   // pass 1: total decode keys, decode requests and their longest length, to
   // size the split-KV chunk (a thread keeps its first request's
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   long long dec_keys = 0;
   int dec_reqs = 0, dec_lmax = 0;
   ReqInfo first{0, 0, 0, 0, 0};
-  for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
+  for (int r = tid; r < a.num_reqs; r += nt) {
     ReqInfo ri = classify(a, r);
     if (r == tid) first = ri;
     if (ri.kind == 1) {
@@ -158,8 +162,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   }
   __syncthreads();
   if (tid < 32) {
-    long long x = red[tid];
-    int n = red_n[tid], l = red_l[tid];
+    long long x = tid < nw ? red[tid] : 0;
+    int n = tid < nw ? red_n[tid] : 0, l = tid < nw ? red_l[tid] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   };
   int4 cnt = make_int4(0, 0, 0, 0);  // units of classes 0..3 of this thread's requests
                                      // (class 4 comes last: its count is not needed)
-  for (int r = tid; r < a.num_reqs; r += kPlanThreads) {
+  for (int r = tid; r < a.num_reqs; r += nt) {
     const ReqInfo ri = r == tid ? first : classify(a, r);
     if (ri.kind != 1) continue;
     cnt.x += (ri.L / chunk) * a.hkv;
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   __syncthreads();
   int4 cls = make_int4(0, 0, 0, 0);
 #pragma unroll 4
-  for (int w = 0; w < kPlanThreads / 32; ++w) {  // (every thread, the same order)
+  for (int w = 0; w < nw; ++w) {  // (every thread, the same order)
     const int4 v = smem33[w];
     cls.x += v.x;
     cls.y += v.y;
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   __syncthreads();
   int unit_carry = 0, part_carry = 0, pre_carry = 0, pair_carry = 0;
   int cls_carry[5] = {0, 0, 0, 0, 0};
-  for (int base = 0; base < a.num_reqs; base += kPlanThreads) {
+  for (int base = 0; base < a.num_reqs; base += nt) {
     const int r = base + tid;
     ReqInfo ri{0, 0, 0, 0, 0};
     if (r < a.num_reqs) ri = base == 0 ? first : classify(a, r);
@@ -290,16 +294,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     s_n[tid] = ri.n;
     s_q0[tid] = ri.q0;
     if (tid == 0) {
-      s_off_u[kPlanThreads] = tot_u;
-      s_off_t[kPlanThreads] = tot_t;
-      s_off_q[kPlanThreads] = tot_q;
+      s_off_u[nt] = tot_u;
+      s_off_t[nt] = tot_t;
+      s_off_q[nt] = tot_q;
     }
     __syncthreads();
     // decode units and split pairs: one warp of the grid per request (a
     // request's entries are contiguous), lanes over its entries, so that
     // consecutive lanes write consecutive entries with no search for the owner
-    for (int lo = blockIdx.x * (kPlanThreads / 32) + (tid >> 5);
-         lo < kPlanThreads && base + lo < a.num_reqs; lo += gridDim.x * (kPlanThreads / 32)) {
+    for (int lo = blockIdx.x * nw + (tid >> 5); lo < nt && base + lo < a.num_reqs;
+         lo += gridDim.x * nw) {
       const int ln = tid & 31;
       const int cnt_u = s_off_u[lo + 1] - s_off_u[lo];
       if (cnt_u == 0) continue;
@@ -324,8 +328,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
         dst[1] = make_int4(s_q0[lo], qn, 0, 0);
       }
     }
-    for (int i = blockIdx.x * kPlanThreads + tid; i < tot_t; i += gridDim.x * kPlanThreads) {
-      const int lo = find_owner(s_off_t, i);
+    for (int i = blockIdx.x * nt + tid; i < tot_t; i += gridDim.x * nt) {
+      const int lo = find_owner(s_off_t, nt, i);
       // a request's query tiles from the last (most keys) to the first, so
       // that the persistent prefill grid starts with the longest items
       const int n = s_n[lo], ctx = s_len[lo] - n;
@@ -362,10 +366,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
 }  // namespace
 
 cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cudaStream_t st) {
-  // one warp per request of the first 1024-request chunk, at most 16 CTAs
-  const int warps = kPlanThreads / 32;
-  const int grid = a.num_reqs <= warps ? 1 : (a.num_reqs >= 16 * warps ? 16 : (a.num_reqs + warps - 1) / warps);
-  plan_kernel<<<grid, kPlanThreads, 0, st>>>(a, ws, dec_grid);
+  // a thread per request of a chunk (whole warps, at most 1024); one warp
+  // of the grid per request of the first chunk, at most 16 CTAs
+  const int threads = std::min(kPlanThreads, std::max(32, (a.num_reqs + 31) / 32 * 32));
+  const int warps = threads / 32;
+  const int want = (std::min(a.num_reqs, threads) + warps - 1) / warps;
+  const int grid = std::max(1, std::min(16, want));
+  plan_kernel<<<grid, threads, 0, st>>>(a, ws, dec_grid);
   return cudaGetLastError();
 }
 

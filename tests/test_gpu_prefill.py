@@ -158,3 +158,18 @@ def test_prefill_chunk_after_long_context():
     key tiles, the steady state of the prefill kernel, next to a decode."""
     step = W.build(W.custom([32768, 900], [200, 1], 8, 2, seed=73))
     run_and_check(step, "prefill after a long context")
+
+
+def test_more_requests_than_one_plan_pass():
+    """2,600 requests: the step plan takes them in passes of 1,024, carrying
+    every offset (decode units by length class, split pairs, partial rows,
+    prefill tiles) from one pass to the next.  Decodes of 1 to 4 tokens and
+    prefill chunks are spread over all three passes."""
+    rng = np.random.default_rng(2600)
+    n = 2600
+    kind = rng.choice(3, size=n, p=[0.9, 0.07, 0.03])  # decode, multi-token decode, chunk
+    q_len = np.where(kind == 0, 1, np.where(kind == 1, rng.integers(2, 5, n),
+                                            rng.integers(20, 200, n)))
+    ctx = np.where(kind == 2, rng.integers(0, 300, n), rng.integers(1, 160, n))
+    step = W.build(W.custom(ctx.tolist(), q_len.tolist(), 4, 2, seed=2600, pad_tokens=3))
+    run_and_check(step, "2600 requests")
