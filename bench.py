@@ -515,7 +515,8 @@ def main():
                 "peak": peak, "unit": "TFLOP/s", "peak_source": "measured" if peak else None}
         srcs = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu",
                 "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
-                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
+                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh",
+                "paged_kv_attention_05_gb300/csrc/pkv_combine.cuh"]
     else:
         algo = decode_algorithmic_bytes(spec, 1 if int8 else 2) if dominant == "decode" else \
             2 * s.num_tokens * s.hkv * d * 2 * (1.5 if int8 else 2)
