@@ -101,6 +101,14 @@ def _require(t, dtype, name, device=True):
         raise ValueError("%s must be a CUDA tensor" % name)
 
 
+def _per_row(t):
+    """Elements in one row of a [rows, ...] tensor (also when it has no rows)."""
+    n = 1
+    for x in t.shape[1:]:
+        n *= x
+    return n
+
+
 def _rows3(t, name):
     """Row stride of a [rows, heads, 128] tensor whose per-row block is contiguous."""
     if t.dim() == 2:
@@ -153,7 +161,7 @@ def pkv_attention(q, key_cache, value_cache, query_start_loc, seq_lens, block_ta
     if q.dim() != 3:
         raise ValueError("q must be [rows, num_heads, head_size]")
     rows, hq, _ = q.shape
-    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+    if out.shape[0] < rows or _per_row(out) != hq * d:
         raise ValueError("out must hold [rows, num_heads * head_size]")
     bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
     if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
@@ -214,7 +222,7 @@ def pkv_attention_int8(q, key_cache, value_cache, k_scale, v_scale, query_start_
     if q.dim() != 3:
         raise ValueError("q must be [rows, num_heads, head_size]")
     rows, hq, _ = q.shape
-    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+    if out.shape[0] < rows or _per_row(out) != hq * d:
         raise ValueError("out must hold [rows, num_heads * head_size]")
     bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
     if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
@@ -258,7 +266,7 @@ def pkv_attention_planned(q, key_cache, value_cache, block_table, scale, out, st
     if q.dim() != 3:
         raise ValueError("q must be [rows, num_heads, head_size]")
     rows, hq, _ = q.shape
-    if out.shape[0] < rows or out.numel() // max(out.shape[0], 1) != hq * d:
+    if out.shape[0] < rows or _per_row(out) != hq * d:
         raise ValueError("out must hold [rows, num_heads * head_size]")
     _check(load().pkv_attention_planned(q.data_ptr(), _rows3(q, "q"), hq, key_cache.data_ptr(),
                                         value_cache.data_ptr(), nb, bs, hkv, d,
