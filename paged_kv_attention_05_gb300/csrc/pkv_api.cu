@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -164,6 +165,17 @@ Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv)
   return z;
 }
 
+// Room for the plan's one-wave split of a small batch: as many decode units
+// as the decode grid has workers, each with up to one unit's query rows of
+// partial results (the plan takes a chunk shorter than kMinChunk only where
+// the workspace holds what it makes).
+Sizes with_wave_room(Sizes z, int64_t q_rows, int group, int workers) {
+  if (z.units < workers) z.units = workers;
+  const int64_t rows = std::min<int64_t>(dec_rows_cap(group), q_rows * group);
+  if (z.part_rows < (int64_t)workers * rows) z.part_rows = (int64_t)workers * rows;
+  return z;
+}
+
 size_t workspace_bytes(const Sizes& z) {
   size_t b = 256;                                      // header
   b += (size_t)z.units * sizeof(DecUnit);
@@ -306,7 +318,10 @@ int check_meta(int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
 int plan_locked(DeviceState* s, int64_t q_rows, int32_t num_heads, int32_t num_kv_heads,
                 const int32_t* query_start_loc, const int32_t* seq_lens,
                 int64_t block_table_width, int32_t num_reqs, int kv_int8, cudaStream_t st) {
-  const Sizes z = sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads);
+  const int workers = decode_workers(num_heads / num_kv_heads, kv_int8, s->sms);
+  const Sizes z = with_wave_room(
+      sizes_for(num_reqs, q_rows, block_table_width, num_heads, num_kv_heads), q_rows,
+      num_heads / num_kv_heads, workers);
   Workspace ws;
   int rc = ensure_workspace(s, z, st, &ws);
   if (rc) return rc;
@@ -319,7 +334,6 @@ int plan_locked(DeviceState* s, int64_t q_rows, int32_t num_heads, int32_t num_k
   a.bt_width = block_table_width;
   a.num_reqs = num_reqs;
   a.kv_int8 = kv_int8;
-  const int workers = decode_workers(num_heads / num_kv_heads, kv_int8, s->sms);
   cudaError_t e = traced(1, st, [&] { return launch_plan(a, ws, workers, st); });
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   // an int8 plan leaves prefill-class requests out: it cannot serve a bf16 call
@@ -526,8 +540,11 @@ extern "C" int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows,
   int rc = current_state(&s);
   if (rc) return rc;
   Workspace ws;
-  return ensure_workspace(s, sizes_for(max_reqs, max_q_rows, block_table_width, num_heads,
-                                       num_kv_heads),
+  const int group = num_heads / num_kv_heads;
+  const int workers = std::max(decode_workers(group, 0, s->sms), decode_workers(group, 1, s->sms));
+  return ensure_workspace(s, with_wave_room(sizes_for(max_reqs, max_q_rows, block_table_width,
+                                                      num_heads, num_kv_heads),
+                                            max_q_rows, group, workers),
                           nullptr, &ws);
 }
 

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // size the split-KV chunk (a thread keeps its first request's
   // classification for pass 2)
   long long dec_keys = 0;
-  int dec_reqs = 0, dec_lmax = 0;
+  int dec_reqs = 0, dec_lmax = 0, dec_rmax = 0;  // rmax: most query rows of a decode
   ReqInfo first{0, 0, 0, 0, 0};
   for (int r = tid; r < a.num_reqs; r += nt) {
     ReqInfo ri = classify(a, r);
@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       dec_keys += ri.L;
       dec_reqs += 1;
       dec_lmax = max(dec_lmax, ri.L);
+      dec_rmax = max(dec_rmax, ri.n * (a.hq / a.hkv));
     }
   }
 #pragma unroll
@@ -153,33 +154,39 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     dec_keys += __shfl_xor_sync(0xffffffffu, dec_keys, o);
     dec_reqs += __shfl_xor_sync(0xffffffffu, dec_reqs, o);
     dec_lmax = max(dec_lmax, __shfl_xor_sync(0xffffffffu, dec_lmax, o));
+    dec_rmax = max(dec_rmax, __shfl_xor_sync(0xffffffffu, dec_rmax, o));
   }
-  __shared__ int red_n[32], red_l[32];
+  __shared__ int red_n[32], red_l[32], red_r[32];
   if ((tid & 31) == 0) {
     red[tid >> 5] = dec_keys;
     red_n[tid >> 5] = dec_reqs;
     red_l[tid >> 5] = dec_lmax;
+    red_r[tid >> 5] = dec_rmax;
   }
   __syncthreads();
   if (tid < 32) {
     long long x = tid < nw ? red[tid] : 0;
     int n = tid < nw ? red_n[tid] : 0, l = tid < nw ? red_l[tid] : 0;
+    int rr = tid < nw ? red_r[tid] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       x += __shfl_xor_sync(0xffffffffu, x, o);
       n += __shfl_xor_sync(0xffffffffu, n, o);
       l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+      rr = max(rr, __shfl_xor_sync(0xffffffffu, rr, o));
     }
     if (tid == 0) {
       red[0] = x;
       red_n[0] = n;
       red_l[0] = l;
+      red_r[0] = rr;
     }
   }
   __syncthreads();
   const long long total_keys = red[0];
   const long long dec_pairs = (long long)red_n[0] * a.hkv;  // (request, KV head) pairs
   const int lmax = red_l[0];
+  const int rmax = red_r[0];
   // aim for about four units per decode worker (dec_grid = workers), in
   // whole 64-key tiles, at most kMaxChunk keys; at least kMinChunk keys, and
   // at least 32 keys per query head of the group, so that a split's partial
@@ -191,13 +198,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   int chunk = (int)(want < lo_chunk ? lo_chunk : (want > kMaxChunk ? kMaxChunk : want));
   // When even the longest request's splits, times the pairs, fit one wave of
   // workers, the step takes one unit's time: give every pair as many splits
-  // as the wave has room for (units of at most that many keys, kMinChunk at
-  // least), so that the wave is full and each unit short.
+  // as the wave has room for (units of at most that many keys), so that the
+  // wave is full and each unit short.  The workspace is sized for chunks of
+  // kMinChunk keys; a shorter chunk, down to one 64-key tile, is taken where
+  // the workspace also holds the units and partial rows it makes: at most
+  // `per` splits a pair, pairs x per units and pairs x per x rmax rows.  (The
+  // batch is small then: the extra partial results are small next to the
+  // latency a long unit's chain of pages costs.)
   if (dec_pairs > 0 && dec_pairs * ((lmax + chunk - 1) / chunk) <= dec_grid) {
     const long long per_pair = dec_grid / dec_pairs;
     long long c = (lmax + per_pair - 1) / per_pair;
     c = (c + kDecTile - 1) / kDecTile * kDecTile;
-    if (c < kMinChunk) c = kMinChunk;
+    if (c < kMinChunk) {
+      long long per = per_pair;
+      per = min(per, ws.max_units / dec_pairs);
+      per = min(per, ws.max_part_rows / (dec_pairs * (long long)max(rmax, 1)));
+      long long c2 = per >= 1 ? (lmax + per - 1) / per : kMinChunk;
+      c2 = (c2 + kDecTile - 1) / kDecTile * kDecTile;
+      c = c2 < kMinChunk ? (c2 > c ? c2 : c) : kMinChunk;
+    }
     if (c < chunk) chunk = (int)c;
   }
 
