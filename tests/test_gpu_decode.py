@@ -123,3 +123,40 @@ def test_decode_longest_request():
     ctx = [32768 * 16 - 1, 40]
     step = W.build(W.custom(ctx, [1, 1], 8, 1, seed=71, num_blocks=32768 + 8, bt_width=32768))
     run_and_check(step, "longest request decode")
+
+
+def test_split_size_does_not_change_the_result():
+    """The same four decode requests, on the same cache, split two ways: alone
+    (one wave of 64-key units) and as the first requests of a 204-request
+    batch (384-key units).  Both match the oracle; against each other they
+    differ only by rounding: the splits change each probability's reference
+    max, and P is rounded to bf16 (2^-9 relative) before P.V, then the output
+    to bf16 (one ulp, 2^-7 relative)."""
+    ctx = [3000, 1500, 700, 9000] + [4096] * 200
+    step = W.build(W.custom(ctx, [1] * len(ctx), 8, 2, seed=4242))
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()                       # all 204 requests
+    alone = torch.empty_like(ds.out)
+    alone.view(torch.int16).fill_(W.BF16_NAN)
+    pkv.pkv_attention(ds.q, ds.key_cache, ds.value_cache, ds.qsl, ds.seq_lens, ds.block_table,
+                      4, step.scale, alone)
+    assert pkv.pkv_get_error() == 0
+    in_batch = ds.out_f64()[:4]
+    by_itself = W.bf16_to_f32(alone.view(torch.int16).cpu().numpy().view(np.uint16))
+    by_itself = by_itself.astype(np.float64)
+    assert np.isnan(by_itself[4:]).all()
+    by_itself = by_itself[:4]
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    rows = np.repeat(np.arange(4, dtype=np.int64), 8)
+    heads = np.tile(np.arange(8, dtype=np.int32), 4)
+    ref, err = oracle.attention_sampled(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                        step.block_table, step.num_reqs, step.scale, rows, heads)
+    assert err == 0
+    ref = ref.reshape(4, 8, 128)
+    assert_close(in_batch, ref, "in the batch")
+    assert_close(by_itself, ref, "alone")
+    diff = np.abs(in_batch - by_itself)
+    assert (diff <= 1e-3 + 2.0 ** -7 * np.maximum(np.abs(in_batch), np.abs(by_itself))).all(), \
+        float(diff.max())
