@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   using C = Cfg<MT>;
-  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -129,6 +128,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
   }
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  grid_dep_wait();
+  grid_dep_launch();
+  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
@@ -408,6 +411,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {
   constexpr int kWarpsPerBlock = kCombineThreads / 32;
+  grid_dep_wait();  // the decode kernel's partial results
   combine_splits(a, ws, blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), gridDim.x * kWarpsPerBlock);
 }
 
@@ -422,8 +426,8 @@ cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  decode_kernel<MT><<<sms, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
-  return cudaGetLastError();
+  return launch_dependent(decode_kernel<MT>, dim3(sms), dim3(C::kThreads), C::kSmem, st, tq, tk,
+                          tv, a, ws);
 }
 
 }  // namespace
@@ -440,8 +444,7 @@ cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaS
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
-  combine_kernel<<<sms * 8, kCombineThreads, 0, st>>>(a, ws);
-  return cudaGetLastError();
+  return launch_dependent(combine_kernel, dim3(sms * 8), dim3(kCombineThreads), 0, st, a, ws);
 }
 
 }  // namespace pkv

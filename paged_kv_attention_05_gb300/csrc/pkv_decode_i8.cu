@@ -112,7 +112,6 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   using C = Cfg8<MT>;
-  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -140,6 +139,10 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
       *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
   }
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  grid_dep_wait();
+  grid_dep_launch();
+  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
@@ -467,8 +470,8 @@ cudaError_t launch_i8(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
       !make_cache_map_i8(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map_i8(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  decode_i8_kernel<MT><<<sms, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a, ws);
-  return cudaGetLastError();
+  return launch_dependent(decode_i8_kernel<MT>, dim3(sms), dim3(C::kThreads), C::kSmem, st, tq,
+                          tk, tv, a, ws);
 }
 
 }  // namespace

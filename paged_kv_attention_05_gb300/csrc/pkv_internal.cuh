@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "pkv.h"
 
@@ -178,5 +179,43 @@ cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cuda
 int decode_workers(int group, int kv_int8, int sms);
 int decode_i8_warps(int group);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
+
+// Programmatic dependent launch.  The attention kernels after the cache write
+// (plan, decode, prefill, merge) are launched with programmatic stream
+// serialisation: a kernel's CTAs may start while the kernel before it in the
+// stream is still running, do their set-up (barriers, shared-memory
+// clearing), and then wait in grid_dep_wait() until that kernel has finished
+// and its writes are visible, before reading anything it produced.  Each such
+// kernel waits before it finishes, so finishing implies that every kernel
+// before it has finished too.  Launched without the attribute, the wait
+// returns at once.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Waits until the kernel before this one in the stream has finished and its
+// memory is visible (a no-op without programmatic serialisation).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+// Lets the next kernel in the stream start its set-up; it still waits for
+// this kernel to finish before it reads what this kernel writes.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+#endif
 
 }  // namespace pkv

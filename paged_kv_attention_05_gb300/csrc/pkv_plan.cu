@@ -132,6 +132,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   __shared__ int4 smem33[33];
   __shared__ long long red[32];
   const int tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
+  // the metadata may come from the kernel before this one (a device-side
+  // step preparation), and the work lists it overwrites were read by the
+  // previous step's kernels: wait for it, then let the decode grid set up
+  grid_dep_wait();
+  grid_dep_launch();
 
   // pass 1: total decode keys, decode requests and their longest length, to
   // size the split-KV chunk (a thread keeps its first request's
@@ -391,8 +396,7 @@ cudaError_t launch_plan(const AttnArgs& a, const Workspace& ws, int dec_grid, cu
   const int warps = threads / 32;
   const int want = (std::min(a.num_reqs, threads) + warps - 1) / warps;
   const int grid = std::max(1, std::min(16, want));
-  plan_kernel<<<grid, threads, 0, st>>>(a, ws, dec_grid);
-  return cudaGetLastError();
+  return launch_dependent(plan_kernel, dim3(grid), dim3(threads), 0, st, a, ws, dec_grid);
 }
 
 }  // namespace pkv

@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // decode kernel ran before it in stream order), which saves a launch of its
   // own: every warp of the grid does it when the batch has no prefill work,
   // else the epilogue warps, before their first output tile is due.
+  grid_dep_wait();  // the work lists and the decode kernel's partial results
   if (ws.hdr->n_pre_entries == 0) {  // (every CTA agrees)
     combine_splits(a, ws, blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5),
                    gridDim.x * (kThreads / 32));
@@ -745,8 +746,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cuda
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  prefill_kernel<<<sms, kThreads, kSmemBytes, st>>>(tq, tk, tv, a, ws);
-  return cudaGetLastError();
+  return launch_dependent(prefill_kernel, dim3(sms), dim3(kThreads), kSmemBytes, st, tq, tk, tv,
+                          a, ws);
 }
 
 }  // namespace pkv
