@@ -14,7 +14,11 @@
  *   - Row strides are counted in elements, not bytes.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on `stream` and returns; none
- *     synchronises except pkv_get_error.
+ *     synchronises except pkv_get_error.  Work is stream ordered as usual:
+ *     the attention calls launch their kernels with programmatic dependent
+ *     launch, so a kernel may begin its set-up while the work before it on
+ *     the stream is finishing, but it reads and writes no global memory
+ *     until that work has finished.
  *   - The caller owns every buffer it passes; the library keeps no pointer to
  *     any of them after the call returns.  The library owns one grow-only
  *     device workspace per device (step plan, split-KV partial results and
