@@ -16,6 +16,7 @@ replica of the batch (the step shards by request with no exchange), and the
 value is the total over ranks divided by the slowest rank's time.
 """
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -119,7 +120,7 @@ def profiled_traffic(kernel, workload, sources):
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -140,7 +141,10 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Ends sampling; clocks and reasons from the samples taken between the
+        host times t0 and t1 (the loaded window), all samples if none fall
+        there."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
@@ -149,25 +153,29 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]),
+                                 {nm for nm, val in zip(names, parts[6:10])
+                                  if val.lower().startswith("active")}))
                 except ValueError:
                     continue
-                for nm, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(nm)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        loaded = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        use = loaded or rows
+        reasons = set().union(*[r[3] for r in use]) if use else set()
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": ("the timed steps, the traced pass and at least 0.6 s more of the "
+                           "same steps" if loaded else "whole run (no sample in the loaded window)")}
 
 
 def max_over_ranks(x, dist, device):
@@ -368,11 +376,16 @@ def main():
         pkv.pkv_attention(q, kc, vc, qsl, seq_lens, block_table, s.num_reqs,
                           s.scale, outs[c], stream=stream)
 
+    # the clock sampler starts before the warm-up, so that the GPU goes from
+    # the warm-up steps straight into the timed ones (no idle gap)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
     for i in range(max(args.warmup, 0)):
         one_step(i)
     torch.cuda.synchronize()
     bits = pkv.pkv_get_error()
     if bits:
+        clocks.stop()
         raise SystemExit("device error word %d after warm-up" % bits)
 
     def barrier():
@@ -383,10 +396,9 @@ def main():
     # The timed region: K steps, no per-launch events (recording an event
     # between two launches holds the next one back by a few microseconds,
     # which lengthens short steps by up to a third).
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
     launches0 = pkv.pkv_launch_count()
     barrier()
+    t_load0 = time.time()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -405,8 +417,19 @@ def main():
     barrier()
     pkv.pkv_trace_enable(False)
     trace = pkv.pkv_trace_read()
-    clk = clocks.stop()
+    # the same steps for at least 0.6 s more (untimed, in batches of about
+    # 50 ms), so that the 200 ms clock samples see the GPU under this load
+    # even when the timed region is shorter than one sampling period
     ms = e0.elapsed_time(e1)
+    per = max(1, int(0.05 / max(ms / args.steps / 1e3, 1e-6)))
+    i, t_soak = args.steps, time.time() + 0.6
+    while time.time() < t_soak:
+        for _ in range(per):
+            one_step(i)
+            i += 1
+        torch.cuda.synchronize()
+    t_load1 = time.time()
+    clk = clocks.stop(t_load0, t_load1)
     ms = max_over_ranks(ms, dist, "cuda")
     ms_per_step = ms / args.steps
     name, unit = metric_of(spec)

@@ -101,3 +101,34 @@ def test_timed_steps_read_from_hbm(name, elem):
         assert n == 1
     if name == "tiny_mixed":
         assert n > 40
+
+
+def test_clock_record_takes_the_loaded_window(tmp_path):
+    # nvidia-smi lines (timestamp first): one before the load, two inside it,
+    # one of them with the power cap active; the record keeps the two
+    import datetime
+    import time
+    b = _bench()
+    now = time.time()
+
+    def line(t, sm, cap):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return "%s, 0, %d, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, %s\n" % (
+            ts, sm, "Active" if cap else "Not Active")
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    cs = b.ClockSampler(0)
+    cs.path = str(tmp_path / "clocks.csv")
+    with open(cs.path, "w") as f:
+        f.write(line(now - 1.0, 1200, False) + line(now + 0.1, 2070, True) +
+                line(now + 0.3, 2040, False))
+    cs.proc = Done()
+    rec = cs.stop(now, now + 0.5)
+    assert rec["samples"] == 2 and rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["window"].startswith("the timed steps")
