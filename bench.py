@@ -66,11 +66,13 @@ def decode_algorithmic_bytes(spec, kv_elem_bytes=2):
     """Algorithmic bytes of one decode-kernel launch: every decode request's
     K and V rows once per KV head (bf16, or int8 codes), its query rows read
     and output rows written (bf16)."""
+    G = spec.hq // spec.hkv
+    cap = 16 if G <= 16 else 32  # query rows of one decode unit
     b = 0
     for c, n in zip(spec.ctx, spec.q_len):
-        if n == 1:
-            b += (c + 1) * spec.hkv * spec.head_size * kv_elem_bytes * 2
-            b += 2 * spec.hq * spec.head_size * 2
+        if 0 < n and n * G <= cap:  # the requests the decode kernel serves
+            b += (c + n) * spec.hkv * spec.head_size * kv_elem_bytes * 2
+            b += 2 * n * spec.hq * spec.head_size * 2
     return b
 
 

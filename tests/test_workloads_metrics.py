@@ -132,3 +132,23 @@ def test_clock_record_takes_the_loaded_window(tmp_path):
     rec = cs.stop(now, now + 0.5)
     assert rec["samples"] == 2 and rec["sm_mhz"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
     assert rec["reasons"] == ["sw_power_cap"] and rec["window"].startswith("the timed steps")
+
+
+def test_decode_kernel_algorithmic_bytes():
+    # every decode request's K/V rows once per KV head, its query row read and
+    # output row written; prefill-class requests are not the decode kernel's
+    b = _bench()
+    assert b.decode_algorithmic_bytes(W.spec("gqa_decode")) == \
+        4_295_491_584 + 128 * 2 * 32 * 128 * 2 == 4_297_588_736
+    assert b.decode_algorithmic_bytes(W.spec("gqa_decode"), 1) == \
+        4_295_491_584 // 2 + 128 * 2 * 32 * 128 * 2
+    mqa = W.spec("mqa_long_decode")
+    assert b.decode_algorithmic_bytes(mqa) == 536_887_296 + 32 * 2 * 32 * 128 * 2
+    # the 512-token mixed batch: 64 decodes count, the two 224-token chunks do not
+    mc = W.spec("mixed_chunked")
+    dec = [(c, n) for c, n in zip(mc.ctx, mc.q_len) if n == 1]
+    assert b.decode_algorithmic_bytes(mc) == sum(
+        (c + 1) * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 for c, _ in dec)
+    # a 3-token decode of a GQA group of 4 (12 rows) is decode work; 5 tokens are not
+    s = W.custom([100, 100], [3, 5], 32, 8)
+    assert b.decode_algorithmic_bytes(s) == 103 * 8 * 128 * 4 + 2 * 3 * 32 * 128 * 2
