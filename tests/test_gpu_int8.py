@@ -112,3 +112,32 @@ def test_int8_decode_full_size(name):
     step = W.build(W.spec(name))
     ds, got, ref = run_int8(step, "int8 " + name)
     _check_all(step, got, ref, "int8 " + name)
+
+
+def test_int8_split_size_does_not_change_the_result():
+    """As for the bf16 cache: the same four decode requests over the same
+    codes, alone (one wave of 64-key units) and as the first requests of a
+    204-request batch (longer units), both within the tolerance of the
+    oracle and within 1e-3 + one bf16 ulp of each other (P is rounded to fp16
+    before P.V and the splits move each probability's reference max)."""
+    ctx = [3000, 1500, 700, 9000] + [4096] * 200
+    step = W.build(W.custom(ctx, [1] * len(ctx), 8, 2, seed=4343))
+    ds, got, ref = run_int8(step, "int8 batch")
+    in_batch = got[:4]
+    k8, v8 = _history_codes(step)
+    dk, dv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pkv.pkv_write_int8(ds.k, ds.v, dk, dv, ds.slot_mapping, KS, VS)
+    alone = torch.empty_like(ds.out)
+    alone.view(torch.int16).fill_(W.BF16_NAN)
+    pkv.pkv_attention_int8(ds.q, dk, dv, KS, VS, ds.qsl, ds.seq_lens, ds.block_table, 4,
+                           step.scale, alone)
+    assert pkv.pkv_get_error() == 0
+    by_itself = W.bf16_to_f32(alone.view(torch.int16).cpu().numpy().view(np.uint16))
+    by_itself = by_itself.astype(np.float64)
+    assert np.isnan(by_itself[4:]).all()
+    by_itself = by_itself[:4]
+    assert_close(in_batch, ref[:4], "int8 in the batch")
+    assert_close(by_itself, ref[:4], "int8 alone")
+    diff = np.abs(in_batch - by_itself)
+    assert (diff <= 1e-3 + 2.0 ** -7 * np.maximum(np.abs(in_batch), np.abs(by_itself))).all(), \
+        float(diff.max())
