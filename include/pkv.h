@@ -66,6 +66,11 @@ extern "C" {
 #define PKV_DEV_ERR_TIMEOUT 32   /* an on-chip pipeline wait gave up          */
 #define PKV_DEV_ERR_INT8_PREFILL 64 /* pkv_attention_int8: a request too long for
                                        the decode path (its rows are skipped)  */
+#define PKV_DEV_ERR_CAPACITY 128 /* the step plan outgrew the workspace: the
+                                    whole step was skipped (no output row
+                                    written).  The library sizes the workspace
+                                    so that this does not happen; the bit
+                                    reports a broken bound, never truncation */
 
 /*
  * pkv_write — the cache-write scatter.
@@ -268,30 +273,36 @@ int pkv_attention_int8(const void* q, int64_t q_row_stride, int64_t q_rows, int3
  * pkv_attention_noalloc — pkv_attention for callers that cannot allocate
  * device memory.  The pages this library follows have no counterpart to it.
  *
- * Some callers cannot call cudaMalloc: code running while a CUDA graph is
- * being captured, services that fix their device-memory footprint at start-up,
- * or hosts whose device memory is handed out by an allocator the library must
- * not bypass.  pkv_attention grows its workspace with cudaMalloc on first
- * use; this call computes the same result with the same kernels but keeps the
- * scratch (step plan, work lists, split-KV partials) in one statically sized
- * device array inside the library (32 MiB; every GPU that loads the library
- * holds it until the process exits), and allocates nothing.
+ * Some callers cannot call cudaMalloc: services that fix their device-memory
+ * footprint at start-up and may not grow it later, hosts whose device memory
+ * is handed out by an allocator of their own that the library must not
+ * bypass, and latency-critical loops that cannot take the device-wide
+ * synchronisation a cudaMalloc / cudaFree pair brings.  pkv_attention grows
+ * its workspace with cudaMalloc on first use; this call runs the same kernels
+ * but keeps the scratch (step plan, work lists, split-KV partials) in one
+ * statically sized device array inside the library (32 MiB; every GPU that
+ * loads the library holds it until the process exits), and allocates
+ * nothing.
  *
- * Arguments, layouts and results are those of pkv_attention.  A batch whose
- * scratch bound (the bound pkv_attention sizes its workspace by: with
- * S = ceil(16 * block_table_width / 256) splits and G = num_heads /
+ * Arguments, layouts, checks and results are those of pkv_attention.  A
+ * batch whose scratch bound (the bound pkv_attention sizes its workspace by:
+ * with S = ceil(16 * block_table_width / 256) splits and G = num_heads /
  * num_kv_heads, num_reqs * num_kv_heads * S split units of 32 bytes, plus
  * S * num_kv_heads * min(q_rows * G, num_reqs * (G <= 16 ? 16 : 32)) partial
  * rows of 520 bytes, plus the prefill and pair lists) exceeds 32 MiB is
- * refused with PKV_ERR_UNSUPPORTED before anything
- * is enqueued.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Every call shares the one array: calls
- * whose kernels overlap on the GPU (e.g. on two streams) race, and must be
- * serialised by the caller.  Device-side metadata errors are skipped as in
- * pkv_attention but are not reported (pkv_get_error reads only the word of
- * the allocating calls), and pkv_last_error_string is not set: the return
- * code alone says which host check failed.
+ * refused with PKV_ERR_UNSUPPORTED before anything is enqueued.  Where the
+ * array also holds pkv_attention's extra room for a small batch's one-wave
+ * split (pkv_workspace_size), both calls make the same plan and give the same
+ * bits; otherwise a small batch may be split into fewer, longer pieces and
+ * the result agrees with pkv_attention's up to fp32 rounding.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Every call shares the one array: calls whose kernels overlap on the GPU
+ * (e.g. on two streams) race, and must be serialised by the caller.
+ * Device-side metadata errors are skipped as in pkv_attention and reported in
+ * an error word of this call's own, which pkv_get_error reads and clears
+ * along with the other; pkv_last_error_string is not set: the return code
+ * alone says which host check failed.
  */
 int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_t q_rows, int32_t num_heads,
                           const void* key_cache, const void* value_cache, int64_t num_blocks,
@@ -314,9 +325,36 @@ int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows, int64_t block_ta
                           int32_t num_heads, int32_t num_kv_heads);
 
 /*
+ * pkv_workspace_size — what pkv_reserve_workspace would hold for these sizes
+ * on a device with num_sms SMs (pkv_num_sms()), computed on the host alone
+ * (no device is touched, nothing is allocated): the workspace's bytes and the
+ * capacities of the step plan kept in it.  A plan never holds more than these
+ * (the plan kernel reports PKV_DEV_ERR_CAPACITY and runs nothing if it
+ * would); the split-KV chunk the plan chooses is sized for decode_workers
+ * independent decode workers (decode_workers_int8 for int8 caches).
+ * Returns PKV_OK, or PKV_ERR_ARG for negative sizes, a head count that is not
+ * a multiple of num_kv_heads or num_sms <= 0.
+ */
+typedef struct {
+  int64_t bytes;            /* device bytes of the workspace                   */
+  int64_t decode_units;     /* split-KV decode work units                     */
+  int64_t prefill_tiles;    /* prefill work entries (128-row query tiles)     */
+  int64_t split_pairs;      /* (request, KV head) pairs whose splits merge    */
+  int64_t partial_rows;     /* split-KV partial rows (130 fp32 values each)   */
+  int32_t decode_workers;   /* decode workers of a bf16 call                  */
+  int32_t decode_workers_int8; /* decode workers of an int8 call              */
+} pkv_workspace_info;
+int pkv_workspace_size(int32_t max_reqs, int64_t max_q_rows, int64_t block_table_width,
+                       int32_t num_heads, int32_t num_kv_heads, int32_t num_sms,
+                       pkv_workspace_info* info);
+
+/*
  * pkv_get_error — synchronises `stream`, then returns the current device's
- * error word (an OR of PKV_DEV_ERR_* bits accumulated since the last read)
- * in *bits and clears it.  Returns PKV_OK or a host error code.
+ * error words (an OR of PKV_DEV_ERR_* bits accumulated since the last read:
+ * the allocating calls' word and pkv_attention_noalloc's) in *bits and
+ * clears them.  Allocates nothing (a device no allocating call has used has
+ * no word of its own yet and reports only pkv_attention_noalloc's).  Returns
+ * PKV_OK or a host error code.
  */
 int pkv_get_error(void* stream, int32_t* bits);
 

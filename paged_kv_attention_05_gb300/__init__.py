@@ -21,12 +21,12 @@ from ._binding import (DEV_ERR_BITS, TRACE_KINDS, PkvError, library_path, load,
                        pkv_attention, pkv_attention_int8, pkv_attention_noalloc,
                        pkv_attention_planned, pkv_get_error, pkv_plan,
                        pkv_launch_count, pkv_num_sms, pkv_prepare_step,
-                       pkv_reserve_workspace, pkv_trace_enable, pkv_trace_read, pkv_write,
-                       pkv_write_int8)
+                       pkv_reserve_workspace, pkv_trace_enable, pkv_trace_read,
+                       pkv_workspace_size, pkv_write, pkv_write_int8)
 
 __all__ = ["pkv_write", "pkv_attention", "pkv_attention_noalloc", "pkv_prepare_step",
            "pkv_write_int8", "pkv_attention_int8", "pkv_plan", "pkv_attention_planned",
            "pkv_get_error",
-           "pkv_reserve_workspace",
+           "pkv_reserve_workspace", "pkv_workspace_size",
            "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read", "pkv_launch_count",
            "PkvError", "DEV_ERR_BITS", "TRACE_KINDS", "load", "library_path"]

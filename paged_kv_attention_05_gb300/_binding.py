@@ -14,12 +14,13 @@ DEV_ERR_BITS = {
     "BLOCK_ID": 16,
     "TIMEOUT": 32,
     "INT8_PREFILL": 64,
+    "CAPACITY": 128,
 }
 
 EXPORTS = ["pkv_write", "pkv_attention", "pkv_reserve_workspace", "pkv_get_error",
            "pkv_last_error_string", "pkv_num_sms", "pkv_trace_enable", "pkv_trace_read",
            "pkv_launch_count", "pkv_prepare_step", "pkv_write_int8", "pkv_attention_int8",
-           "pkv_plan", "pkv_attention_planned"]
+           "pkv_plan", "pkv_attention_planned", "pkv_workspace_size"]
 TRACE_KINDS = ["write", "plan", "decode", "prefill", "combine", "prepare"]
 
 
@@ -279,8 +280,33 @@ def pkv_reserve_workspace(max_reqs, max_q_rows, block_table_width, num_heads, nu
                                         int(num_heads), int(num_kv_heads)))
 
 
+class WorkspaceInfo(ctypes.Structure):
+    """Mirror of pkv_workspace_info (include/pkv.h)."""
+    _fields_ = [("bytes", ctypes.c_int64), ("decode_units", ctypes.c_int64),
+                ("prefill_tiles", ctypes.c_int64), ("split_pairs", ctypes.c_int64),
+                ("partial_rows", ctypes.c_int64), ("decode_workers", ctypes.c_int32),
+                ("decode_workers_int8", ctypes.c_int32)]
+
+
+def pkv_workspace_size(max_reqs, max_q_rows, block_table_width, num_heads, num_kv_heads,
+                       num_sms) -> dict:
+    """Bytes and plan capacities of the workspace pkv_reserve_workspace would
+    hold for these sizes on a device with num_sms SMs (host-only)."""
+    L = load()
+    fn = L.pkv_workspace_size
+    if fn.argtypes is None:
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                       ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(WorkspaceInfo)]
+    info = WorkspaceInfo()
+    _check(fn(int(max_reqs), int(max_q_rows), int(block_table_width), int(num_heads),
+              int(num_kv_heads), int(num_sms), ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in WorkspaceInfo._fields_}
+
+
 def pkv_get_error(stream=None) -> int:
-    """Synchronises the stream; returns and clears the device error word."""
+    """Synchronises the stream; returns and clears the device error words
+    (the allocating calls' and pkv_attention_noalloc's)."""
     bits = ctypes.c_int32(0)
     _check(load().pkv_get_error(_stream(stream), ctypes.byref(bits)))
     return bits.value

@@ -548,22 +548,57 @@ extern "C" int pkv_reserve_workspace(int32_t max_reqs, int64_t max_q_rows,
                           nullptr, &ws);
 }
 
+extern "C" int pkv_workspace_size(int32_t max_reqs, int64_t max_q_rows,
+                                  int64_t block_table_width, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t num_sms,
+                                  pkv_workspace_info* info) {
+  g_msg[0] = 0;
+  if (!info) return fail(PKV_ERR_ARG, "info is null");
+  if (max_reqs < 0 || max_q_rows < 0 || block_table_width < 0 || num_kv_heads <= 0 ||
+      num_heads <= 0 || num_heads % num_kv_heads || num_sms <= 0)
+    return fail(PKV_ERR_ARG, "bad sizes");
+  const int group = num_heads / num_kv_heads;
+  const int w16 = decode_workers(group, 0, num_sms), w8 = decode_workers(group, 1, num_sms);
+  // what pkv_reserve_workspace holds: room for both cache types' plans
+  const Sizes z = with_wave_room(
+      sizes_for(max_reqs, max_q_rows, block_table_width, num_heads, num_kv_heads), max_q_rows,
+      group, std::max(w16, w8));
+  info->bytes = (int64_t)workspace_bytes(z);
+  info->decode_units = z.units;
+  info->prefill_tiles = z.pre;
+  info->split_pairs = z.pairs;
+  info->partial_rows = z.part_rows;
+  info->decode_workers = w16;
+  info->decode_workers_int8 = w8;
+  return PKV_OK;
+}
+
 extern "C" int pkv_get_error(void* stream, int32_t* bits) {
   g_msg[0] = 0;
   if (!bits) return fail(PKV_ERR_ARG, "bits is null");
   std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState* s = nullptr;
-  int rc = current_state(&s);
-  if (rc) return rc;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_NO_DEVICE, "device %d out of range", dev);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaStreamSynchronize(st);
+  e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  // the word of the allocating calls (only if one ran on this device: a
+  // device no allocating call has used gets no state, and nothing is
+  // allocated here), then the word of pkv_attention_noalloc
   int v = 0;
-  e = cudaMemcpy(&v, s->err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "read error word");
-  e = cudaMemset(s->err, 0, sizeof(int));
-  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
-  *bits = v;
+  DeviceState& s = g_dev[dev];
+  if (s.ready) {
+    e = cudaMemcpy(&v, s.err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    e = cudaMemset(s.err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  int w = 0;
+  const int ce = noalloc_take_error(dev, &w);
+  if (ce) return cuda_fail(static_cast<cudaError_t>(ce), "read the no-alloc error word");
+  *bits = v | w;
   return PKV_OK;
 }
 

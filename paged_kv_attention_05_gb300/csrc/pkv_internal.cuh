@@ -88,6 +88,13 @@ struct Sizes {
 };
 Sizes sizes_for(int64_t reqs, int64_t q_rows, int64_t bt_width, int hq, int hkv);
 size_t workspace_bytes(const Sizes& z);
+// z grown to hold a small batch's one-wave split: one decode unit per worker,
+// each with up to one unit's query rows of partial results.
+Sizes with_wave_room(Sizes z, int64_t q_rows, int group, int workers);
+// Reads and clears the device error word of pkv_attention_noalloc on device
+// dev (0 when that call never ran there); returns 0 or a cudaError_t.
+// Allocates nothing.
+int noalloc_take_error(int dev, int* bits);
 Workspace carve_workspace(void* base, const Sizes& z, int* err);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current

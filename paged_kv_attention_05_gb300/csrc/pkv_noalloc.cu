@@ -1,13 +1,15 @@
 // pkv_attention_noalloc: the attention call for callers that must not
 // allocate device memory.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// being captured, services that must keep a fixed device-memory footprint
-// once they are up, or hosts whose memory is handed out by an allocator the
-// library is not allowed to bypass.  pkv_attention grows a workspace with
-// cudaMalloc on first use; this entry point runs the same kernels with their
-// scratch (step plan, work lists, split-KV partial results) in one
-// file-scope device array of fixed size instead, and allocates nothing.
+// Some callers cannot call cudaMalloc: services that fix their device-memory
+// footprint when they start and must not grow it afterwards, hosts whose
+// device memory is handed out by an allocator of their own that the library
+// must not bypass, and latency-critical loops that cannot afford the device
+// synchronisation a cudaMalloc/cudaFree pair implies.  pkv_attention grows a
+// workspace with cudaMalloc on first use; this entry point runs the same
+// kernels on the same step plan with their scratch (step plan, work lists,
+// split-KV partial results) in one file-scope device array of fixed size
+// instead, and allocates nothing.
 //
 // The array is a static __device__ object: every GPU that loads the library
 // holds kScratchBytes of it until the process exits.  In host code its name
@@ -17,7 +19,9 @@
 // previous call's contents; the plan kernel rewrites the work lists and
 // resets the scheduler cursors at the start of each call, which is all that
 // must start from zero.  Calls whose kernels overlap on the GPU (for example
-// on two streams) race on the array.
+// on two streams) race on the array.  The device error word of these calls
+// lives beside the array; pkv_get_error reads and clears it together with the
+// allocating calls' word.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -61,6 +65,8 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
   // same argument contract as pkv_attention
   if (block_size != kBlockSize || head_size != kHeadSize)
     return noalloc_fail(PKV_ERR_UNSUPPORTED, "block_size must be 16 and head_size 128");
+  // a decode unit packs the KV head into 16 bits (with the query-token count)
+  if (num_kv_heads > 32767) return noalloc_fail(PKV_ERR_UNSUPPORTED, "num_kv_heads > 32767");
   if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads)
     return noalloc_fail(PKV_ERR_UNSUPPORTED, "num_heads must be a multiple of num_kv_heads");
   if (num_heads / num_kv_heads > kMaxGroup)
@@ -123,7 +129,15 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
     sms = g_sms[dev];
   }
 
-  Workspace ws = carve_workspace(scratch, z, err);
+  // The plan of pkv_attention: a workspace for z plus room for a small
+  // batch's one-wave split (shorter split chunks, more units and partial
+  // rows), carved the same way, so that both calls make the same plan and the
+  // same bits.  Where that room does not fit beside z, the plan holds no more
+  // than z: a small batch may then take fewer, longer splits than
+  // pkv_attention, with the same result up to fp32 rounding.
+  Sizes zc = with_wave_room(z, q_rows, group, decode_workers(group, 0, sms));
+  if (workspace_bytes(zc) > kScratchBytes) zc = z;
+  Workspace ws = carve_workspace(scratch, zc, err);
   AttnArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.q_stride = q_row_stride;
@@ -150,3 +164,19 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
     return noalloc_fail(PKV_ERR_CUDA, "kernel launch failed");
   return PKV_OK;
 }
+
+namespace pkv {
+
+int noalloc_take_error(int dev, int* bits) {
+  *bits = 0;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (dev < 0 || dev >= kMaxDevices || !g_err_ptr[dev]) return 0;  // never used on dev
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, g_err_ptr[dev], sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(g_err_ptr[dev], 0, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  *bits = v;
+  return 0;
+}
+
+}  // namespace pkv

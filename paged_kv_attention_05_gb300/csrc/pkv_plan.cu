@@ -377,12 +377,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     __syncthreads();  // the chunk's offsets are reused by the next chunk
   }
   if (blockIdx.x == 0 && tid == 0) {
-    ws.hdr->n_dec_units = (int)min((int64_t)unit_carry, ws.max_units);
-    ws.hdr->n_pre_entries = (int)min((int64_t)pre_carry, ws.max_pre);
+    // A plan that does not fit the workspace runs nothing: entries past a
+    // capacity were not written and partial rows past it have no room, so
+    // the whole step is dropped (no output row is written) and reported.
+    // The host sizes the workspace so that this cannot happen.
+    const bool fits = (int64_t)unit_carry <= ws.max_units && (int64_t)pre_carry <= ws.max_pre &&
+                      (int64_t)pair_carry <= ws.max_pairs &&
+                      (int64_t)part_carry <= ws.max_part_rows;
+    if (!fits) atomicOr(ws.err, PKV_DEV_ERR_CAPACITY);
+    ws.hdr->n_dec_units = fits ? unit_carry : 0;
+    ws.hdr->n_pre_entries = fits ? pre_carry : 0;
     ws.hdr->dec_counter = 0;
     ws.hdr->pre_counter = 0;
     ws.hdr->chunk = chunk;
-    ws.hdr->n_pairs = (int)min((int64_t)pair_carry, ws.max_pairs);
+    ws.hdr->n_pairs = fits ? pair_carry : 0;
     ws.hdr->max_rows = s_max_rows;
   }
 }

@@ -1,8 +1,9 @@
 """pkv_attention_noalloc, the attention call for callers that cannot allocate
-device memory (code running under CUDA-graph capture, services with a fixed
-device-memory footprint, hosts whose allocator the library must not bypass).
-It keeps its scratch in a static device array instead of a cudaMalloc'd
-workspace; its results must match pkv_attention's.
+device memory (services with a device-memory footprint fixed at start-up,
+hosts whose own allocator the library must not bypass, loops that cannot take
+the synchronisation of a cudaMalloc).  It keeps its scratch in a static
+device array instead of a cudaMalloc'd workspace; its results must match
+pkv_attention's.
 
 This file is collected last on purpose: if it fails, a run that stops at
 the first failure has already run every other test."""
@@ -29,6 +30,21 @@ def test_refuses_a_batch_beyond_the_static_scratch():
                    i64, vp]
     rc = fn(FAKE, 4096, 4096, 32, FAKE, FAKE, 100000, 16, 8, 128, FAKE, FAKE, FAKE, 32768, 4096,
             0.088, FAKE, 4096, None)
+    assert rc == -2
+
+
+def test_refuses_kv_heads_beyond_the_unit_packing():
+    """Host-side check, as pkv_attention's: a decode unit packs the KV head in
+    16 bits, so num_kv_heads above 32767 is refused before any device work."""
+    lib = pkv.load()
+    fn = lib.pkv_attention_noalloc
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    fn.restype = ctypes.c_int
+    fn.argtypes = [vp, i64, i64, i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64, i32, f32, vp,
+                   i64, vp]
+    hkv = 65536
+    rc = fn(FAKE, hkv * 128, 1, hkv, FAKE, FAKE, 10, 16, hkv, 128, FAKE, FAKE, FAKE, 1, 1,
+            0.088, FAKE, hkv * 128, None)
     assert rc == -2
 
 
