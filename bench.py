@@ -11,9 +11,13 @@ per KV head, divided by the step time.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the float64 CPU oracle, same workload
 
-With N > 1 (launched by torchrun, one process per GPU) every rank runs its own
-replica of the batch (the step shards by request with no exchange), and the
-value is the total over ranks divided by the slowest rank's time.
+With N > 1 (launched by torchrun, one process per GPU; a plain
+``python bench.py --gpus N`` re-executes itself under torch.distributed.run)
+every rank runs its own replica of the batch (the step shards by request with
+no exchange), and the value is the total over ranks divided by the slowest
+rank's time.  On one GPU the line also carries ``extra_configs``: the other
+workloads (prefill, mixed, GQA and MQA decode, the trace step, and the int8
+cache lines), each timed the same way.
 """
 import argparse
 import datetime
@@ -234,6 +238,29 @@ def cpu_baseline_bounded(step, target_s=10.0):
     return cpu_baseline(step, sample_reqs=reqs, target_s=target_s)
 
 
+def l2_note(spec, int8):
+    """How the timed steps keep K/V reads in HBM (stated in the line's config)."""
+    n_copies = l2_copies(step_bytes(spec, 1 if int8 else 2))
+    sb_mb = step_bytes(spec, 1 if int8 else 2) / 1e6
+    if n_copies == 1:
+        return "inputs larger than L2 (%.0f MB touched per step vs 129 MB)" % sb_mb
+    return ("inputs larger than L2: %d copies of cache, qkv and output rotated, "
+            "%.1f MB touched per step, %.0f MB per rotation vs 129 MB"
+            % (n_copies, sb_mb, sb_mb * n_copies))
+
+
+def config_of(spec, kv_dtype, with_prepare, world):
+    """The workload a line measures; both arms print the same keys."""
+    int8 = kv_dtype == "int8"
+    return {"workload": spec.name, "requests": spec.num_reqs, "query_tokens": spec.num_tokens,
+            "step": ("prepare + " if with_prepare else "") + "write + attention",
+            "num_heads": spec.hq, "num_kv_heads": spec.hkv, "head_size": spec.head_size,
+            "block_size": spec.block_size,
+            "kv_bytes_per_step": spec.kv_bytes() // (2 if int8 else 1),
+            "kv_dtype": kv_dtype, "l2": l2_note(spec, int8),
+            "parallelism": "replica per GPU (dp%d)" % world}
+
+
 def run_reference(args, spec, rank):
     """--impl reference: the float64 CPU oracle as it stands, same workload."""
     if rank != 0:
@@ -247,25 +274,306 @@ def run_reference(args, spec, rank):
     sample = max(1, min(spec.num_reqs, int(8.0 / max(per_req, 1e-9))))
     for _ in range(args.warmup if args.warmup < 1 else 1):
         cpu_baseline(step, sample)
-    times, work = [], None
+    times = []
     for _ in range(args.steps):
-        r = cpu_baseline(step, sample)
-        times.append(r)
+        times.append(cpu_baseline(step, sample))
     vals = [t["value"] for t in times]
     value = statistics.median(vals)
     # a step here is the bounded sample: its wall time, median over the steps
     ms_step = statistics.median([t["seconds_per_pass"] for t in times]) * 1e3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     rec = {"metric": name, "value": value, "unit": unit, "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": spec.name, "requests_per_step": sample},
+           "config": config_of(spec, args.kv_dtype, args.with_prepare, world),
            "impl": "reference",
            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
-                            "kind": "oracle", "sample": times[-1]["sample"]},
+                            "kind": "oracle", "sample": times[-1]["sample"],
+                            "requests_per_step": sample},
            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(rec))
+
+
+def launch_check(args):
+    """--gpus N must run N ranks: under torchrun WORLD_SIZE has to equal N;
+    without it, N > 1 re-executes this script under torch.distributed.run
+    (one process per GPU on this node) after checking that N GPUs exist.
+    Returns only when this process is a rank of the right world."""
+    world = os.environ.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != args.gpus:
+            raise SystemExit("bench.py: --gpus %d but WORLD_SIZE=%s; launch one process per GPU"
+                             % (args.gpus, world))
+        return
+    if args.gpus == 1:
+        return
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be at least 1")
+    if args.impl == "ours":
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            raise SystemExit("bench.py: --gpus %d but %d CUDA device(s) visible" %
+                             (args.gpus, have))
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           "--nproc-per-node=%d" % args.gpus, "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    sys.stdout.flush()
+    os.execv(sys.executable, cmd)
+
+
+class Workload:
+    """Device buffers of one workload and its step: pkv_write + pkv_attention
+    (int8 caches: pkv_write_int8 + pkv_attention_int8), optionally preceded by
+    pkv_prepare_step.  Steps whose inputs fit in L2 rotate through copies of
+    the cache, the qkv rows and the output (same contents, same block ids), so
+    that every timed step reads its K/V from HBM as a serving step would."""
+
+    KS = VS = 0.03  # int8 scales: codes saturate beyond about 3.8 sigma
+
+    def __init__(self, spec, int8=False, with_prepare=False):
+        import torch
+        import paged_kv_attention_05_gb300 as pkv
+        self.pkv, self.torch = pkv, torch
+        self.spec, self.int8, self.with_prepare = spec, int8, with_prepare
+        self.step = step = W.build(spec)
+        s, d = spec, spec.head_size
+        rows = step.qkv.shape[0]
+        self.rows = rows
+        self.n_copies = l2_copies(step_bytes(s, 1 if int8 else 2))
+        qkv = self.dev(step.qkv)
+        self.qkv = qkv
+        self.qkvs = [self.split(t) for t in [qkv] + [qkv.clone() for _ in range(self.n_copies - 1)]]
+        self.slot_mapping = torch.from_numpy(step.slot_mapping).cuda()
+        self.qsl = torch.from_numpy(step.query_start_loc).cuda()
+        self.seq_lens = torch.from_numpy(step.seq_lens).cuda()
+        self.block_table = torch.from_numpy(step.block_table).cuda()
+        self.outs = [torch.empty((rows, s.hq, d), dtype=torch.bfloat16, device="cuda")
+                     for _ in range(self.n_copies)]
+        self.stream = torch.cuda.current_stream()
+        pkv.pkv_reserve_workspace(s.num_reqs, rows, step.block_table.shape[1], s.hq, s.hkv)
+        key_cache, value_cache = self.dev(step.key_cache), self.dev(step.value_cache)
+        if int8:
+            # the history as int8 codes, quantised once by the library's own write
+            nb = key_cache.shape[0]
+            kc8 = torch.empty(key_cache.shape, dtype=torch.int8, device="cuda")
+            vc8 = torch.empty_like(kc8)
+            all_slots = torch.arange(nb * s.block_size, dtype=torch.int64, device="cuda")
+            pkv.pkv_write_int8(key_cache.view(-1, s.hkv, d), value_cache.view(-1, s.hkv, d), kc8,
+                               vc8, all_slots, self.KS, self.VS)
+            pkv.pkv_get_error()
+            key_cache = value_cache = all_slots = None  # the bf16 history is no longer needed
+            self.caches = [(kc8, vc8)] + [(kc8.clone(), vc8.clone())
+                                          for _ in range(self.n_copies - 1)]
+        else:
+            self.caches = [(key_cache, value_cache)] + [
+                (key_cache.clone(), value_cache.clone()) for _ in range(self.n_copies - 1)]
+        if with_prepare:
+            self.num_computed = torch.tensor(s.ctx, dtype=torch.int32, device="cuda")
+            self.persistent_bt = self.block_table.clone()
+            self.positions = torch.empty(rows, dtype=torch.int64, device="cuda")
+
+    def dev(self, bits):
+        torch = self.torch
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    def split(self, t):
+        s, d, rows = self.spec, self.spec.head_size, self.rows
+        return (t[:, :s.hq * d].view(rows, s.hq, d),
+                t[:, s.hq * d:(s.hq + s.hkv) * d].view(rows, s.hkv, d),
+                t[:, (s.hq + s.hkv) * d:].view(rows, s.hkv, d))
+
+    def one_step(self, i=0):
+        pkv, s, st = self.pkv, self.spec, self.stream
+        c = i % self.n_copies
+        q, k, v = self.qkvs[c]
+        kc, vc = self.caches[c]
+        if self.with_prepare:
+            pkv.pkv_prepare_step(self.qsl, self.num_computed, self.persistent_bt, s.num_reqs,
+                                 self.rows, self.positions, self.seq_lens, self.slot_mapping,
+                                 self.block_table, stream=st)
+        if self.int8:
+            pkv.pkv_write_int8(k, v, kc, vc, self.slot_mapping, self.KS, self.VS, stream=st)
+            pkv.pkv_attention_int8(q, kc, vc, self.KS, self.VS, self.qsl, self.seq_lens,
+                                   self.block_table, s.num_reqs, s.scale, self.outs[c], stream=st)
+            return
+        pkv.pkv_write(k, v, kc, vc, self.slot_mapping, stream=st)
+        pkv.pkv_attention(q, kc, vc, self.qsl, self.seq_lens, self.block_table, s.num_reqs,
+                          s.scale, self.outs[c], stream=st)
+
+
+def time_steps(wl, steps, warmup, dist=None):
+    """W warm-up steps, then K timed steps (CUDA events on the launch stream,
+    barrier + synchronize on both sides, no per-launch events), then the same
+    K steps again with the library's per-launch trace events, then the same
+    steps for at least 0.6 s more so that the 200 ms clock samples see the
+    GPU under this load.  Returns (timed ms, launches in the timed region,
+    per-kernel trace, clocks)."""
+    torch, pkv, stream = wl.torch, wl.pkv, wl.stream
+    # the clock sampler starts before the warm-up, so that the GPU goes from
+    # the warm-up steps straight into the timed ones (no idle gap)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for i in range(max(warmup, 0)):
+        wl.one_step(i)
+    torch.cuda.synchronize()
+    bits = pkv.pkv_get_error()
+    if bits:
+        clocks.stop()
+        raise SystemExit("device error word %d after warm-up of %s" % (bits, wl.spec.name))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # the timed region: recording an event between two launches holds the
+    # next one back by a few microseconds, which lengthens short steps by up
+    # to a third, so only its two ends are recorded
+    launches0 = pkv.pkv_launch_count()
+    barrier()
+    t_load0 = time.time()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        wl.one_step(i)
+    e1.record(stream)
+    barrier()
+    launches = pkv.pkv_launch_count() - launches0
+    # the per-kernel durations behind the roofline
+    pkv.pkv_trace_read()
+    pkv.pkv_trace_enable(True)
+    barrier()
+    for i in range(steps):
+        wl.one_step(i)
+    barrier()
+    pkv.pkv_trace_enable(False)
+    trace = pkv.pkv_trace_read()
+    ms = e0.elapsed_time(e1)
+    per = max(1, int(0.05 / max(ms / steps / 1e3, 1e-6)))
+    i, t_soak = steps, time.time() + 0.6
+    while time.time() < t_soak:
+        for _ in range(per):
+            wl.one_step(i)
+            i += 1
+        torch.cuda.synchronize()
+    t_load1 = time.time()
+    if pkv.pkv_get_error():
+        clocks.stop()
+        raise SystemExit("device error word set while timing %s" % wl.spec.name)
+    return ms, launches, trace, clocks.stop(t_load0, t_load1)
+
+
+PREFILL_SOURCES = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu",
+                   "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
+                   "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh",
+                   "paged_kv_attention_05_gb300/csrc/pkv_combine.cuh"]
+
+
+def kernel_sources(kind, int8):
+    if kind == "prefill":
+        return PREFILL_SOURCES
+    kfile = "decode_i8" if (int8 and kind == "decode") else kind
+    return ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % kfile,
+            "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
+            "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
+
+
+def write_bytes(spec, int8):
+    """Algorithmic bytes of one cache-write launch: the new K and V rows read
+    (bf16) and stored (bf16, or int8 codes)."""
+    return 2 * spec.num_tokens * spec.hkv * spec.head_size * (2 + (1 if int8 else 2))
+
+
+def rooflines(spec, trace, int8, peaks):
+    """(dominant kernel's roofline, the cache write's roofline, the whole
+    step's floor), from the live per-launch durations."""
+    d = spec.head_size
+    kinds = {k: v for k, v in trace.items() if v[1] > 0}
+    dominant = max(kinds, key=lambda k: kinds[k][0]) if kinds else "decode"
+    dom_ms, dom_n = trace.get(dominant, (0.0, 0))
+    avg_ms = dom_ms / max(dom_n, 1)
+    if dominant == "prefill":
+        algo = causal_flops(spec)
+        peak = peaks.get("bf16_tflops")
+        roof = {"bound": "tensor", "achieved": algo / (avg_ms / 1e3) / 1e12,
+                "peak": peak, "unit": "TFLOP/s", "peak_source": "measured" if peak else None}
+    else:
+        algo = decode_algorithmic_bytes(spec, 1 if int8 else 2) if dominant == "decode" else \
+            write_bytes(spec, int8) if dominant == "write" else 0
+        peak = peaks.get("hbm_gbs")
+        roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
+                "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
+    if roof["peak"] is None:
+        roof["peak"] = 1900.0 if roof["unit"] == "TFLOP/s" else 6800.0
+        roof["peak_source"] = "fallback"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dominant
+    roof["avg_launch_ms"] = avg_ms
+    roof["traffic"] = profiled_traffic(dominant, spec.name + ("_int8" if int8 else ""),
+                                       kernel_sources(dominant, int8))
+    bw = peaks.get("hbm_gbs") or 6800.0
+    tf = peaks.get("bf16_tflops") or 1900.0
+    w_ms, w_n = trace.get("write", (0.0, 0))
+    wroof = None
+    if w_n:
+        w_avg = w_ms / w_n
+        wb = write_bytes(spec, int8)
+        wroof = {"bound": "hbm", "bytes": wb, "avg_launch_ms": w_avg,
+                 "achieved": wb / (w_avg / 1e3) / 1e9, "peak": bw, "unit": "GB/s",
+                 "frac": wb / (w_avg / 1e3) / 1e9 / bw,
+                 "traffic": profiled_traffic("write", spec.name + ("_int8" if int8 else ""),
+                                             kernel_sources("write", int8))}
+    # the whole step against its own floor: max(bytes / copy bandwidth,
+    # flops / bf16 peak), both algorithmic
+    sb, sf = step_bytes(spec, 1 if int8 else 2), causal_flops(spec)
+    floor_ms = max(sb / (bw * 1e9), sf / (tf * 1e12)) * 1e3
+    step_roof = {"bytes": sb, "flops": sf, "floor_ms": floor_ms,
+                 "bound": "hbm" if sb / (bw * 1e9) >= sf / (tf * 1e12) else "tensor"}
+    return roof, wroof, step_roof
+
+
+def metric_value(spec, int8, world, ms_per_step):
+    name, unit = metric_of(spec)
+    work = metric_work(spec)
+    if int8:  # one byte per cached element instead of two
+        name, work = name + " (int8 cache)", work / 2
+    return name, unit, work, whole_job_value(work, world, ms_per_step / 1e3)
+
+
+EXTRA_CONFIGS = [("large_prefill", "bf16"), ("mixed_chunked", "bf16"), ("gqa_decode", "bf16"),
+                 ("mqa_long_decode", "bf16"), ("tiny_mixed", "bf16"), ("mha_decode", "int8"),
+                 ("gqa_decode", "int8"), ("mqa_long_decode", "int8")]
+
+
+def measure_extra(name, kv_dtype, args, peaks):
+    """One extra workload, measured as the headline is (same timing, trace
+    and clock rules) without the end-to-end and CPU-baseline legs."""
+    import torch
+    spec = W.spec(name)
+    int8 = kv_dtype == "int8"
+    wl = Workload(spec, int8=int8)
+    ms, launches, trace, clk = time_steps(wl, args.steps, args.warmup)
+    del wl
+    torch.cuda.empty_cache()
+    ms_per_step = ms / args.steps
+    metric, unit, _, value = metric_value(spec, int8, 1, ms_per_step)
+    roof, wroof, step_roof = rooflines(spec, trace, int8, peaks)
+    step_roof["frac"] = step_roof["floor_ms"] / ms_per_step
+    return {"metric": metric, "value": value, "unit": unit, "ms_per_step": ms_per_step,
+            "dtype": "int8 cache, fp16 math" if int8 else "bf16",
+            "config": config_of(spec, kv_dtype, False, 1), "gpu_launches": int(launches),
+            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
+            "roofline": roof, "write_roofline": wroof, "step_roofline": step_roof,
+            "clocks": clk}
 
 
 def main():
@@ -277,6 +585,8 @@ def main():
     ap.add_argument("--config", default="mha_decode", choices=W.CONFIG_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip the other workloads (extra_configs of the line)")
     ap.add_argument("--with-prepare", action="store_true",
                     help="start each step with pkv_prepare_step (positions, seq_lens, slot "
                          "mapping and block table computed on the device)")
@@ -287,6 +597,7 @@ def main():
                     help="first N requests of the workload only, with a pool sized for them "
                          "(a small case of the same kernel shapes, e.g. for profiling)")
     args = ap.parse_args()
+    launch_check(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -303,142 +614,25 @@ def main():
         return
 
     import torch
-    import paged_kv_attention_05_gb300 as pkv
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    step = W.build(spec)
-    s = spec
-    d = s.head_size
-
-    def dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
-            torch.bfloat16).cuda()
-
-    rows = step.qkv.shape[0]
-    # Steps whose inputs fit in L2 rotate through copies of the cache, the
-    # qkv rows and the output (same contents, same block ids), so that every
-    # timed step reads its K/V from HBM as a serving step would.
-    n_copies = l2_copies(step_bytes(s, 1 if int8 else 2))
-
-    def split(t):
-        return (t[:, :s.hq * d].view(rows, s.hq, d),
-                t[:, s.hq * d:(s.hq + s.hkv) * d].view(rows, s.hkv, d),
-                t[:, (s.hq + s.hkv) * d:].view(rows, s.hkv, d))
-
-    qkv = dev(step.qkv)
-    qkvs = [split(t) for t in [qkv] + [qkv.clone() for _ in range(n_copies - 1)]]
-    slot_mapping = torch.from_numpy(step.slot_mapping).cuda()
-    qsl = torch.from_numpy(step.query_start_loc).cuda()
-    seq_lens = torch.from_numpy(step.seq_lens).cuda()
-    block_table = torch.from_numpy(step.block_table).cuda()
-    outs = [torch.empty((rows, s.hq, d), dtype=torch.bfloat16, device="cuda")
-            for _ in range(n_copies)]
-    out = outs[0]
-    stream = torch.cuda.current_stream()
-    pkv.pkv_reserve_workspace(s.num_reqs, rows, step.block_table.shape[1], s.hq, s.hkv)
-    KS, VS = 0.03, 0.03  # int8 scales: codes saturate beyond about 3.8 sigma
-    key_cache, value_cache = dev(step.key_cache), dev(step.value_cache)
-    if int8:
-        # the history as int8 codes, quantised once by the library's own write
-        nb = key_cache.shape[0]
-        kc8 = torch.empty(key_cache.shape, dtype=torch.int8, device="cuda")
-        vc8 = torch.empty_like(kc8)
-        all_slots = torch.arange(nb * s.block_size, dtype=torch.int64, device="cuda")
-        pkv.pkv_write_int8(key_cache.view(-1, s.hkv, d), value_cache.view(-1, s.hkv, d), kc8,
-                           vc8, all_slots, KS, VS)
-        pkv.pkv_get_error()
-        key_cache = value_cache = all_slots = None  # the bf16 history is no longer needed
-        caches = [(kc8, vc8)] + [(kc8.clone(), vc8.clone()) for _ in range(n_copies - 1)]
-    else:
-        caches = [(key_cache, value_cache)] + [(key_cache.clone(), value_cache.clone())
-                                               for _ in range(n_copies - 1)]
-
-    if args.with_prepare:
-        num_computed = torch.tensor(s.ctx, dtype=torch.int32, device="cuda")
-        persistent_bt = block_table.clone()
-        positions = torch.empty(rows, dtype=torch.int64, device="cuda")
-
-    def one_step(i=0):
-        c = i % n_copies
-        q, k, v = qkvs[c]
-        kc, vc = caches[c]
-        if args.with_prepare:
-            pkv.pkv_prepare_step(qsl, num_computed, persistent_bt, s.num_reqs, rows, positions,
-                                 seq_lens, slot_mapping, block_table, stream=stream)
-        if int8:
-            pkv.pkv_write_int8(k, v, kc, vc, slot_mapping, KS, VS, stream=stream)
-            pkv.pkv_attention_int8(q, kc, vc, KS, VS, qsl, seq_lens, block_table, s.num_reqs,
-                                   s.scale, outs[c], stream=stream)
-            return
-        pkv.pkv_write(k, v, kc, vc, slot_mapping, stream=stream)
-        pkv.pkv_attention(q, kc, vc, qsl, seq_lens, block_table, s.num_reqs,
-                          s.scale, outs[c], stream=stream)
-
-    # the clock sampler starts before the warm-up, so that the GPU goes from
-    # the warm-up steps straight into the timed ones (no idle gap)
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    for i in range(max(args.warmup, 0)):
-        one_step(i)
-    torch.cuda.synchronize()
-    bits = pkv.pkv_get_error()
-    if bits:
-        clocks.stop()
-        raise SystemExit("device error word %d after warm-up" % bits)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
+    wl = Workload(spec, int8=int8, with_prepare=args.with_prepare)
+    pkv, step, s, d = wl.pkv, wl.step, spec, spec.head_size
+    ms, launches, trace, clk = time_steps(wl, args.steps, args.warmup, dist)
+    ms = max_over_ranks(ms, dist, "cuda")
+    ms_per_step = ms / args.steps
+    name, unit, work, value = metric_value(spec, int8, world, ms_per_step)
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-
-    # The timed region: K steps, no per-launch events (recording an event
-    # between two launches holds the next one back by a few microseconds,
-    # which lengthens short steps by up to a third).
-    launches0 = pkv.pkv_launch_count()
-    barrier()
-    t_load0 = time.time()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        one_step(i)
-    e1.record(stream)
-    barrier()
-    launches = pkv.pkv_launch_count() - launches0
-    # The per-kernel durations behind the roofline: the same K steps again,
-    # with CUDA events recorded around each launch on its stream.
-    pkv.pkv_trace_read()
-    pkv.pkv_trace_enable(True)
-    barrier()
-    for i in range(args.steps):
-        one_step(i)
-    barrier()
-    pkv.pkv_trace_enable(False)
-    trace = pkv.pkv_trace_read()
-    # the same steps for at least 0.6 s more (untimed, in batches of about
-    # 50 ms), so that the 200 ms clock samples see the GPU under this load
-    # even when the timed region is shorter than one sampling period
-    ms = e0.elapsed_time(e1)
-    per = max(1, int(0.05 / max(ms / args.steps / 1e3, 1e-6)))
-    i, t_soak = args.steps, time.time() + 0.6
-    while time.time() < t_soak:
-        for _ in range(per):
-            one_step(i)
-            i += 1
-        torch.cuda.synchronize()
-    t_load1 = time.time()
-    clk = clocks.stop(t_load0, t_load1)
-    ms = max_over_ranks(ms, dist, "cuda")
-    ms_per_step = ms / args.steps
-    name, unit = metric_of(spec)
-    work = metric_work(spec)
-    if int8:  # one byte per cached element instead of two
-        name, work = name + " (int8 cache)", work / 2
-    value = whole_job_value(work, world, ms_per_step / 1e3)
 
     # end to end through the public API with host buffers, as a serving loop
     # runs it: every step's inputs (fused qkv and metadata) copied in from
@@ -448,6 +642,8 @@ def main():
     # shared cache sees each write before the next step's attention)
     e2e = None
     if not args.no_e2e:
+        rows, stream = wl.rows, wl.stream
+        KS, VS = wl.KS, wl.VS
         h_qkv = torch.from_numpy(step.qkv.view(np.int16)).pin_memory()
         h_slots = torch.from_numpy(step.slot_mapping).pin_memory()
         h_qsl = torch.from_numpy(step.query_start_loc).pin_memory()
@@ -459,14 +655,16 @@ def main():
         d2h = h_out[0].numel() * h_out[0].element_size()
         sets = []
         for _ in range(2):
-            b_qkv = torch.empty_like(qkv)
+            b_qkv = torch.empty_like(wl.qkv)
             sets.append({"qkv": b_qkv,
                          "q": b_qkv[:, :s.hq * d].view(rows, s.hq, d),
                          "k": b_qkv[:, s.hq * d:(s.hq + s.hkv) * d].view(rows, s.hkv, d),
                          "v": b_qkv[:, (s.hq + s.hkv) * d:].view(rows, s.hkv, d),
-                         "slots": torch.empty_like(slot_mapping), "qsl": torch.empty_like(qsl),
-                         "sl": torch.empty_like(seq_lens), "bt": torch.empty_like(block_table),
-                         "out": torch.empty_like(out)})
+                         "slots": torch.empty_like(wl.slot_mapping),
+                         "qsl": torch.empty_like(wl.qsl),
+                         "sl": torch.empty_like(wl.seq_lens),
+                         "bt": torch.empty_like(wl.block_table),
+                         "out": torch.empty_like(wl.outs[0])})
         up, down = torch.cuda.Stream(), torch.cuda.Stream()
         ev = {n: [torch.cuda.Event() for _ in range(2)]
               for n in ("in_ready", "in_free", "out_ready", "out_free")}
@@ -484,7 +682,7 @@ def main():
 
         def compute(i):
             b, j = sets[i % 2], i % 2
-            kc, vc = caches[i % n_copies]
+            kc, vc = wl.caches[i % wl.n_copies]
             stream.wait_event(ev["in_ready"][j])
             stream.wait_event(ev["out_free"][j])  # step i-2's output is read back
             if int8:
@@ -525,77 +723,34 @@ def main():
                "ms_per_step": e2e_s * 1e3,
                "overlap": "double-buffered: step i+1's upload and step i-1's download on "
                           "copy streams during step i's kernels"}
+        if pkv.pkv_get_error():
+            raise SystemExit("device error word set in the end-to-end loop")
 
-    # roofline of the dominant kernel, from its live CUDA-event durations
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    peaks = json.load(open(peaks_path)) if os.path.exists(peaks_path) else {}
-    kinds = {k: v for k, v in trace.items() if v[1] > 0}
-    dominant = max(kinds, key=lambda k: kinds[k][0]) if kinds else "decode"
-    dom_ms, dom_n = trace.get(dominant, (0.0, 0))
-    avg_ms = dom_ms / max(dom_n, 1)
-    if dominant == "prefill":
-        algo = causal_flops(spec)
-        peak = peaks.get("bf16_tflops")
-        roof = {"bound": "tensor", "achieved": algo / (avg_ms / 1e3) / 1e12,
-                "peak": peak, "unit": "TFLOP/s", "peak_source": "measured" if peak else None}
-        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_prefill.cu",
-                "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
-                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh",
-                "paged_kv_attention_05_gb300/csrc/pkv_combine.cuh"]
-    else:
-        algo = decode_algorithmic_bytes(spec, 1 if int8 else 2) if dominant == "decode" else \
-            2 * s.num_tokens * s.hkv * d * 2 * (1.5 if int8 else 2)
-        peak = peaks.get("hbm_gbs")
-        roof = {"bound": "hbm", "achieved": algo / (avg_ms / 1e3) / 1e9,
-                "peak": peak, "unit": "GB/s", "peak_source": "measured" if peak else None}
-        kfile = "decode_i8" if (int8 and dominant == "decode") else dominant
-        srcs = ["paged_kv_attention_05_gb300/csrc/pkv_%s.cu" % kfile,
-                "paged_kv_attention_05_gb300/csrc/pkv_device.cuh",
-                "paged_kv_attention_05_gb300/csrc/pkv_internal.cuh"]
-    if roof["peak"] is None:
-        roof["peak"] = 1900.0 if roof["unit"] == "TFLOP/s" else 6800.0
-        roof["peak_source"] = "fallback"
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = dominant
-    roof["avg_launch_ms"] = avg_ms
-    traffic = profiled_traffic(dominant, spec.name + ("_int8" if int8 else ""), srcs)
-    roof["traffic"] = traffic
-    # the whole step against its own floor: max(bytes / copy bandwidth,
-    # flops / bf16 peak), both algorithmic
-    sb, sf = step_bytes(spec, 1 if int8 else 2), causal_flops(spec)
-    bw = peaks.get("hbm_gbs") or 6800.0
-    tf = peaks.get("bf16_tflops") or 1900.0
-    floor_ms = max(sb / (bw * 1e9), sf / (tf * 1e12)) * 1e3
-    step_roof = {"bytes": sb, "flops": sf, "floor_ms": floor_ms,
-                 "bound": "hbm" if sb / (bw * 1e9) >= sf / (tf * 1e12) else "tensor",
-                 "frac": floor_ms / ms_per_step}
-
-    sb_mb = step_bytes(s, 1 if int8 else 2) / 1e6
-    if n_copies == 1:
-        l2_note = "inputs larger than L2 (%.0f MB touched per step vs 129 MB)" % sb_mb
-    else:
-        l2_note = ("inputs larger than L2: %d copies of cache, qkv and output rotated, "
-                   "%.1f MB touched per step, %.0f MB per rotation vs 129 MB"
-                   % (n_copies, sb_mb, sb_mb * n_copies))
+    roof, wroof, step_roof = rooflines(spec, trace, int8, peaks)
+    step_roof["frac"] = step_roof["floor_ms"] / ms_per_step
     rec = {"metric": name, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
            "dtype": "int8 cache, fp16 math" if int8 else "bf16", "data": "synthetic",
-           "config": {"workload": spec.name, "requests": s.num_reqs, "query_tokens": s.num_tokens,
-                      "step": ("prepare + " if args.with_prepare else "") + "write + attention",
-                      "num_heads": s.hq, "num_kv_heads": s.hkv, "head_size": d,
-                      "block_size": s.block_size,
-                      "kv_bytes_per_step": s.kv_bytes() // (2 if int8 else 1),
-                      "kv_dtype": args.kv_dtype,
-                      "l2": l2_note,
-                      "parallelism": "replica per GPU (dp%d)" % world},
+           "config": config_of(spec, args.kv_dtype, args.with_prepare, world),
            "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
            "kernel_ms": {k: v[0] / max(v[1], 1) for k, v in trace.items() if v[1]},
            "kernel_timing": "CUDA events around each launch, in a second pass of the same K "
                             "steps right after the timed one (which records none)",
-           "roofline": roof, "step_roofline": step_roof}
+           "roofline": roof, "write_roofline": wroof, "step_roofline": step_roof}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not int8:
         rec["cpu_baseline"] = cpu_baseline_bounded(step)
+    # the other workloads, each timed as the headline is (one GPU only: the
+    # scaling runs carry the headline alone)
+    if world == 1 and not args.no_extra_configs and not args.reqs:
+        del wl, step
+        torch.cuda.empty_cache()
+        extra = {}
+        for nm, kvd in EXTRA_CONFIGS:
+            if nm == spec.name and kvd == args.kv_dtype:
+                continue
+            extra[nm if kvd == "bf16" else nm + "_int8"] = measure_extra(nm, kvd, args, peaks)
+        rec["extra_configs"] = extra
     if rank == 0:
         print(json.dumps(rec))
     if dist is not None:

@@ -131,6 +131,30 @@ def test_large_prefill_sampled_rows():
     assert np.isfinite(got).all()
 
 
+def test_large_prefill_one_whole_request():
+    """The full large_prefill step (8 prompts of 2048 tokens, Hq 64 / Hkv 8,
+    causal) on the GPU, and one of its requests compared element by element:
+    all 2048 rows x 64 heads x 128 columns, i.e. every query tile, every
+    head pair and every diagonal key tile of the launch's geometry."""
+    step = W.build(W.spec("large_prefill"))
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()
+    assert pkv.pkv_get_error() == 0
+    got = ds.out_f64()
+    r = 5
+    qsl = step.query_start_loc
+    q0, q1 = int(qsl[r]), int(qsl[r + 1])
+    sub_qsl = np.array([q0, q1], dtype=np.int32)
+    ref, err = oracle.attention(step.q, kc, vc, sub_qsl, step.seq_lens[r:r + 1],
+                                step.block_table[r:r + 1], 1, step.scale)
+    assert err == 0
+    assert_close(got[q0:q1], ref[q0:q1], "large_prefill request %d" % r)
+    assert np.isfinite(got).all()
+
+
 def test_prefill_scores_growing_along_the_keys():
     """Scores that rise steadily along the keys (by about 2^8 in the log2
     domain every 128 keys): the running maximum grows past the rescale

@@ -52,3 +52,27 @@ def test_two_ranks_take_the_slowest_time_and_sum_the_work():
     for rank, t, v in res:
         assert t == 2.0
         assert v == pytest.approx(2 * work / 2.0)
+
+
+def _bench_run(args, env_extra):
+    import subprocess
+    env = dict(os.environ)
+    env.pop("WORLD_SIZE", None)
+    env.update(env_extra)
+    env["CUDA_VISIBLE_DEVICES"] = ""          # no GPU: the refusal must come first
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, env=env,
+                          capture_output=True, text=True, timeout=300)
+
+
+def test_bench_refuses_a_world_size_other_than_gpus():
+    r = _bench_run(["--gpus", "2", "--steps", "1", "--warmup", "1"], {"WORLD_SIZE": "3"})
+    assert r.returncode != 0
+    assert "WORLD_SIZE=3" in r.stderr
+    assert '"n_gpus"' not in r.stdout
+
+
+def test_bench_with_more_gpus_than_visible_never_prints_a_one_gpu_line():
+    r = _bench_run(["--gpus", "2", "--steps", "1", "--warmup", "1"], {})
+    assert r.returncode != 0
+    assert "CUDA device" in r.stderr
+    assert '"n_gpus"' not in r.stdout
