@@ -38,6 +38,24 @@ def test_prefill_single_tile_and_ragged(hq, hkv):
     run_and_check(step, "prefill hq=%d hkv=%d" % (hq, hkv))
 
 
+def test_prefill_odd_group_single_head_items():
+    """Hq / Hkv = 3: every work item carries one query tile, and the second
+    tile's softmax warps stand by; prompts of several key tiles and a chunk
+    after a cached context."""
+    step = W.build(W.custom([0, 300, 0], [700, 150, 65], 12, 4, seed=303))
+    run_and_check(step, "odd group")
+
+
+def test_prefill_many_one_tile_items():
+    """Two hundred short prompts (17 to 60 rows, one 64-key tile each): the
+    score cursor of the MMA issuer runs up to two items ahead of P.V, across
+    item boundaries, through the four-slot item ring and both Q buffers."""
+    rng = np.random.default_rng(17)
+    n = rng.integers(17, 61, 200).tolist()
+    step = W.build(W.custom([0] * 200, n, 2, 2, seed=1717, pad_tokens=1))
+    run_and_check(step, "one-tile items")
+
+
 def test_prefill_many_query_and_key_tiles():
     step = W.build(W.custom([0, 0], [300, 513], 4, 2, seed=12))
     run_and_check(step, "multi-tile prefill")
