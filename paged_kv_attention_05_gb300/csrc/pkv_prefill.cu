@@ -14,33 +14,30 @@
 //
 // GB300 design.  A work item is a 128-row query tile of one request for two
 // query heads of the same KV head (one head when Hq / Hkv is odd): tiles "a"
-// and "b" share every K/V tile.  Keys are taken 64 at a time.  Tensor memory
-// (512 columns) holds each query tile's output O (128 columns) and two score
-// buffers S[0], S[1] (64 columns each): while the softmax works on the scores
-// of key tile j, the tensor cores already hold those of tile j + 1 and compute
-// P.V of tile j - 1 and S of tile j + 1's successor, so a query tile's chain
-// (scores -> softmax -> P.V) never waits for its own next scores.  A
-// persistent grid (one CTA per SM) takes items from an atomic cursor, longest
-// first, and treats the key tiles of consecutive items as one stream.  Roles:
-//   warp 0      K producer: publishes items in a four-slot ring, loads the
-//               two Q tiles of an item by TMA into one of two Q buffers, and
-//               the K tiles (4 pages, one 16-slot x 64-dim box per page and
-//               half, 128-byte swizzle) into a 3-stage ring;
-//   warp 14     V producer: the V tiles into a 2-stage ring; in a request's
-//               last tile it zero-fills the V rows of keys past seq_len so
-//               that no stale value (NaN) reaches P.V;
-//   warp 1      allocates TMEM and issues every MMA from one thread: S_x(g) =
-//               Q_x K_g^T into S_x[g % 2] as soon as P.V of tile g - 2 (which
-//               read that buffer) is issued, and O_x += P_x(g) V_g with P
-//               taken from TMEM (the scores' first 32 columns, overwritten
-//               with bf16 probabilities) and V from shared memory (MN-major);
-//               tcgen05.commit drives the mbarriers;
-//   warps 2-9   softmax, one warp per (query tile, TMEM lane quarter), one
-//               query row per thread: scores -> causal/length mask (only on
-//               tiles that cross the diagonal) -> running max in the log2
-//               domain -> exp2 -> row sum -> bf16 P back into TMEM.  O is
-//               rescaled in TMEM only when a row's max grows by more than 2^8
-//               (exact, rare), after P.V of the previous tile is complete;
+// and "b" share every K/V tile.  A persistent grid (one CTA per SM, all 512
+// TMEM columns) takes items from an atomic cursor, longest first.  Roles:
+//   warp 0      producer: publishes the item in a two-slot ring, loads the two
+//               Q tiles by TMA as soon as the previous item's last S = Q K^T
+//               has consumed them, then the K and V tiles of 128 keys (8 pages
+//               each, one 16-slot x 64-dim box per page and half, 128-byte
+//               swizzle) into a 2-stage ring, K and V released separately; in
+//               a request's last tile it zero-fills the V rows of keys past
+//               seq_len so that no stale value (NaN) reaches P.V;
+//   warp 1      allocates TMEM and issues every MMA from one thread, in the
+//               order S_a(0) S_b(0) | PV_a(j) S_a(j+1) PV_b(j) S_b(j+1) ...:
+//               S into TMEM, P taken from TMEM (the scores' columns,
+//               overwritten with bf16 probabilities) and V from shared memory
+//               (MN-major), O accumulating in TMEM; tcgen05.commit drives the
+//               mbarriers.  Because one thread's MMAs complete in order, S(j+1)
+//               being ready also means PV(j) is done;
+//   warps 2-9   softmax, two warps per row quarter (one per 64-key half of
+//               the scores), one query row per thread (TMEM lane = 32 *
+//               (warp % 4) + lane = row), both query tiles in turn: scores ->
+//               causal/length mask (only on tiles that cross the diagonal) ->
+//               running max in the log2 domain -> exp2 -> row sum -> bf16 P
+//               back into TMEM.  O is rescaled in TMEM only when a row's max
+//               grows by more than 2^8 (exact, rare).  At the end of an item
+//               each warp leaves its partial row sums in shared memory;
 //   warps 10-13 epilogue: once O_x is final, read it out of TMEM in two
 //               64-column halves, divide by the row sum, release O_x to the
 //               next item's first P.V and write the bf16 rows to global memory
@@ -55,55 +52,50 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 480;                     // 15 warps
-constexpr int kTileK = 64;                        // keys per KV tile
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
-constexpr int kItemSlots = 4;
-constexpr int kQHalf = 128 * 128;                 // 128 query rows x 64 bf16
-constexpr int kQTile = 2 * kQHalf;                // 32 KB
-constexpr int kKVHalf = kTileK * 128;             // 64 keys x 64 bf16
-constexpr int kKVTile = 2 * kKVHalf;              // 16 KB
+constexpr int kThreads = 448;                     // 14 warps
+constexpr int kStages = 2;
+constexpr int kTileK = 128;                       // keys per KV tile
+constexpr int kHalfBytes = 128 * 128;             // 128 rows x 64 bf16
+constexpr int kTileBytes = 2 * kHalfBytes;        // a Q, K or V tile: 32 KB
 constexpr int kPageBoxBytes = 16 * 128;           // one 16-slot x 64-dim box
 constexpr int kTmemCols = 512;
-constexpr int kColS = 256;                        // S_x[p] at kColS + 128 x + 64 p; O_x at 128 x
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                          // Q(x, buffer b) at kOffQ + (2 x + b) kQTile
-constexpr int kOffK = kOffQ + 4 * kQTile;
-constexpr int kOffV = kOffK + kKStages * kKVTile;
+constexpr int kOffQ = 0;                          // Q_a | Q_b
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kStageWarp = 32 * 64;               // epilogue staging: 32 rows x 64 bytes
-constexpr int kOffStage = kOffV + kVStages * kKVTile;  // one staging area per epilogue warp
-constexpr int kOffLsum = kOffStage + 4 * kStageWarp;   // [item slot][tile][128 rows] floats
-constexpr int kOffBar = kOffLsum + kItemSlots * 2 * 128 * 4;
+constexpr int kOffStage = kOffV + kStages * kTileBytes;  // one staging area per epilogue warp
+constexpr int kOffLsum = kOffStage + 4 * kStageWarp;  // [2 items][2 tiles][2 halves][128 rows]
+constexpr int kOffBar = kOffLsum + 2 * 2 * 2 * 128 * 4;
 enum {
-  B_QF = 0,   // [2 x + b] Q tile loaded
-  B_QE = 4,   // [2 x + b] Q buffer read by the item's last S
-  B_KF = 8,   // [3] K stage loaded
-  B_KE = 11,  // [3] K stage free
-  B_VF = 14,  // [2] V stage ready
-  B_VT = 16,  // [2] V stage loaded (tail tiles: before the zero fill)
-  B_VE = 18,  // [2] V stage free
-  B_SF = 20,  // [2 x + p] S_x[p] ready
-  B_PF = 24,  // [2 x + p] P_x written into S_x[p]
-  B_PD = 28,  // [x] a P.V into O_x complete
-  B_OF = 30,  // [x] O_x final for the item
-  B_OE = 32,  // [x] O_x read by the epilogue
-  B_IF = 34,  // [slot] item published
-  B_IE = 38,  // [slot] item released by every role
-  B_LF = 42,  // [4 x + slot] row sums of tile x written for the epilogue
-  kNumBars = 50
+  B_QF = 0,   // [2] Q tile loaded
+  B_QE = 2,   // [2] Q tile consumed by the item's last S
+  B_KF = 4,   // [2] K stage loaded
+  B_KE = 6,   // [2] K stage free
+  B_VF = 8,   // [2] V stage ready
+  B_VT = 10,  // [2] V stage loaded (tail tiles: before the zero fill)
+  B_VE = 12,  // [2] V stage free
+  B_SF = 14,  // [2] S_x ready
+  B_PF = 16,  // [2] P_x written
+  B_OF = 18,  // [2] O_x final for the item
+  B_OE = 20,  // [2] O_x read by the epilogue
+  B_IF = 22,  // [2] item slot published
+  B_IE = 24,  // [2] item slot released
+  B_XP = 26,  // [4] exchange between the two softmax warps of a row quarter
+  B_LF = 30,  // [2] row sums of tile x written for the epilogue
+  kNumBars = 32
 };
-constexpr int kOffItems = kOffBar + kNumBars * 8;           // kItemSlots items
-constexpr int kOffCtl = kOffItems + kItemSlots * 48;        // TMEM address, abort flag
-constexpr int kSmemBytes = kOffCtl + 16 + 1024;             // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 item slots
+constexpr int kOffXch = kOffItems + 2 * 48;        // [4 quarters][2 slots][2 halves][32] floats
+constexpr int kOffCtl = kOffXch + 4 * 2 * 2 * 32 * 4;  // TMEM address, abort flag
+constexpr int kSmemBytes = kOffCtl + 16 + 1024;    // + alignment slack
 
 struct Item {
   int r, qt, ha, hb;  // hb < 0: single-tile item
   int g, q0, n, L;
-  int ctx, nkv, pad0, pad1;  // nkv: 64-key tiles the item reads
+  int ctx, nkv, pad0, pad1;
 };
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -125,13 +117,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n, bool b_mn_major) {
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = N = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
   return (1u << 4)                         // D format f32
          | (1u << 7)                       // A format bf16
          | (1u << 10)                      // B format bf16
          | ((b_mn_major ? 1u : 0u) << 16)  // B major-ness
-         | ((n >> 3) << 17)                // N
+         | ((128u >> 3) << 17)             // N
          | ((128u >> 4) << 24);            // M
 }
 
@@ -236,21 +228,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + kOffCtl);
   volatile int* abort = ctl + 1;  // ctl[0] = TMEM base address
   Item* items = reinterpret_cast<Item*>(smem + kOffItems);
-  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.hq / a.hkv;
   const bool pairs = (G % 2) == 0;  // two heads of one KV head per item
-  const int nx = pairs ? 2 : 1;
   const int per_entry = pairs ? a.hq / 2 : a.hq;
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(bar(B_PF + i), 4);  // the four softmax warps of a tile
-    for (int x = 0; x < 2; ++x) mbar_init(bar(B_OE + x), 4);  // the four epilogue warps
-    for (int i = 0; i < 8; ++i) mbar_init(bar(B_LF + i), 4);  // the four softmax warps of a tile
-    // MMA warp, 8 softmax warps, 4 epilogue warps, V producer
-    for (int i = 0; i < kItemSlots; ++i) mbar_init(bar(B_IE + i), 1 + 8 + 4 + 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(B_PF + x), 8);  // one arrival per softmax warp (each writes half of P)
+      mbar_init(bar(B_OE + x), 4);  // one arrival per epilogue warp
+      mbar_init(bar(B_LF + x), 8);  // one arrival per softmax warp
+      mbar_init(bar(B_IE + x), 1 + 8 + 4);  // MMA warp, softmax warps, epilogue warps
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_XP + i), 2);
     ctl[1] = 0;
     fence_barrier_init();
   }
@@ -266,34 +258,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = (uint32_t)ctl[0];
   const int n_items = ws.hdr->n_pre_entries * per_entry;
 
-  // the item in ring slot n & 3, once published (every role reads it this way)
-  auto take_item = [&](uint32_t n, Item* it) -> bool {
-    if (!mbar_wait_warp(bar(B_IF + (n & 3)), (n >> 2) & 1, abort, ws.err)) return false;
-    *it = items[n & 3];
-    __syncwarp();
-    return true;
-  };
-  // pages of key tile j of an item, and whether it holds keys past seq_len
-  auto tile_pages = [&](const Item& it, int j) { return min(4, (it.L - j * kTileK + 15) / 16); };
-
   if (warp == 0) {
-    // ------------------------------ K producer ------------------------------
+    // ------------------------------ producer ------------------------------
     // Global loads are issued one step before their values are needed: the
     // next item's cursor and entry (which carries its request's lengths)
-    // while the current item is being loaded, and each tile's block ids one
+    // while the current item is being issued, and each tile's block ids one
     // tile ahead; a load only stalls at its first use.
-    uint32_t g = 0;  // K tiles loaded (all items)
+    uint32_t tile_cnt = 0, vt_uses[kStages] = {0, 0}, qx_cnt[2] = {0, 0};
     int w_nxt = 0;
     if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
     w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
     const PreEntry none{-1, 0, 0, 0, 0, 0, 0, 0};
     PreEntry e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
     for (uint32_t it_cnt = 0;; ++it_cnt) {
-      const int slot = it_cnt & 3;
+      const int slot = it_cnt & 1;
       const int w = w_nxt;
       const PreEntry e = e_nxt;
-      if (it_cnt >= kItemSlots &&
-          !mbar_wait_warp(bar(B_IE + slot), ((it_cnt >> 2) - 1) & 1, abort, ws.err))
+      const int q0 = e.q0, q1 = e.q0 + e.n, Lr = e.L;
+      if (it_cnt >= 2 &&
+          !mbar_wait_warp(bar(B_IE + slot), ((it_cnt >> 1) - 1) & 1, abort, ws.err))
         break;
       if (w >= n_items || *abort) {
         if (lane == 0) {
@@ -307,15 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hp = w % per_entry;
         it.r = e.r;
         it.qt = e.qt;
+        it.nkv = e.nkv;
         it.ha = pairs ? 2 * hp : hp;
         it.hb = pairs ? 2 * hp + 1 : -1;
         it.g = it.ha / G;
-        it.q0 = e.q0;
-        it.n = e.n;
-        it.L = e.L;
-        it.ctx = e.L - e.n;
-        const int last_row = min(kPreTileQ * (e.qt + 1), e.n);
-        it.nkv = (it.ctx + last_row + kTileK - 1) / kTileK;
+        it.q0 = q0;
+        it.n = q1 - q0;
+        it.L = Lr;
+        it.ctx = Lr - it.n;
         it.pad0 = it.pad1 = 0;
       }
       if (lane == 0) {
@@ -328,34 +310,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
       const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
       const int row0 = it.q0 + it.qt * kPreTileQ;
-      // Q tiles into buffer it_cnt & 1, once the item before last has read it
-      const int qb = it_cnt & 1;
+      // Q tiles, once the previous item's last S has read them
       bool ok = true;
-      for (int x = 0; x < nx && ok; ++x) {
+      for (int x = 0; x < 2 && ok; ++x) {
         const int h = x == 0 ? it.ha : it.hb;
-        if (it_cnt >= 2 &&
-            !mbar_wait_warp(bar(B_QE + 2 * x + qb), ((it_cnt >> 1) - 1) & 1, abort, ws.err)) {
+        if (h < 0) continue;
+        if (qx_cnt[x] > 0 &&
+            !mbar_wait_warp(bar(B_QE + x), (qx_cnt[x] - 1) & 1, abort, ws.err)) {
           ok = false;
           break;
         }
+        qx_cnt[x]++;
         if (lane == 0) {
-          const uint32_t qd = sbase + kOffQ + (2 * x + qb) * kQTile;
-          mbar_expect_tx(bar(B_QF + 2 * x + qb), kQTile);
-          tma_load_3d(qd, &tm_q, bar(B_QF + 2 * x + qb), 0, h, row0);
-          tma_load_3d(qd + kQHalf, &tm_q, bar(B_QF + 2 * x + qb), 64, h, row0);
+          const uint32_t qd = sbase + kOffQ + x * kTileBytes;
+          mbar_expect_tx(bar(B_QF + x), kTileBytes);
+          tma_load_3d(qd, &tm_q, bar(B_QF + x), 0, h, row0);
+          tma_load_3d(qd + kHalfBytes, &tm_q, bar(B_QF + x), 64, h, row0);
         }
       }
       // lane p < pages(j) holds the block id of page p of tile j
-      int blk_nxt = lane < tile_pages(it, 0) ? __ldg(btrow + lane) : 0;
+      auto tile_pages = [&](int j) { return min(8, (it.L - j * kTileK + 15) / 16); };
+      int blk_nxt = lane < tile_pages(0) ? __ldg(btrow + lane) : 0;
       for (int j = 0; ok && j < it.nkv; ++j) {
-        const uint32_t c = g++;
-        const int s = c % kKStages;
-        const int pages = tile_pages(it, j);
+        const uint32_t c = tile_cnt++;
+        const int s = c % kStages;
+        const int key0 = j * kTileK;
+        const int pages = tile_pages(j);
+        const bool tail = key0 + kTileK > it.L;
         int blk = blk_nxt;
-        if (j + 1 < it.nkv && lane < tile_pages(it, j + 1))
-          blk_nxt = __ldg(btrow + (((j + 1) * kTileK) >> 4) + lane);
-        if (c >= (uint32_t)kKStages &&
-            !mbar_wait_warp(bar(B_KE + s), ((c / kKStages) - 1) & 1, abort, ws.err)) {
+        if (j + 1 < it.nkv && lane < tile_pages(j + 1))
+          blk_nxt = __ldg(btrow + ((key0 + kTileK) >> 4) + lane);
+        if (c >= (uint32_t)kStages &&
+            !mbar_wait_warp(bar(B_KE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
           ok = false;
           break;
         }
@@ -363,48 +349,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
           blk = 0;
         }
-        const uint32_t kdst = sbase + kOffK + s * kKVTile;
+        const uint32_t kdst = sbase + kOffK + s * kTileBytes;
         if (lane == 0) mbar_expect_tx(bar(B_KF + s), pages * 2 * kPageBoxBytes);
         __syncwarp();
         if (lane < pages) {
           tma_load_4d(kdst + lane * kPageBoxBytes, &tm_k, bar(B_KF + s), 0, it.g, 0, blk);
-          tma_load_4d(kdst + kKVHalf + lane * kPageBoxBytes, &tm_k, bar(B_KF + s), 64, it.g, 0,
-                      blk);
+          tma_load_4d(kdst + kHalfBytes + lane * kPageBoxBytes, &tm_k, bar(B_KF + s), 64, it.g,
+                      0, blk);
         }
-      }
-      if (!ok) break;
-    }
-  } else if (warp == 14) {
-    // ------------------------------ V producer ------------------------------
-    uint32_t g = 0, vt_uses[kVStages] = {0, 0};
-    for (uint32_t it_cnt = 0;; ++it_cnt) {
-      Item it;
-      if (!take_item(it_cnt, &it) || it.r < 0) break;
-      const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
-      bool ok = true;
-      int blk_nxt = lane < tile_pages(it, 0) ? __ldg(btrow + lane) : 0;
-      for (int j = 0; j < it.nkv; ++j) {
-        const uint32_t c = g++;
-        const int s = c % kVStages;
-        const int key0 = j * kTileK;
-        const int pages = tile_pages(it, j);
-        const bool tail = key0 + kTileK > it.L;
-        int blk = blk_nxt;
-        if (j + 1 < it.nkv && lane < tile_pages(it, j + 1))
-          blk_nxt = __ldg(btrow + ((key0 + kTileK) >> 4) + lane);
-        if (c >= (uint32_t)kVStages &&
-            !mbar_wait_warp(bar(B_VE + s), ((c / kVStages) - 1) & 1, abort, ws.err)) {
+        if (c >= (uint32_t)kStages &&
+            !mbar_wait_warp(bar(B_VE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
           ok = false;
           break;
         }
-        if (lane < pages && (blk < 0 || (int64_t)blk >= a.num_blocks)) blk = 0;  // (K reports it)
-        const uint32_t vdst = sbase + kOffV + s * kKVTile;
+        const uint32_t vdst = sbase + kOffV + s * kTileBytes;
         const uint32_t vbar = tail ? bar(B_VT + s) : bar(B_VF + s);
         if (lane == 0) mbar_expect_tx(vbar, pages * 2 * kPageBoxBytes);
         __syncwarp();
         if (lane < pages) {
           tma_load_4d(vdst + lane * kPageBoxBytes, &tm_v, vbar, 0, it.g, 0, blk);
-          tma_load_4d(vdst + kKVHalf + lane * kPageBoxBytes, &tm_v, vbar, 64, it.g, 0, blk);
+          tma_load_4d(vdst + kHalfBytes + lane * kPageBoxBytes, &tm_v, vbar, 64, it.g, 0, blk);
         }
         if (tail) {
           // wait for the V boxes, zero the rows of keys >= seq_len, publish
@@ -412,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           vt_uses[s]++;
           if (!ok) break;
           const int z0 = it.L - key0;
-          uint8_t* v = smem + kOffV + s * kKVTile;
+          uint8_t* v = smem + kOffV + s * kTileBytes;
           for (int i = lane; i < (kTileK - z0) * 16; i += 32) {
             const int row = z0 + (i >> 4), within = i & 15;
-            *reinterpret_cast<uint4*>(v + (within >> 3) * kKVHalf + row * 128 +
+            *reinterpret_cast<uint4*>(v + (within >> 3) * kHalfBytes + row * 128 +
                                       (within & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_async_smem();
@@ -424,265 +388,290 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) mbar_arrive(bar(B_IE + (it_cnt & 3)));
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // (the whole warp runs this, in step; see mma_ss)  Two cursors over the
-    // stream of key tiles g of consecutive items: P.V of tile g_p, and S of
-    // tile g_s <= g_p + 1 (S of tile g overwrites the buffer P.V of tile
-    // g - 2 read, so it is issued after that P.V; one thread's MMAs run in
-    // order).
-    const uint32_t id_s = idesc_bf16(kTileK, false), id_o = idesc_bf16(128, true);
-    // Operand descriptors of the first buffer of each kind, built once: a
-    // descriptor's low field is the address / 16, so other buffers and
-    // k-steps add their offset / 16.
-    const uint64_t dq = sdesc(sbase + kOffQ, 16);
-    const uint64_t dk = sdesc(sbase + kOffK, 16);
-    const uint64_t dv = sdesc(sbase + kOffV, kKVHalf);
-    // S_x(g) = Q_x K_g^T into S_x[g % 2]
-    auto issue_s = [&](int x, int qb, uint32_t g) {
-      const uint64_t da = dq + (((2 * x + qb) * kQTile) >> 4);
-      const uint64_t db = dk + (((g % kKStages) * kKVTile) >> 4);
-      const uint32_t d = tmem + kColS + x * 128 + (g & 1) * 64;
+    // (the whole warp runs this, in step; see mma_ss)
+    {
+      const uint32_t id_s = idesc_bf16(false), id_o = idesc_bf16(true);
+      uint32_t tile_cnt = 0, s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
+      // Operand descriptors of every buffer, built once: a descriptor's low
+      // field is the address / 16, so a k-step's offset is added to it.
+      const uint64_t dq0 = sdesc(sbase + kOffQ, 16), dq1 = sdesc(sbase + kOffQ + kTileBytes, 16);
+      const uint64_t dk0 = sdesc(sbase + kOffK, 16), dk1 = sdesc(sbase + kOffK + kTileBytes, 16);
+      const uint64_t dv0 = sdesc(sbase + kOffV, kHalfBytes);
+      const uint64_t dv1 = sdesc(sbase + kOffV + kTileBytes, kHalfBytes);
+      static_assert(kStages == 2, "one descriptor per stage");
+      // S_x(c) = Q_x K_c^T
+      auto issue_s = [&](int x, uint32_t c) {
+        const uint64_t da = x ? dq1 : dq0, db = (c & 1) ? dk1 : dk0;
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss(d, da + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
-               db + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), id_s, kk > 0);
-      mma_commit(bar(B_SF + 2 * x + (g & 1)));
-    };
-    // O_x (+)= P_x(g) V_g  (P_x(g): bf16 pairs in the first 32 columns of S_x[g % 2])
-    auto issue_pv = [&](int x, uint32_t g, bool acc) {
-      const uint64_t db = dv + (((g % kVStages) * kKVTile) >> 4);
-      const uint32_t d = tmem + x * 128, pa = tmem + kColS + x * 128 + (g & 1) * 64;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d, da + off, db + off, id_s, kk > 0);
+        }
+        mma_commit(bar(B_SF + x));
+        s_cnt[x]++;
+      };
+      // O_x (+)= P_x V_c  (P_x: bf16 pairs, keys 0-63 in columns 0-31 and keys
+      // 64-127 in columns 64-95 of S_x: each half where its own scores were)
+      auto issue_pv = [&](int x, uint32_t c, bool acc) {
+        const uint64_t db = (c & 1) ? dv1 : dv0;
+        const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ts(d, pa + kk * 8, db + ((kk * 16 * 128) >> 4), id_o, (acc || kk > 0) ? 1u : 0u);
-      mma_commit(bar(B_PD + x));
-    };
-    uint32_t n_s = 0, n_p = 0, g_s = 0, g_p = 0, o_cnt[2] = {0, 0};
-    int j_s = 0, j_p = 0;
-    Item it_s, it_p;
-    bool ok = take_item(0, &it_s);
-    it_p = it_s;
-    bool s_live = ok && it_s.r >= 0;
-    while (ok && it_p.r >= 0) {
-      // S of the tiles up to one past P.V's, into the next items if need be
-      while (s_live && g_s < g_p + 2) {
-        if (j_s == it_s.nkv) {
-          ++n_s;
-          j_s = 0;
-          if (!(ok = take_item(n_s, &it_s))) break;
-          if (it_s.r < 0) {
-            s_live = false;
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(d, pa + (kk >> 2) * 64 + (kk & 3) * 8, db + ((kk * 16 * 128) >> 4), id_o,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      for (uint32_t it_cnt = 0; ok; ++it_cnt) {
+        const int slot = it_cnt & 1;
+        if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+        const Item it = items[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IE + slot));
+        if (it.r < 0) break;
+        const int nx = it.hb >= 0 ? 2 : 1;
+        for (int x = 0; x < nx && ok; ++x)
+          ok = mbar_wait_warp(bar(B_QF + x), q_cnt[x]++ & 1, abort, ws.err);
+        const uint32_t c0 = tile_cnt;
+        if (!ok || !mbar_wait_warp(bar(B_KF + c0 % kStages), (c0 / kStages) & 1, abort, ws.err)) break;
+        tc_fence_after();
+        for (int x = 0; x < nx; ++x) issue_s(x, c0);
+        mma_commit(bar(B_KE + c0 % kStages));
+        if (it.nkv == 1)
+          for (int x = 0; x < nx; ++x) mma_commit(bar(B_QE + x));
+        for (int j = 0; j < it.nkv && ok; ++j) {
+          const uint32_t c = c0 + j;
+          const bool more = j + 1 < it.nkv;
+          if (!mbar_wait_warp(bar(B_VF + c % kStages), (c / kStages) & 1, abort, ws.err)) {
+            ok = false;
             break;
           }
+          for (int x = 0; x < nx; ++x) {
+            if (!mbar_wait_warp(bar(B_PF + x), (s_cnt[x] - 1) & 1, abort, ws.err) ||
+                (j == 0 && o_cnt[x] > 0 &&
+                 !mbar_wait_warp(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(x, c, j > 0);
+            if (x == nx - 1) mma_commit(bar(B_VE + c % kStages));  // every PV of V_c issued
+            if (more) {
+              // the next K tile is waited for only now, with PV_x already queued
+              if (x == 0 && !mbar_wait_warp(bar(B_KF + (c + 1) % kStages), ((c + 1) / kStages) & 1,
+                                           abort, ws.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(x, c + 1);
+            } else {
+              mma_commit(bar(B_OF + x));  // O_x final: its epilogue need not wait for the other tile
+              o_cnt[x]++;
+            }
+          }
+          if (!ok) break;
+          if (more) {
+            mma_commit(bar(B_KE + (c + 1) % kStages));
+            if (j + 2 == it.nkv)
+              for (int x = 0; x < nx; ++x) mma_commit(bar(B_QE + x));
+          }
         }
-        if (j_s == 0)
-          for (int x = 0; x < nx && ok; ++x)
-            ok = mbar_wait_warp(bar(B_QF + 2 * x + (n_s & 1)), (n_s >> 1) & 1, abort, ws.err);
-        if (!ok || !mbar_wait_warp(bar(B_KF + g_s % kKStages), (g_s / kKStages) & 1, abort,
-                                   ws.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int x = 0; x < nx; ++x) issue_s(x, n_s & 1, g_s);
-        mma_commit(bar(B_KE + g_s % kKStages));
-        if (j_s == it_s.nkv - 1)
-          for (int x = 0; x < nx; ++x) mma_commit(bar(B_QE + 2 * x + (n_s & 1)));
-        ++j_s;
-        ++g_s;
-      }
-      if (!ok) break;
-      // P.V of tile g_p
-      if (!mbar_wait_warp(bar(B_VF + g_p % kVStages), (g_p / kVStages) & 1, abort, ws.err)) break;
-      const bool last = j_p == it_p.nkv - 1;
-      for (int x = 0; x < nx && ok; ++x) {
-        if (!mbar_wait_warp(bar(B_PF + 2 * x + (g_p & 1)), (g_p >> 1) & 1, abort, ws.err) ||
-            (j_p == 0 && o_cnt[x] > 0 &&
-             !mbar_wait_warp(bar(B_OE + x), (o_cnt[x] - 1) & 1, abort, ws.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(x, g_p, j_p > 0);
-        if (last) {
-          mma_commit(bar(B_OF + x));  // O_x final: its epilogue need not wait for the other tile
-          o_cnt[x]++;
-        }
-      }
-      if (!ok) break;
-      mma_commit(bar(B_VE + g_p % kVStages));  // every P.V of V_g issued
-      ++g_p;
-      if (++j_p == it_p.nkv) {
-        if (lane == 0) mbar_arrive(bar(B_IE + (n_p & 3)));
-        ++n_p;
-        j_p = 0;
-        if (!(ok = take_item(n_p, &it_p))) break;
+        if (!ok) break;
+        tile_cnt += it.nkv;
       }
     }
     __syncwarp();
   } else if (warp < 10) {
-    // --------------- softmax: one warp per (query tile, row quarter) ---------------
-    // Warp w handles query tile x = (w - 2) / 4 and reads TMEM lanes 32 * (w %
-    // 4) .. + 31 (its 32 rows, one per thread), all 64 columns of each score
-    // tile; the two warps of an SM sub-partition work on the two query tiles.
-    const int x = (warp - 2) >> 2;
+    // ------------------- softmax: two warps per row, a column half each -------------------
+    // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its 32 rows, one per
+    // thread) and key columns 64 * hf .. 64 * hf + 63, hf = (w - 2) / 4, of
+    // both query tiles of the item in turn; both warps of a row quarter (w and
+    // w + 4) sit on the same SM sub-partition and work on the same tile at the
+    // same time, so each tile's softmax takes half as long.  The warps of a
+    // quarter exchange per-row values (the need for a max pass, the partial
+    // maxima, the partial sums) through shared memory and a two-arrival
+    // mbarrier, whose waits are bounded like every other.
+    const int hf = (warp - 2) >> 2;
     const int qd = warp & 3;
     const int row = qd * 32 + lane;  // == TMEM lane
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + kOffXch);
     const float sl2 = a.scale * kLog2e;
-    uint32_t g = 0;  // key tiles of this query tile so far (all items)
+    uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, x_cnt = 0;
     bool ok = true;
+    // this lane's value out, the other warp's value for the same row back
+    auto exchange = [&](float v) -> float {
+      const int sl = x_cnt & 1;  // two slots: a slot is rewritten only after both read it
+      xch[((qd * 2 + sl) * 2 + hf) * 32 + lane] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_XP + qd));
+      if (!mbar_wait_warp(bar(B_XP + qd), x_cnt & 1, abort, ws.err)) ok = false;
+      x_cnt++;
+      return xch[((qd * 2 + sl) * 2 + (1 - hf)) * 32 + lane];
+    };
+    float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
     for (uint32_t it_cnt = 0; ok; ++it_cnt) {
-      Item it;
-      if (!take_item(it_cnt, &it) || it.r < 0) break;
-      const int slot = it_cnt & 3;
-      if (x >= nx) {  // single-head items: the second tile's warps have no work
-        if (lane == 0) mbar_arrive(bar(B_IE + slot));
-        continue;
-      }
+      const int slot = it_cnt & 1;
+      if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+      const Item it = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IE + slot));
+      if (it.r < 0) break;
+      const int nx = it.hb >= 0 ? 2 : 1;
       const int qrow = it.qt * kPreTileQ + row;  // row inside the request
       const bool valid_row = qrow < it.n;
       const int qpos = valid_row ? it.ctx + qrow : 0;  // last visible key
-      float m_used = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < it.nkv; ++j) {
-        const uint32_t c = g++;
-        const int p = c & 1;
-        const int lim = qpos - j * kTileK;  // columns <= lim are visible
-        const bool masked = !__all_sync(0xffffffffu, lim >= kTileK - 1);
-        if (!mbar_wait_warp(bar(B_SF + 2 * x + p), (c >> 1) & 1, abort, ws.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t t_s = tmem + kColS + x * 128 + p * 64 + lane_off;
-        // the row's 64 scores in registers (one wait), then P in place
-        float sv[64];
-        auto load_scores = [&]() {
-          PKV_LD32(t_s + 0, (sv + 0));
-          PKV_LD32(t_s + 32, (sv + 32));
-          tmem_wait_ld();
-          if (masked) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
-          }
-        };
-        // p = exp2(s * scale * log2(e) - m) two columns at a time (packed
-        // fp32 pairs for the multiply-add and the sums); the bf16 pairs are
-        // packed over sv[0..31] (sv[2i], sv[2i+1] read before sv[i] is written)
-        float rs[4];
-        auto exp_pack = [&](float m) {
-          rs[0] = rs[1] = rs[2] = rs[3] = 0.f;
-          const float nm = -m;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x0, x1;
-            fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
-            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
-            sv[i] = __uint_as_float(pack_bf16(p0, p1));
-          }
-        };
-        load_scores();
-        float alpha = 1.f;
-        bool resc = false;
-        // After an item's first tile, P is computed with the running max
-        // straight away: no p exceeds 2^8 (the rescale threshold) while the
-        // row sum does not, so the max pass is taken only when some row's sum
-        // in the warp does (or is not finite).
-        bool need_max = j == 0;
-        if (!need_max) {
-          exp_pack(m_used);
-          const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
-          need_max = __any_sync(0xffffffffu, !(tot <= 256.f));
-          if (need_max) load_scores();
-        }
-        if (need_max) {
-          // the row maximum: three-input max chains
-          float mx[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
-#pragma unroll
-          for (int i = 12; i < 60; i += 8)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[60 + k]);
-          const float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-          resc = mt > m_used + kRescaleThreshold;
-          if (resc) {
-            alpha = fast_exp2(m_used - mt);  // 0 on the first tile
-            m_used = mt;
-          }
-          exp_pack(m_used);
-        }
-        PKV_ST32(t_s, (sv + 0));  // P: 32 packed columns where the scores began
-        l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O_x holds P.V of the item's tiles up to j - 1 once that P.V is
-          // complete; rescale the warp's 32 rows (128 columns)
-          if (!mbar_wait_warp(bar(B_PD + x), (c - 1) & 1, abort, ws.err)) {
+      float m_used[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+      for (int j = 0; j < it.nkv && ok; ++j) {
+        const int lim = qpos - j * kTileK - 64 * hf;  // my columns <= lim are visible
+        const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+        for (int x = 0; x < nx && ok; ++x) {
+          if (!mbar_wait_warp(bar(B_SF + x), s_cnt[x]++ & 1, abort, ws.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t t_o = tmem + x * 128 + lane_off;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float ov[32];
-            PKV_LD32(t_o + ch * 32, ov);
+          const uint32_t t_s = tmem + x * 128 + 64 * hf + lane_off;
+          // my 64 scores of the row in registers (one wait), then P in place
+          float sv[64];
+          auto load_scores = [&]() {
+            PKV_LD32(t_s + 0, (sv + 0));
+            PKV_LD32(t_s + 32, (sv + 32));
             tmem_wait_ld();
+            if (masked) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-            PKV_ST32(t_o + ch * 32, ov);
+              for (int i = 0; i < 64; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+            }
+          };
+          // p = exp2(s * scale * log2(e) - m) two columns at a time (packed
+          // fp32 pairs for the multiply-add and the sums); the bf16 pairs are
+          // packed over sv[0..31] (sv[2i], sv[2i+1] read before sv[i] is written)
+          float rs[4];
+          auto exp_pack = [&](float m) {
+            rs[0] = rs[1] = rs[2] = rs[3] = 0.f;
+            const float nm = -m;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x0, x1;
+              fma2(x0, x1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nm, nm);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(rs[2 * (i & 1)], rs[2 * (i & 1) + 1], p0, p1);
+              sv[i] = __uint_as_float(pack_bf16(p0, p1));
+            }
+          };
+          load_scores();
+          float alpha = 1.f;
+          bool resc = false;
+          // After the first tile, P is computed with the running max straight
+          // away: no p exceeds 2^8 (the rescale threshold) while a half-row
+          // sum does not, so the max pass is taken only when some half-row's
+          // sum does (or is not finite) in either warp of the quarter.
+          bool need_max = j == 0;
+          if (!need_max) {
+            exp_pack(m_used[x]);
+            const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+            const float mine = (tot <= 256.f) ? 0.f : 1.f;
+            const float other = exchange(mine);
+            if (!ok) break;
+            need_max = __any_sync(0xffffffffu, mine + other > 0.f);
+            if (need_max) load_scores();
           }
+          if (need_max) {
+            // the row maximum over both halves: three-input max chains, then
+            // the other warp's half through the exchange
+            float mx[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = max3f(sv[k], sv[k + 4], sv[k + 8]);
+#pragma unroll
+            for (int i = 12; i < 60; i += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], sv[i + k], sv[i + 4 + k]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], sv[60 + k]);
+            const float pm = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
+            const float po = exchange(pm);
+            if (!ok) break;
+            // (both warps form the same value: the halves in a fixed order)
+            const float mt = (hf == 0 ? fmaxf(pm, po) : fmaxf(po, pm)) * sl2;
+            resc = mt > m_used[x] + kRescaleThreshold;
+            if (resc) {
+              alpha = fast_exp2(m_used[x] - mt);  // 0 on the first tile
+              m_used[x] = mt;
+            }
+            exp_pack(m_used[x]);
+          }
+          PKV_ST32(t_s, (sv + 0));  // P half: 32 packed columns where my scores began
+          l_part[x] = l_part[x] * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+            // PV(j-1) is complete (S(j) is, and one thread's MMAs finish in
+            // order); each warp rescales its own 64 output columns
+            const uint32_t t_o = tmem + 256 + x * 128 + 64 * hf + lane_off;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              float ov[32];
+              PKV_LD32(t_o + ch * 32, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+              PKV_ST32(t_o + ch * 32, ov);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_PF + x));
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PF + 2 * x + p));
       }
       if (!ok) break;
-      // the row sums of the item, for the epilogue warps
-      lsum[(slot * 2 + x) * 128 + row] = l_run;
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_LF + 4 * x + slot));
-        mbar_arrive(bar(B_IE + slot));
+      // this warp's partial row sums of the item, for the epilogue warps
+      for (int x = 0; x < nx; ++x) {
+        lsum[(((it_cnt & 1) * 2 + x) * 2 + hf) * 128 + row] = l_part[x];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_LF + x));
       }
     }
   } else {
     // ------------------ epilogue: one warp per TMEM lane quarter ------------------
     // Warp w (10..13) owns rows 32 * (w % 4) .. + 31 of both output tiles.  When
-    // O_x is final (its last P.V done) and the row sums are in, the warp reads
-    // the 128-column row block out of TMEM in two halves, normalises them and
-    // packs them to bf16 in registers, and releases O_x as soon as the second
-    // half is read (the next item's first P.V may then overwrite it); each
-    // 32-column chunk goes out through the warp's staging area in shared
-    // memory, so that each global store writes whole 64-byte row pieces (8
-    // rows x 4 lanes).  The softmax warps never wait for this work.
+    // O_x is final (its last P.V done) and both partial row sums are in, the
+    // warp reads the 128-column row block out of TMEM in two halves,
+    // normalises them and packs them to bf16 in registers, and releases O_x as
+    // soon as the second half is read (the next item's first P.V may then
+    // overwrite it); each 32-column chunk goes out through the warp's staging
+    // area in shared memory, so that each global store writes whole 64-byte
+    // row pieces (8 rows x 4 lanes).
+    // The softmax warps never wait for this work.
     const int qd = warp & 3;
     const int row = qd * 32 + lane;  // == TMEM lane
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const float* lsum = reinterpret_cast<const float*>(smem + kOffLsum);
     const uint32_t stg = sbase + kOffStage + (warp - 10) * kStageWarp;
     combine_splits(a, ws, blockIdx.x * 4 + (warp - 10), gridDim.x * 4);
     uint32_t o_cnt[2] = {0, 0};
     for (uint32_t it_cnt = 0;; ++it_cnt) {
-      Item it;
-      if (!take_item(it_cnt, &it) || it.r < 0) break;
-      const int slot = it_cnt & 3;
+      const int slot = it_cnt & 1;
+      if (!mbar_wait_warp(bar(B_IF + slot), (it_cnt >> 1) & 1, abort, ws.err)) break;
+      const Item it = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IE + slot));
+      if (it.r < 0) break;
+      const int nx = it.hb >= 0 ? 2 : 1;
       bool ok = true;
       for (int x = 0; x < nx && ok; ++x) {
-        if (!mbar_wait_warp(bar(B_OF + x), o_cnt[x]++ & 1, abort, ws.err) ||
-            !mbar_wait_warp(bar(B_LF + 4 * x + slot), (it_cnt >> 2) & 1, abort, ws.err)) {
+        const uint32_t par = o_cnt[x]++ & 1;
+        if (!mbar_wait_warp(bar(B_OF + x), par, abort, ws.err) ||
+            !mbar_wait_warp(bar(B_LF + x), par, abort, ws.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float inv = 1.f / lsum[(slot * 2 + x) * 128 + row];
-        const uint32_t t_o = tmem + x * 128 + lane_off;
+        const float* ls = lsum + ((it_cnt & 1) * 2 + x) * 2 * 128;
+        const float inv = 1.f / (ls[row] + ls[128 + row]);  // the two column halves' sums
+        const uint32_t t_o = tmem + 256 + x * 128 + lane_off;
         const int h = x == 0 ? it.ha : it.hb;
         const int row_base = it.qt * kPreTileQ + qd * 32;  // the warp's first row
         uint16_t* obase = a.out + (int64_t)it.q0 * a.out_stride + (int64_t)h * kHeadSize;
@@ -735,7 +724,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) mbar_arrive(bar(B_IE + slot));
     }
   }
 
