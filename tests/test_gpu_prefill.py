@@ -56,6 +56,32 @@ def test_prefill_many_one_tile_items():
     run_and_check(step, "one-tile items")
 
 
+def test_prefill_rows_alone_and_in_a_large_batch():
+    """Batch-composition invariance of the prefill path: four requests (a
+    chunk after a 1024-token context, a 300-token prompt, a chunk after 100
+    cached tokens, a 20-token prompt) computed in a step of their own (few
+    work items, most SMs idle) and again at the head of a batch with 24 more
+    prompts (hundreds of items, other tiles on every SM).  Both runs are
+    checked against the oracle and against each other."""
+    small_ctx, small_n = [1024, 0, 100, 0], [224, 300, 60, 20]
+    small = W.build(W.custom(small_ctx, small_n, 16, 4, seed=909, pad_tokens=2))
+    _, got_small = run_and_check(small, "prefill alone")
+    rng = np.random.default_rng(910)
+    extra = 24
+    big = W.build(W.custom(small_ctx + [0] * extra, small_n + rng.integers(200, 257, extra).tolist(),
+                           16, 4, seed=909, pad_tokens=2))
+    # the shared requests get the same inputs in both runs
+    n_small = int(small.query_start_loc[-1])
+    big.qkv[:n_small] = small.qkv[:n_small]
+    for r in range(len(small_ctx)):
+        full, part = divmod(small_ctx[r], 16)
+        for b in range(full + (1 if part else 0)):
+            big.key_cache[big.block_table[r, b]] = small.key_cache[small.block_table[r, b]]
+            big.value_cache[big.block_table[r, b]] = small.value_cache[small.block_table[r, b]]
+    _, got_big = run_and_check(big, "prefill in a large batch")
+    assert_close(got_small[:n_small], got_big[:n_small], "alone vs in a large batch")
+
+
 def test_prefill_many_query_and_key_tiles():
     step = W.build(W.custom([0, 0], [300, 513], 4, 2, seed=12))
     run_and_check(step, "multi-tile prefill")
