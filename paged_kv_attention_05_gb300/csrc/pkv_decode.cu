@@ -409,6 +409,329 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   }
 }
 
+// Groups above 16 heads: a unit's rows are the G heads of its one query token
+// (qn * G <= 32 leaves a single token), two 16-row tiles.  A warp pair takes
+// the unit: each warp runs one tile's MMA chain, and the two share the unit's
+// page ring and query rows, so a page is loaded once for both tiles and each
+// warp's chain per page is that of a one-tile unit.  The first warp of the
+// pair takes the unit from the cursor (and hands it over through shared
+// memory), loads the query rows and the pages, and refills a stage only once
+// both warps have released it.
+struct CfgP {
+  static constexpr int kPairs = 6;
+  static constexpr int kWarps = 2 * kPairs;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kStages = 3;
+  static constexpr int kQHalf = 32 * 128;  // 32 query rows x one 64-dim half
+  static constexpr int kPairBytes = kStages * kPage + 2 * kQHalf;
+  // per pair: full[kStages], empty[kStages], query full, query read, unit[2]
+  static constexpr int kBarsPerPair = 2 * kStages + 4;
+  static constexpr int kOffUnit = kPairs * kPairBytes;  // int[kPairs][2]: unit handed over
+  static constexpr int kOffBar = kOffUnit + kPairs * 2 * 4;
+  static constexpr int kOffCtl = kOffBar + kPairs * kBarsPerPair * 8;
+  static constexpr int kSmem = kOffCtl + 16 + 1024;
+};
+static_assert(CfgP::kSmem <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(CfgP::kThreads, 1)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
+  using C = CfgP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pair = warp >> 1, tile = warp & 1;  // tile 0: the pair's first warp
+  const int G = a.hq / a.hkv;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t pbase = sbase + pair * C::kPairBytes;  // the pair's page stages
+  const uint32_t qbuf = pbase + C::kStages * kPage;     // and query rows
+  const uint32_t bars = sbase + C::kOffBar + pair * C::kBarsPerPair * 8;
+  auto full_bar = [&](int st) { return bars + 8u * st; };
+  auto empty_bar = [&](int st) { return bars + 8u * (C::kStages + st); };
+  const uint32_t q_full = bars + 8u * (2 * C::kStages), q_read = q_full + 8u;
+  auto unit_bar = [&](int k) { return bars + 8u * (2 * C::kStages + 2 + k); };
+  volatile int* uslot = reinterpret_cast<volatile int*>(smem + C::kOffUnit) + 2 * pair;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffCtl);
+
+  if (tile == 0) {
+    if (lane == 0) {
+      for (int st = 0; st < C::kStages; ++st) {
+        mbar_init(full_bar(st), 1);
+        mbar_init(empty_bar(st), 2);  // both warps release a stage
+      }
+      mbar_init(q_full, 1);
+      mbar_init(q_read, 2);  // both warps hold their query fragments
+      mbar_init(unit_bar(0), 1);
+      mbar_init(unit_bar(1), 1);
+      if (warp == 0) *abort = 0;
+      fence_barrier_init();
+    }
+    // query rows past the group's G heads stay zero; their results are dropped
+    for (int i = lane; i < 2 * 32 * 8; i += 32) {
+      const int row = (i >> 3) % 32, half = (i >> 3) / 32, c = i & 7;
+      if (row >= G)
+        *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+  }
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  grid_dep_wait();
+  grid_dep_launch();
+  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
+  __syncthreads();
+
+  const int n_units = ws.hdr->n_dec_units;
+  const float sl2 = a.scale * kLog2e;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int mi = lane >> 3, rr = lane & 7;
+  const int roff = 16 * tile;  // this warp's rows (heads of the group)
+  uint32_t page_cnt = 0;
+
+  for (uint32_t unit_cnt = 0;; ++unit_cnt) {
+    const int slot = unit_cnt & 1;
+    int u = 0;
+    if (tile == 0) {
+      if (lane == 0) {
+        u = atomicAdd(&ws.hdr->dec_counter, 1);
+        uslot[slot] = u;
+        mbar_arrive(unit_bar(slot));
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+    } else {
+      if (!mbar_wait_warp(unit_bar(slot), (unit_cnt >> 1) & 1, abort, ws.err)) break;
+      u = uslot[slot];
+    }
+    if (u >= n_units || *abort) break;
+    const DecUnit un = ws.units[u];
+    const int ug = un.gq & 0xFFFF;  // KV head
+    const int k0 = un.k0, k1 = un.k1;
+    const int p0 = k0 / kBlockSize;
+    const int npages = (k1 + kBlockSize - 1) / kBlockSize - p0;
+    const int nrows = G;            // one query token: the group's heads
+
+    // block ids of the unit (the loading warp only), one per lane per 32 pages
+    int ids[kIdRegs];
+#pragma unroll
+    for (int j = 0; j < kIdRegs; ++j) ids[j] = 0;
+    if (tile == 0) {
+      const int* btrow = a.bt + (int64_t)un.r * a.bt_width + p0;
+#pragma unroll
+      for (int j = 0; j < kIdRegs; ++j) {
+        const int p = lane + 32 * j;
+        int blk = 0;
+        if (p < npages) {
+          blk = __ldg(btrow + p);
+          if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+            atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
+            blk = 0;
+          }
+        }
+        ids[j] = blk;
+      }
+    }
+    // page p of the unit into stage (page_cnt + p) % kStages, once both warps
+    // have released the stage's previous page
+    bool ok = true;
+    auto issue_page = [&](int p) {
+      const uint32_t x = page_cnt + p;
+      const int st = x % C::kStages;
+      if (x >= (uint32_t)C::kStages &&
+          !mbar_wait_warp(empty_bar(st), ((x / C::kStages) - 1) & 1, abort, ws.err)) {
+        ok = false;
+        return;
+      }
+      int idv = ids[0];
+#pragma unroll
+      for (int j = 1; j < kIdRegs; ++j)
+        if ((p >> 5) == j) idv = ids[j];
+      const int blk = __shfl_sync(0xffffffffu, idv, p & 31);
+      if (lane == 0) {
+        const uint32_t sa = pbase + st * kPage;
+        mbar_expect_tx(full_bar(st), kPage);
+        tma_load_4d(sa, &tm_k, full_bar(st), 0, ug, 0, blk);
+        tma_load_4d(sa + kBox, &tm_k, full_bar(st), 64, ug, 0, blk);
+        tma_load_4d(sa + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk);
+        tma_load_4d(sa + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk);
+      }
+    };
+    if (tile == 0) {
+      // the query rows, once both warps hold the previous unit's fragments
+      if (unit_cnt > 0 && !mbar_wait_warp(q_read, (unit_cnt - 1) & 1, abort, ws.err)) break;
+      if (lane == 0) {
+        mbar_expect_tx(q_full, 2 * G * 128);
+        tma_load_3d(qbuf, &tm_q, q_full, 0, ug * G, un.q0);
+        tma_load_3d(qbuf + C::kQHalf, &tm_q, q_full, 64, ug * G, un.q0);
+      }
+      for (int p = 0; p < C::kStages && p < npages && ok; ++p) issue_page(p);
+      if (!ok) break;
+    }
+    // every row sees keys < ctx + 1, clipped to the unit
+    const int vis = min(k1, un.ctx + 1);
+    if (!mbar_wait_warp(q_full, unit_cnt & 1, abort, ws.err)) break;
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int kstep = 0; kstep < 8; ++kstep)
+      ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf +
+                  sw128(roff + rr + ((mi & 1) << 3), (kstep & 3) * 2 + (mi >> 1)),
+              qa[kstep][0], qa[kstep][1], qa[kstep][2], qa[kstep][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_read);
+
+    float o[16][4];
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[dn][e] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+    for (int p = 0; p < npages; ++p) {
+      const uint32_t x = page_cnt + p;
+      const int st = x % C::kStages;
+      if (!mbar_wait_warp(full_bar(st), (x / C::kStages) & 1, abort, ws.err)) {
+        ok = false;
+        break;
+      }
+      const int pos0 = k0 + p * kBlockSize;
+      const int valid = k1 - pos0;  // keys of this page inside the unit
+      const uint32_t sa = pbase + st * kPage;
+
+      // S = Q K^T for the page's 16 keys (two n-tiles of 8)
+      float sacc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+      for (int kstep = 0; kstep < 8; ++kstep) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sa + (kstep >> 2) * kBox + sw128(rr + ((mi >> 1) << 3), (kstep & 3) * 2 + (mi & 1)),
+                b0, b1, b2, b3);
+        mma_bf16(sacc[0], qa[kstep], b0, b1);
+        mma_bf16(sacc[1], qa[kstep], b2, b3);
+      }
+
+      // online softmax in the log2 domain (as in decode_kernel)
+      uint32_t pa[4];
+      {
+        float xs[2][4];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + tig * 2 + (e & 1);
+            xs[nt][e] = pos0 + tok < vis ? sacc[nt][e] * sl2 : -INFINITY;
+          }
+          mx0 = fmaxf(mx0, fmaxf(xs[nt][0], xs[nt][1]));
+          mx1 = fmaxf(mx1, fmaxf(xs[nt][2], xs[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const bool up0 = mx0 > m_run[0] + 8.f, up1 = mx1 > m_run[1] + 8.f;
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+          const float n0 = up0 ? mx0 : m_run[0], n1 = up1 ? mx1 : m_run[1];
+          const float al0 = up0 ? fast_exp2(m_run[0] - n0) : 1.f;
+          const float al1 = up1 ? fast_exp2(m_run[1] - n1) : 1.f;
+          m_run[0] = n0;
+          m_run[1] = n1;
+          l_run[0] *= al0;
+          l_run[1] *= al1;
+#pragma unroll
+          for (int dn = 0; dn < 16; ++dn) {
+            o[dn][0] *= al0;
+            o[dn][1] *= al0;
+            o[dn][2] *= al1;
+            o[dn][3] *= al1;
+          }
+        }
+        const float c0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float c1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          xs[nt][0] = fast_exp2(xs[nt][0] - c0);
+          xs[nt][1] = fast_exp2(xs[nt][1] - c0);
+          xs[nt][2] = fast_exp2(xs[nt][2] - c1);
+          xs[nt][3] = fast_exp2(xs[nt][3] - c1);
+          l_run[0] += xs[nt][0] + xs[nt][1];
+          l_run[1] += xs[nt][2] + xs[nt][3];
+        }
+        pa[0] = pack_bf16(xs[0][0], xs[0][1]);
+        pa[1] = pack_bf16(xs[0][2], xs[0][3]);
+        pa[2] = pack_bf16(xs[1][0], xs[1][1]);
+        pa[3] = pack_bf16(xs[1][2], xs[1][3]);
+      }
+
+      // O += P V (V rows read transposed); V of keys past the unit zeroed
+#pragma unroll
+      for (int dn = 0; dn < 16; dn += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sa + (2 + (dn >> 3)) * kBox + sw128(rr + ((mi & 1) << 3), (dn & 7) + (mi >> 1)),
+                  b0, b1, b2, b3);
+        if (valid < 16) {
+          b0 = mask_pair(b0, 2 * tig, valid);
+          b2 = mask_pair(b2, 2 * tig, valid);
+          b1 = mask_pair(b1, 8 + 2 * tig, valid);
+          b3 = mask_pair(b3, 8 + 2 * tig, valid);
+        }
+        mma_bf16(o[dn], pa, b0, b1);
+        mma_bf16(o[dn + 1], pa, b2, b3);
+      }
+      // this warp is done with the stage; the loading warp refills it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st));
+      if (tile == 0 && p + C::kStages < npages) {
+        issue_page(p + C::kStages);
+        if (!ok) break;
+      }
+    }
+    if (!ok) break;
+    page_cnt += npages;
+
+    // finish: row sums across the quad, then output or split partials
+    float l0 = l_run[0], l1 = l_run[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int ra = roff + gid, rb = ra + 8;  // rows: heads of the group
+    if (un.nsplit == 1) {
+      uint16_t* oa = a.out + (int64_t)un.q0 * a.out_stride + (int64_t)(ug * G + ra) * kHeadSize;
+      uint16_t* ob = a.out + (int64_t)un.q0 * a.out_stride + (int64_t)(ug * G + rb) * kHeadSize;
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        const int col = dn * 8 + tig * 2;
+        if (ra < nrows)
+          *reinterpret_cast<uint32_t*>(oa + col) = pack_bf16(o[dn][0] * i0, o[dn][1] * i0);
+        if (rb < nrows)
+          *reinterpret_cast<uint32_t*>(ob + col) = pack_bf16(o[dn][2] * i1, o[dn][3] * i1);
+      }
+    } else {
+      const int64_t pra = (int64_t)un.part + ra, prb = (int64_t)un.part + rb;
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        const int col = dn * 8 + tig * 2;
+        if (ra < nrows)
+          *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
+              make_float2(o[dn][0], o[dn][1]);
+        if (rb < nrows)
+          *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
+              make_float2(o[dn][2], o[dn][3]);
+      }
+      if (tig == 0) {
+        if (ra < nrows)
+          *reinterpret_cast<float2*>(ws.part_ml + pra * 2) = make_float2(m_run[0], l0);
+        if (rb < nrows)
+          *reinterpret_cast<float2*>(ws.part_ml + prb * 2) = make_float2(m_run[1], l1);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {
   constexpr int kWarpsPerBlock = kCombineThreads / 32;
   grid_dep_wait();  // the decode kernel's partial results
@@ -430,17 +753,29 @@ cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
                           tv, a, ws);
 }
 
+cudaError_t launch_pair(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
+  static std::atomic<bool> attr[kMaxAttrDevices];
+  if (cudaError_t e = smem_attr_once(decode_pair_kernel, CfgP::kSmem, attr)) return e;
+  const int G = a.hq / a.hkv;
+  CUtensorMap tq, tk, tv;
+  if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) ||
+      !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
+      !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
+    return cudaErrorInvalidValue;
+  return launch_dependent(decode_pair_kernel, dim3(sms), dim3(CfgP::kThreads), CfgP::kSmem, st,
+                          tq, tk, tv, a, ws);
+}
+
 }  // namespace
 
 int decode_workers(int group, int kv_int8, int sms) {
-  return sms * (kv_int8 ? decode_i8_warps(group)
-                        : (group <= 16 ? Cfg<1>::kWarps : Cfg<2>::kWarps));
+  return sms * (kv_int8 ? decode_i8_warps(group) : (group <= 16 ? Cfg<1>::kWarps : CfgP::kPairs));
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   const int G = a.hq / a.hkv;
   if (a.kv_int8) return launch_decode_i8(a, ws, sms, st);
-  return G <= 16 ? launch_mt<1>(a, ws, sms, st) : launch_mt<2>(a, ws, sms, st);
+  return G <= 16 ? launch_mt<1>(a, ws, sms, st) : launch_pair(a, ws, sms, st);
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {

@@ -38,6 +38,17 @@ def test_decode_small_batches(hq, hkv):
     run_and_check(step, "decode hq=%d hkv=%d" % (hq, hkv))
 
 
+@pytest.mark.parametrize("hq,hkv", [(17, 1), (40, 2), (24, 1), (64, 2)])
+def test_decode_groups_above_16(hq, hkv):
+    """Groups of 17 to 32 heads: a warp pair per unit, one 16-row tile each
+    (the second tile partly filled below 32 heads), sharing the page ring;
+    short requests, a page-aligned one and long ones split over several
+    units."""
+    ctx = [0, 15, 16, 300, 4095, 9000]
+    step = W.build(W.custom(ctx, [1] * len(ctx), hq, hkv, seed=hq * 7 + hkv))
+    run_and_check(step, "decode hq=%d hkv=%d" % (hq, hkv))
+
+
 def test_decode_long_requests_split_and_merge():
     ctx = [5000, 9000, 3, 4097]
     step = W.build(W.custom(ctx, [1] * 4, 32, 8, seed=77))
