@@ -223,6 +223,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       c = c2 < kMinChunk ? (c2 > c ? c2 : c) : kMinChunk;
     }
     if (c < chunk) chunk = (int)c;
+  } else if (dec_pairs > 0 && dec_pairs <= dec_grid) {
+    // More splits than one wave of workers, but every pair fits in it with
+    // a somewhat longer chunk: one wave of units under twice as long beats
+    // two waves (32 MQA requests of 32,769 keys on 912 workers: 1216-key
+    // units, 864 of them, instead of 1056 units of 1024 keys)
+    const long long per_pair = dec_grid / dec_pairs;
+    long long c = (lmax + per_pair - 1) / per_pair;
+    c = (c + kDecTile - 1) / kDecTile * kDecTile;
+    if (c <= kMaxChunk && c < 2LL * chunk) chunk = (int)c;
   }
 
   // Units are listed roughly longest first, in five classes: every request's

@@ -32,7 +32,8 @@ def plan_counts(ctx, q_len, hq, hkv, workers, caps):
     """Entries of the plan for one batch: the split chunk chosen as the plan
     kernel chooses it (about four units per decode worker, whole 64-key
     tiles, between max(256, 32 G) and 2048 keys; shorter where every pair's
-    splits fit one wave of workers and the workspace holds them), then the
+    splits fit one wave of workers and the workspace holds them; longer, by
+    less than twice, where that makes one wave instead of more), then the
     units, split pairs, partial rows and prefill tiles of that chunk."""
     G = hq // hkv
     decs, pres = [], []
@@ -61,6 +62,13 @@ def plan_counts(ctx, q_len, hq, hkv, workers, caps):
                 c2 = -(-c2 // 64) * 64
                 c = max(c2, c) if c2 < 256 else 256
             chunk = min(chunk, c)
+        elif pairs <= workers:
+            # one wave of somewhat longer units instead of two waves
+            per_pair = workers // pairs
+            c = -(-lmax // per_pair)
+            c = -(-c // 64) * 64
+            if c <= 2048 and c < 2 * chunk:
+                chunk = c
     units = parts = split_pairs = 0
     for L, n in decs:
         ns = -(-L // chunk)
