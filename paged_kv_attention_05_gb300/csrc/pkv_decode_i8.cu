@@ -11,12 +11,8 @@
 // the same for V), loaded by TMA into a per-warp ring of 3 pages (one 2 KB box
 // each for K and V, 128-byte swizzle).  With half the bytes of a bf16 page
 // per page of work, a warp has less time per page to hide its latencies, so a
-// CTA per SM runs 12 independent warps.  A unit of a group above 16 heads
-// carries two 16-row query tiles; it is taken by a warp pair, one tile per
-// warp, sharing a 4-page ring and the query rows (the first warp of the pair
-// takes the unit, loads the rows and the pages, and refills a stage once
-// both warps have its codes in registers), so that each warp's chain per page
-// is that of a one-tile unit.  The codes go from shared memory straight into
+// CTA per SM runs 12 independent warps (8 when a unit carries two 16-row
+// query tiles, whose accumulators need twice the registers).  The codes go from shared memory straight into
 // the operand registers of fp16 mma.sync m16n8k16 — no widened copy of the
 // page is written back — because every code -127..127 is an fp16 integer:
 // the byte, offset by 128, becomes the low mantissa byte of the fp16 number
@@ -54,22 +50,16 @@ constexpr uint32_t kFp16Bias = 0x64806480u;      // fp16 pair (1152, 1152) = 102
 
 template <int MT>
 struct Cfg8 {
-  // MT query tiles per unit.  One: 12 warps, each with its own 3-page ring
-  // (166 registers).  Two: 6 warp pairs, one tile per warp, a 4-page ring and
-  // the query rows per pair.
-  static constexpr bool kPair = MT == 2;
-  static constexpr int kWarps = 12;
+  // one query tile: 12 warps of 3 stages (166 registers); two: 8 warps
+  static constexpr int kWarps = MT == 1 ? 12 : 8;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kGroups = kWarps / MT;           // warps or pairs, one unit each
-  static constexpr int kStages = kPair ? 4 : 3;
+  static constexpr int kStages = 3;
   static constexpr int kQHalf = MT * 16 * 128;          // bf16 query rows x one 64-dim half
-  static constexpr int kGroupBytes = kStages * kStage8 + 2 * kQHalf;
-  // per group: full[kStages], query loaded; pairs also empty[kStages], query
-  // read by both warps, unit handed over[2]
-  static constexpr int kBarsPerGroup = kPair ? 2 * kStages + 4 : kStages + 1;
-  static constexpr int kOffUnit = kGroups * kGroupBytes;  // int[kGroups][2] (pairs)
-  static constexpr int kOffBar = kOffUnit + kGroups * 2 * 4;
-  static constexpr int kOffCtl = kOffBar + kGroups * kBarsPerGroup * 8;
+  static constexpr int kFrag = MT == 1 ? 0 : MT * 8 * 32 * 16;  // fp16 query fragments
+  static constexpr int kWarpBytes = kStages * kStage8 + 2 * kQHalf + kFrag;
+  static constexpr int kBarsPerWarp = kStages + 1;      // page stages, query
+  static constexpr int kOffBar = kWarps * kWarpBytes;
+  static constexpr int kOffCtl = kOffBar + kWarps * kBarsPerWarp * 8;
   static constexpr int kSmem = kOffCtl + 16 + 1024;
 };
 static_assert(Cfg8<1>::kSmem <= 232448 && Cfg8<2>::kSmem <= 232448, "shared memory per CTA");
@@ -127,40 +117,27 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
                                              ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.hq / a.hkv;
-  const int grp = warp / MT, tile = warp % MT;  // a pair's first warp has tile 0
-  const int roff = 16 * tile;                     // this warp's query rows
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t wbase = sbase + grp * C::kGroupBytes;  // the group's page stages
-  const uint32_t qbuf = wbase + C::kStages * kStage8;    // bf16 query rows (TMA)
-  const uint32_t bars = sbase + C::kOffBar + grp * C::kBarsPerGroup * 8;
+  const uint32_t wbase = sbase + warp * C::kWarpBytes;  // this warp's page stages
+  const uint32_t qbuf = wbase + C::kStages * kStage8;     // bf16 query rows (TMA)
+  const uint32_t frag = qbuf + 2 * C::kQHalf;             // fp16 query fragments (MT = 2)
+  const uint32_t bars = sbase + C::kOffBar + warp * C::kBarsPerWarp * 8;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   const uint32_t q_bar = bars + 8u * C::kStages;
-  auto empty_bar = [&](int s) { return bars + 8u * (C::kStages + 1 + s); };
-  const uint32_t q_read = bars + 8u * (2 * C::kStages + 1);
-  auto unit_bar = [&](int k) { return bars + 8u * (2 * C::kStages + 2 + k); };
-  volatile int* uslot = reinterpret_cast<volatile int*>(smem + C::kOffUnit) + 2 * grp;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffCtl);
 
-  if (tile == 0) {
-    if (lane == 0) {
-      for (int s = 0; s <= C::kStages; ++s) mbar_init(bars + 8u * s, 1);
-      if (C::kPair) {
-        for (int s = 0; s < C::kStages; ++s) mbar_init(empty_bar(s), 2);  // both warps
-        mbar_init(q_read, 2);
-        mbar_init(unit_bar(0), 1);
-        mbar_init(unit_bar(1), 1);
-      }
-      if (warp == 0) *abort = 0;
-      fence_barrier_init();
-    }
-    // rows past a unit's qn * G query rows hold zeros or an earlier unit's
-    // queries; their results are dropped
-    for (int i = lane; i < 2 * MT * 16 * 8; i += 32) {
-      const int row = (i >> 3) % (MT * 16), half = (i >> 3) / (MT * 16), c = i & 7;
-      if (row >= G)
-        *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
-            make_uint4(0, 0, 0, 0);
-    }
+  if (lane == 0) {
+    for (int s = 0; s <= C::kStages; ++s) mbar_init(bars + 8u * s, 1);
+    if (warp == 0) *abort = 0;
+    fence_barrier_init();
+  }
+  // rows past a unit's qn * G query rows hold zeros or an earlier unit's
+  // queries; their results are dropped
+  for (int i = lane; i < 2 * MT * 16 * 8; i += 32) {
+    const int row = (i >> 3) % (MT * 16), half = (i >> 3) / (MT * 16), c = i & 7;
+    if (row >= G)
+      *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
+          make_uint4(0, 0, 0, 0);
   }
   // the set-up above overlaps the plan kernel; the work list is read after it
   grid_dep_wait();
@@ -176,19 +153,8 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
 
   for (uint32_t unit_cnt = 0;; ++unit_cnt) {
     int u = 0;
-    if (tile == 0) {
-      if (lane == 0) {
-        u = atomicAdd(&ws.hdr->dec_counter, 1);
-        if (C::kPair) {  // hand the unit to the pair's second warp
-          uslot[unit_cnt & 1] = u;
-          mbar_arrive(unit_bar(unit_cnt & 1));
-        }
-      }
-      u = __shfl_sync(0xffffffffu, u, 0);
-    } else {
-      if (!mbar_wait_warp(unit_bar(unit_cnt & 1), (unit_cnt >> 1) & 1, abort, ws.err)) break;
-      u = uslot[unit_cnt & 1];
-    }
+    if (lane == 0) u = atomicAdd(&ws.hdr->dec_counter, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= n_units || *abort) break;
     const DecUnit un = ws.units[u];
     const int ug = un.gq & 0xFFFF;  // KV head
@@ -199,9 +165,7 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
     const int nrows = qn * G;
 
     int ids[kIdRegs8];
-#pragma unroll
-    for (int j = 0; j < kIdRegs8; ++j) ids[j] = 0;
-    if (tile == 0) {  // (the warp that loads the pages)
+    {
       const int* btrow = a.bt + (int64_t)un.r * a.bt_width + p0;
 #pragma unroll
       for (int j = 0; j < kIdRegs8; ++j) {
@@ -217,40 +181,28 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
         ids[j] = blk;
       }
     }
-    bool ok = true;
-    // query rows token * G + head of this KV head, by TMA (two 64-dim halves);
-    // a pair's rows once both warps hold the previous unit's fragments
-    if (tile == 0) {
-      if (C::kPair && unit_cnt > 0 &&
-          !mbar_wait_warp(q_read, (unit_cnt - 1) & 1, abort, ws.err))
-        break;
-      if (lane == 0) {
-        fence_async_smem();  // the previous unit's reads of the buffer are done
-        mbar_expect_tx(q_bar, 2 * nrows * 128);
-        for (int i = 0; i < qn; ++i) {
-          tma_load_3d(qbuf + i * G * 128, &tm_q, q_bar, 0, ug * G, un.q0 + i);
-          tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, ug * G, un.q0 + i);
-        }
+    // query rows token * G + head of this KV head, by TMA (two 64-dim halves)
+    if (lane == 0) {
+      fence_async_smem();  // the previous unit's reads of the buffer are done
+      mbar_expect_tx(q_bar, 2 * nrows * 128);
+      for (int i = 0; i < qn; ++i) {
+        tma_load_3d(qbuf + i * G * 128, &tm_q, q_bar, 0, ug * G, un.q0 + i);
+        tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, ug * G, un.q0 + i);
       }
     }
-    int vis[2];
+    int vis[MT][2];
 #pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      const int row = roff + gid + hrow * 8;
-      const int ti = row < nrows ? row / G : qn - 1;
-      vis[hrow] = min(k1, un.ctx + ti + 1);
-    }
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int row = mt * 16 + gid + hrow * 8;
+        const int ti = row < nrows ? row / G : qn - 1;
+        vis[mt][hrow] = min(k1, un.ctx + ti + 1);
+      }
 
-    // page p into stage (page_cnt + p) % kStages: a warp of its own reuses a
-    // stage once it has read it (program order); a pair once both warps have
     auto issue_page = [&](int p) {
       const uint32_t x = page_cnt + p;
       const int s = x % C::kStages;
-      if (C::kPair && x >= (uint32_t)C::kStages &&
-          !mbar_wait_warp(empty_bar(s), ((x / C::kStages) - 1) & 1, abort, ws.err)) {
-        ok = false;
-        return;
-      }
       int idv = ids[0];
 #pragma unroll
       for (int j = 1; j < kIdRegs8; ++j)
@@ -264,41 +216,58 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
         tma_load_4d(st + kBox8, &tm_v, full_bar(s), 0, ug, 0, blk);
       }
     };
-    if (tile == 0) {
-      for (int p = 0; p < C::kStages && p < npages && ok; ++p) issue_page(p);
-      if (!ok) break;
-    }
+    for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
     if (!mbar_wait_warp(q_bar, unit_cnt & 1, abort, ws.err)) break;
 
     // fp16 query fragments in the permuted k order: k-step ks, registers
     // {a0, a2} of row r hold dimensions 32 * tig + 4 * ks .. + 3
-    uint32_t qa[8][4];
+    uint32_t qa[MT == 1 ? 8 : 1][4];
 #pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      const int row = roff + gid + hrow * 8;
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t f[8][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // dimensions 32 * tig + 8 * c .. + 7: half tig / 2, 16-byte chunk
-        // 4 * (tig % 2) + c of the row
-        const uint4 v = lds128(qbuf + (tig >> 1) * C::kQHalf + sw128(row, (tig & 1) * 4 + c));
-        qa[2 * c][hrow] = bf16x2_to_f16x2(v.x, sl2);
-        qa[2 * c][2 + hrow] = bf16x2_to_f16x2(v.y, sl2);
-        qa[2 * c + 1][hrow] = bf16x2_to_f16x2(v.z, sl2);
-        qa[2 * c + 1][2 + hrow] = bf16x2_to_f16x2(v.w, sl2);
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int row = mt * 16 + gid + hrow * 8;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // dimensions 32 * tig + 8 * c .. + 7: half tig / 2, 16-byte chunk
+          // 4 * (tig % 2) + c of the row
+          const uint4 v = lds128(qbuf + (tig >> 1) * C::kQHalf + sw128(row, (tig & 1) * 4 + c));
+          f[2 * c][hrow] = bf16x2_to_f16x2(v.x, sl2);
+          f[2 * c][2 + hrow] = bf16x2_to_f16x2(v.y, sl2);
+          f[2 * c + 1][hrow] = bf16x2_to_f16x2(v.z, sl2);
+          f[2 * c + 1][2 + hrow] = bf16x2_to_f16x2(v.w, sl2);
+        }
+      }
+      if (MT == 1) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qa[MT == 1 ? ks : 0][e] = f[ks][e];
+      } else {
+        // each lane keeps its own fragments (no other lane reads them)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(
+                           frag + ((mt * 8 + ks) * 32 + lane) * 16),
+                       "r"(f[ks][0]), "r"(f[ks][1]), "r"(f[ks][2]), "r"(f[ks][3])
+                       : "memory");
       }
     }
-    if (C::kPair) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_read);
+
+    float o[MT][16][4];
+    float m_run[MT][2], l_run[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][dn][e] = 0.f;
+      m_run[mt][0] = m_run[mt][1] = -INFINITY;
+      l_run[mt][0] = l_run[mt][1] = 0.f;
     }
 
-    float o[16][4];
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-#pragma unroll
-    for (int dn = 0; dn < 16; ++dn)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[dn][e] = 0.f;
-
+    bool ok = true;
     for (int p = 0; p < npages; ++p) {
       const uint32_t x = page_cnt + p;
       const int s = x % C::kStages;
@@ -320,35 +289,47 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
       const uint4 vD = lds128(st + kBox8 + sw128(2 * tig + 9, gid));
 
       // S = Q K^T (log2 domain) for the page's 16 keys (two n-tiles of 8)
-      float sacc[2][4];
+      float sacc[MT][2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t u0 = (ks < 4 ? word_of(ka0, ks) : word_of(kb0, ks - 4)) ^ kSignFlip;
         const uint32_t u1 = (ks < 4 ? word_of(ka1, ks) : word_of(kb1, ks - 4)) ^ kSignFlip;
         const uint32_t b00 = codes_f16x2(u0, 0x4140), b01 = codes_f16x2(u0, 0x4342);
         const uint32_t b10 = codes_f16x2(u1, 0x4140), b11 = codes_f16x2(u1, 0x4342);
-        mma_f16(sacc[0], qa[ks], b00, b01);
-        mma_f16(sacc[1], qa[ks], b10, b11);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t qf[4];
+          if (MT == 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qf[e] = qa[MT == 1 ? ks : 0][e];
+          } else {
+            const uint4 v = lds128(frag + ((mt * 8 + ks) * 32 + lane) * 16);
+            qf[0] = v.x;
+            qf[1] = v.y;
+            qf[2] = v.z;
+            qf[3] = v.w;
+          }
+          mma_f16(sacc[mt][0], qf, b00, b01);
+          mma_f16(sacc[mt][1], qf, b10, b11);
+        }
       }
 
       // the stage's codes are all in registers: its next page can be on its
-      // way (issued here, behind the S MMAs, whose latency hides the branch);
-      // a pair's loading warp waits until the other warp has read it too
+      // way (issued here, behind the S MMAs, whose latency hides the branch)
       __syncwarp();
-      if (C::kPair && lane == 0) mbar_arrive(empty_bar(s));
-      if (tile == 0 && p + C::kStages < npages) {
-        issue_page(p + C::kStages);
-        if (!ok) break;
-      }
+      if (p + C::kStages < npages) issue_page(p + C::kStages);
 
       // online softmax in the log2 domain, keys >= the row's limit masked;
       // the output is rescaled only when a row's maximum grows by more than 2^8
-      uint32_t pa[4];
-      {
+      uint32_t pa[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
         float xs[2][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -356,7 +337,7 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = nt * 8 + tig * 2 + (e & 1);
-            xs[nt][e] = pos0 + tok < vis[e >> 1] ? sacc[nt][e] : -INFINITY;
+            xs[nt][e] = pos0 + tok < vis[mt][e >> 1] ? sacc[mt][nt][e] : -INFINITY;
           }
           mx0 = fmaxf(mx0, fmaxf(xs[nt][0], xs[nt][1]));
           mx1 = fmaxf(mx1, fmaxf(xs[nt][2], xs[nt][3]));
@@ -365,40 +346,40 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const bool up0 = mx0 > m_run[0] + 8.f, up1 = mx1 > m_run[1] + 8.f;
+        const bool up0 = mx0 > m_run[mt][0] + 8.f, up1 = mx1 > m_run[mt][1] + 8.f;
         if (__any_sync(0xffffffffu, up0 || up1)) {
-          const float n0 = up0 ? mx0 : m_run[0], n1 = up1 ? mx1 : m_run[1];
+          const float n0 = up0 ? mx0 : m_run[mt][0], n1 = up1 ? mx1 : m_run[mt][1];
           // (a row that did not grow keeps factor 1: its maximum may still be -inf)
-          const float al0 = up0 ? fast_exp2(m_run[0] - n0) : 1.f;
-          const float al1 = up1 ? fast_exp2(m_run[1] - n1) : 1.f;
-          m_run[0] = n0;
-          m_run[1] = n1;
-          l_run[0] *= al0;
-          l_run[1] *= al1;
+          const float al0 = up0 ? fast_exp2(m_run[mt][0] - n0) : 1.f;
+          const float al1 = up1 ? fast_exp2(m_run[mt][1] - n1) : 1.f;
+          m_run[mt][0] = n0;
+          m_run[mt][1] = n1;
+          l_run[mt][0] *= al0;
+          l_run[mt][1] *= al1;
 #pragma unroll
           for (int dn = 0; dn < 16; ++dn) {
-            o[dn][0] *= al0;
-            o[dn][1] *= al0;
-            o[dn][2] *= al1;
-            o[dn][3] *= al1;
+            o[mt][dn][0] *= al0;
+            o[mt][dn][1] *= al0;
+            o[mt][dn][2] *= al1;
+            o[mt][dn][3] *= al1;
           }
         }
         // a row with no visible key yet keeps m = -inf: use 0 as its reference
-        const float c0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
-        const float c1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+        const float c0 = m_run[mt][0] == -INFINITY ? 0.f : m_run[mt][0];
+        const float c1 = m_run[mt][1] == -INFINITY ? 0.f : m_run[mt][1];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           xs[nt][0] = fast_exp2(xs[nt][0] - c0);
           xs[nt][1] = fast_exp2(xs[nt][1] - c0);
           xs[nt][2] = fast_exp2(xs[nt][2] - c1);
           xs[nt][3] = fast_exp2(xs[nt][3] - c1);
-          l_run[0] += xs[nt][0] + xs[nt][1];
-          l_run[1] += xs[nt][2] + xs[nt][3];
+          l_run[mt][0] += xs[nt][0] + xs[nt][1];
+          l_run[mt][1] += xs[nt][2] + xs[nt][3];
         }
-        pa[0] = pack_f16(xs[0][0], xs[0][1]);
-        pa[1] = pack_f16(xs[0][2], xs[0][3]);
-        pa[2] = pack_f16(xs[1][0], xs[1][1]);
-        pa[3] = pack_f16(xs[1][2], xs[1][3]);
+        pa[mt][0] = pack_f16(xs[0][0], xs[0][1]);
+        pa[mt][1] = pack_f16(xs[0][2], xs[0][3]);
+        pa[mt][2] = pack_f16(xs[1][0], xs[1][1]);
+        pa[mt][3] = pack_f16(xs[1][2], xs[1][3]);
       }
 
       // O += P V: code word i of the four key rows (dimensions 16 * gid +
@@ -418,7 +399,8 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
           const uint32_t ab = e < 2 ? ab_lo : ab_hi, cd = e < 2 ? cd_lo : cd_hi;
           const uint32_t sel = (e & 1) ? 0x4342 : 0x4140;
           const uint32_t b0 = codes_f16x2(ab, sel), b1 = codes_f16x2(cd, sel);
-          mma_f16(o[4 * i + e], pa, b0, b1);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) mma_f16(o[mt][4 * i + e], pa[mt], b0, b1);
         }
       }
     }
@@ -428,13 +410,14 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
     // finish: row sums across the quad; the thread holds output dimensions
     // 32 * tig .. + 31 of rows ra and rb (dimension 32 * tig + j in
     // o[j][0 / 2] for j < 16, o[j - 16][1 / 3] above)
-    {
-      float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float l0 = l_run[mt][0], l1 = l_run[mt][1];
       l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int ra = roff + gid, rb = ra + 8;  // rows: token * G + head in group
+      const int ra = mt * 16 + gid, rb = ra + 8;  // rows: token * G + head in group
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
         const int rw = hrow ? rb : ra;
@@ -452,7 +435,7 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const int j = q4 * 8 + 2 * k;
-                w[k] = pack_bf16(o[j][e0 + h2] * inv, o[j + 1][e0 + h2] * inv);
+                w[k] = pack_bf16(o[mt][j][e0 + h2] * inv, o[mt][j + 1][e0 + h2] * inv);
               }
               *reinterpret_cast<uint4*>(orow + h2 * 16 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
             }
@@ -464,12 +447,12 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
             for (int q4 = 0; q4 < 4; ++q4) {
               const int j = q4 * 4;
               *reinterpret_cast<float4*>(prow + h2 * 16 + j) =
-                  make_float4(o[j][e0 + h2] * o_scale, o[j + 1][e0 + h2] * o_scale,
-                              o[j + 2][e0 + h2] * o_scale, o[j + 3][e0 + h2] * o_scale);
+                  make_float4(o[mt][j][e0 + h2] * o_scale, o[mt][j + 1][e0 + h2] * o_scale,
+                              o[mt][j + 2][e0 + h2] * o_scale, o[mt][j + 3][e0 + h2] * o_scale);
             }
           if (tig == 0)
             *reinterpret_cast<float2*>(ws.part_ml + ((int64_t)un.part + rw) * 2) =
-                make_float2(m_run[hrow], hrow ? l1 : l0);
+                make_float2(m_run[mt][hrow], hrow ? l1 : l0);
         }
       }
     }
@@ -493,7 +476,7 @@ cudaError_t launch_i8(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
 
 }  // namespace
 
-int decode_i8_warps(int group) { return group <= 16 ? Cfg8<1>::kGroups : Cfg8<2>::kGroups; }
+int decode_i8_warps(int group) { return group <= 16 ? Cfg8<1>::kWarps : Cfg8<2>::kWarps; }
 
 cudaError_t launch_decode_i8(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   const int G = a.hq / a.hkv;
