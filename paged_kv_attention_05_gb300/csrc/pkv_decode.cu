@@ -17,12 +17,14 @@
 //     plan kernel.  A CTA per SM holds 8 warps.  Each warp takes units from an
 //     atomic cursor and streams the unit's pages by itself: TMA boxes of 16
 //     slots x 64 dims (K and V, two halves, 128-byte swizzle) into its own
-//     ring of 8 KB page stages (3 deep, 2 for 32-head groups).  Warps never
-//     wait for each other, so each SM keeps 8 independent streams of loads in
-//     flight and 8 warps to hide the latency of the math.
-//   * A warp owns the query rows of its KV head in one or two 16-row tiles:
-//     row = token * G + head in group, for the request's qn tokens (qn * G at
-//     most 16, or 32 for groups above 16; longer requests go to prefill).
+//     ring of 8 KB page stages, 3 deep.  Warps never wait for each other, so
+//     each SM keeps 8 independent streams of loads in flight and 8 warps to
+//     hide the latency of the math.
+//   * A warp owns the query rows of its KV head in one 16-row tile: row =
+//     token * G + head in group, for the request's qn tokens (qn * G at most
+//     16; longer requests go to prefill).  Groups above 16 heads (up to 32
+//     rows, a single token) run decode_pair_kernel below: a warp pair per
+//     unit, one tile per warp, one page ring per pair.
 //     Row (token i) sees the keys before position ctx + i + 1, ctx = keys
 //     before the request's first query token (causal mask inside the
 //     request's own tokens).  S = Q.K^T and O += P.V run
@@ -53,6 +55,8 @@ constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2
 constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
 constexpr int kIdRegs = kMaxChunk / kBlockSize / 32;  // block ids per lane per unit
 
+// MT 16-row query tiles per warp (1: decode_kernel<1> serves every group of
+// up to 16 heads; larger groups take the warp pairs of decode_pair_kernel)
 template <int MT>
 struct Cfg {
   static constexpr int kWarps = 8;
