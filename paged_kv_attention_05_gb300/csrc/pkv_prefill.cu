@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     float* xch = reinterpret_cast<float*>(smem + kOffXch);
     const float sl2 = a.scale * kLog2e;
-    uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0}, x_cnt = 0;
+    uint32_t s_cnt[2] = {0, 0}, x_cnt = 0;
     bool ok = true;
     // this lane's value out, the other warp's value for the same row back
     auto exchange = [&](float v) -> float {
