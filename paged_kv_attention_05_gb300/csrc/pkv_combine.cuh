@@ -1,6 +1,5 @@
-// The merge of split-KV decode results, shared by the combine kernel (int8
-// calls) and the prefill kernel, whose warps run it before their own work in
-// the same launch (bf16 calls).
+// The merge of split-KV decode results, run by the combine kernel after the
+// decode kernel.
 #pragma once
 
 #include "pkv_device.cuh"

@@ -37,9 +37,8 @@
 //     the fragments, so stale or NaN cache slots never reach the product.
 //   * A unit that covers a whole request writes the bf16 output; one split of
 //     several writes (max, sum, unnormalised output) in fp32 to the workspace,
-//     and the merge of the splits (pkv_combine.cuh) runs afterwards: first
-//     thing in the prefill kernel's launch for bf16 calls, in the combine
-//     kernel below for int8 calls.  Every mbarrier wait is bounded.
+//     and the merge of the splits (pkv_combine.cuh) runs afterwards, in the
+//     combine kernel below.  Every mbarrier wait is bounded.
 // The int8-cache variant of the decode kernel is in pkv_decode_i8.cu; it
 // shares the plan, the work units and the merge.
 #include "pkv_combine.cuh"

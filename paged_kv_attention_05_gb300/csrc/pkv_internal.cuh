@@ -188,7 +188,7 @@ int decode_i8_warps(int group);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
 // Programmatic dependent launch.  The attention kernels after the cache write
-// (plan, decode, prefill, merge) are launched with programmatic stream
+// (plan, decode, merge; prefill on its own stream) are launched with programmatic stream
 // serialisation: a kernel's CTAs may start while the kernel before it in the
 // stream is still running, do their set-up (barriers, shared-memory
 // clearing), and then wait in grid_dep_wait() until that kernel has finished

@@ -44,7 +44,6 @@
 //               through a per-warp staging area (whole 64-byte row pieces).
 // Every mbarrier wait is bounded; on expiry the kernel records
 // PKV_DEV_ERR_TIMEOUT, stops issuing work, frees its TMEM and returns.
-#include "pkv_combine.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -209,16 +208,8 @@ __device__ __forceinline__ void tmem_wait_st() {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
-  // This launch also merges the split-KV decode results of the step (the
-  // decode kernel ran before it in stream order), which saves a launch of its
-  // own: every warp of the grid does it when the batch has no prefill work,
-  // else the epilogue warps, before their first output tile is due.
-  grid_dep_wait();  // the work lists and the decode kernel's partial results
-  if (ws.hdr->n_pre_entries == 0) {  // (every CTA agrees)
-    combine_splits(a, ws, blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5),
-                   gridDim.x * (kThreads / 32));
-    return;
-  }
+  grid_dep_wait();  // the work lists
+  if (ws.hdr->n_pre_entries == 0) return;  // a step without prefill work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -650,7 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float* lsum = reinterpret_cast<const float*>(smem + kOffLsum);
     const uint32_t stg = sbase + kOffStage + (warp - 10) * kStageWarp;
-    combine_splits(a, ws, blockIdx.x * 4 + (warp - 10), gridDim.x * 4);
     uint32_t o_cnt[2] = {0, 0};
     for (uint32_t it_cnt = 0;; ++it_cnt) {
       const int slot = it_cnt & 1;
