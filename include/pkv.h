@@ -18,13 +18,9 @@
  *     the attention calls launch their kernels with programmatic dependent
  *     launch, so a kernel may begin its set-up while the work before it on
  *     the stream is finishing, but it reads and writes no global memory
- *     until that work has finished.  pkv_attention and
- *     pkv_attention_planned run their prefill kernel on a stream of the
- *     library's own (one per device), forked from `stream` after the work
- *     already enqueued there and joined back into it with events before the
- *     call returns, so that prefill and decode run side by side; to the
- *     caller the call is one piece of `stream`'s work, including under CUDA
- *     graph capture.
+ *     until that work has finished.  Within a bf16
+ *     attention call the prefill and decode kernels run side by side: the
+ *     decode kernel starts on the SMs the prefill kernel leaves.
  *   - The caller owns every buffer it passes; the library keeps no pointer to
  *     any of them after the call returns.  The library owns one grow-only
  *     device workspace per device (step plan, split-KV partial results and

@@ -30,11 +30,6 @@ struct DeviceState {
   int64_t plan_q_rows = 0, plan_bt_width = 0;
   int plan_hq = 0, plan_hkv = 0, plan_reqs = 0;
   Sizes plan_sizes{};
-  // the prefill kernel runs on a stream of the library's own, forked from
-  // and joined back to the caller's stream (so that it runs beside the
-  // decode kernel)
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 std::mutex g_mu;
@@ -103,11 +98,6 @@ int current_state(DeviceState** out) {
       return fail(PKV_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
                   dev, prop.major, prop.minor);
     s.sms = prop.multiProcessorCount;
-    e = cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
-    e = cudaEventCreateWithFlags(&s.ev_fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.ev_join, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
     e = cudaMalloc(&s.err, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
     e = cudaMemset(s.err, 0, sizeof(int));
@@ -386,25 +376,18 @@ int run_locked(DeviceState* s, const void* q, int64_t q_row_stride, const void* 
   a.v_scale = kv_int8 ? v_scale : 1.f;
   cudaError_t e;
   if (!kv_int8) {
-    // The prefill items run beside the decode units: the prefill kernel on the
-    // library's side stream, forked from the caller's stream here and joined
-    // back after the merge, launched first so that its CTAs without an item
-    // leave their SMs to the decode grid.  (An int8 call has no prefill work:
-    // the plan reports such requests.)
-    if ((e = cudaEventRecord(s->ev_fork, st)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(s->side, s->ev_fork, 0)) != cudaSuccess)
-      return cuda_fail(e, "fork to the prefill stream");
-    e = traced(3, s->side, [&] { return launch_prefill(a, ws, s->sms, s->side); });
+    // Prefill first: its CTAs without an item leave their SMs at once, and
+    // the decode grid, launched as its programmatic dependent, fills them
+    // while the prefill items run (the bf16 decode kernel does not wait for
+    // the prefill grid; see pkv_decode.cu).  An int8 call has no prefill
+    // work: the plan reports such requests.
+    e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-    if ((e = cudaEventRecord(s->ev_join, s->side)) != cudaSuccess)
-      return cuda_fail(e, "record the prefill stream");
   }
   e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if (!kv_int8 && (e = cudaStreamWaitEvent(st, s->ev_join, 0)) != cudaSuccess)
-    return cuda_fail(e, "join the prefill stream");
   return PKV_OK;
 }
 

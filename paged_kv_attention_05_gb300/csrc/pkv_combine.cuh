@@ -19,11 +19,15 @@ namespace dev {
 __device__ __forceinline__ void combine_splits(const AttnArgs& a, const Workspace& ws, int warp_id,
                                                int n_warps) {
   const int G = a.hq / a.hkv;
-  const int max_rows = ws.hdr->max_rows;
-  const int n_items = ws.hdr->n_pairs * max_rows;
+  // (the plan's lists are read through L2: the plan kernel ran two launches
+  // before this one)
+  const int max_rows = __ldcg(&ws.hdr->max_rows);
+  const int n_items = __ldcg(&ws.hdr->n_pairs) * max_rows;
   const int lane = threadIdx.x & 31;
   for (int item = warp_id; item < n_items; item += n_warps) {
-    const SplitPair sp = ws.pairs[item / max_rows];
+    const int4 pw0 = __ldcg(reinterpret_cast<const int4*>(ws.pairs + item / max_rows));
+    const int4 pw1 = __ldcg(reinterpret_cast<const int4*>(ws.pairs + item / max_rows) + 1);
+    const SplitPair sp{pw0.x, pw0.y, pw0.z, pw0.w, pw1.x, pw1.y, pw1.z, pw1.w};
     const int row = item % max_rows;
     const int q0 = sp.q0;
     const int rows = sp.qn * G;

@@ -93,6 +93,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// a work unit written by the plan kernel, read through L2
+__device__ __forceinline__ DecUnit load_unit(const DecUnit* p) {
+  const int4 w0 = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 w1 = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  return DecUnit{w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+}
+
 // keep the bf16 halves of a register whose key index is below `valid`
 __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok_lo, int valid) {
   const uint32_t lo = tok_lo < valid ? 0x0000FFFFu : 0u;
@@ -131,13 +138,22 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
   }
-  // the set-up above overlaps the plan kernel; the work list is read after it
-  grid_dep_wait();
+  // This grid is the programmatic dependent of the prefill grid, which
+  // triggers it only after its own wait for the plan kernel: the plan is
+  // complete when any CTA of this grid runs, so no wait here (waiting would
+  // hold the decode units back until every prefill item is done).  What the
+  // plan and the kernels before it wrote is read through L2 (ld.global.cg).
+  // Each CTA waits for the prefill grid at its end instead, so that this
+  // grid finishing implies the prefill grid has finished (the merge kernel
+  // after this one, and whatever the stream runs next, rely on that).
   grid_dep_launch();
-  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
+  if (__ldcg(&ws.hdr->n_dec_units) == 0) {  // a batch without decode work (every CTA agrees)
+    grid_dep_wait();  // (as at the end: finishing implies the prefill grid has finished)
+    return;
+  }
   __syncthreads();
 
-  const int n_units = ws.hdr->n_dec_units;
+  const int n_units = __ldcg(&ws.hdr->n_dec_units);
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -148,7 +164,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     if (lane == 0) u = atomicAdd(&ws.hdr->dec_counter, 1);
     u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= n_units || *abort) break;
-    const DecUnit un = ws.units[u];
+    const DecUnit un = load_unit(ws.units + u);
     const int ug = un.gq & 0xFFFF;  // KV head
     const int uqn = un.gq >> 16;    // query tokens of the request
     const int k0 = un.k0, k1 = un.k1;
@@ -164,7 +180,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         const int p = lane + 32 * j;
         int blk = 0;
         if (p < npages) {
-          blk = __ldg(btrow + p);
+          blk = __ldcg(btrow + p);
           if (blk < 0 || (int64_t)blk >= a.num_blocks) {
             atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
             blk = 0;
@@ -410,6 +426,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       }
     }
   }
+  grid_dep_wait();  // finishing implies the prefill grid before this one has finished
 }
 
 // Groups above 16 heads: a unit's rows are the G heads of its one query token
@@ -479,13 +496,22 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
             make_uint4(0, 0, 0, 0);
     }
   }
-  // the set-up above overlaps the plan kernel; the work list is read after it
-  grid_dep_wait();
+  // This grid is the programmatic dependent of the prefill grid, which
+  // triggers it only after its own wait for the plan kernel: the plan is
+  // complete when any CTA of this grid runs, so no wait here (waiting would
+  // hold the decode units back until every prefill item is done).  What the
+  // plan and the kernels before it wrote is read through L2 (ld.global.cg).
+  // Each CTA waits for the prefill grid at its end instead, so that this
+  // grid finishing implies the prefill grid has finished (the merge kernel
+  // after this one, and whatever the stream runs next, rely on that).
   grid_dep_launch();
-  if (ws.hdr->n_dec_units == 0) return;  // a batch without decode work (every CTA agrees)
+  if (__ldcg(&ws.hdr->n_dec_units) == 0) {  // a batch without decode work (every CTA agrees)
+    grid_dep_wait();  // (as at the end: finishing implies the prefill grid has finished)
+    return;
+  }
   __syncthreads();
 
-  const int n_units = ws.hdr->n_dec_units;
+  const int n_units = __ldcg(&ws.hdr->n_dec_units);
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -507,7 +533,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
       u = uslot[slot];
     }
     if (u >= n_units || *abort) break;
-    const DecUnit un = ws.units[u];
+    const DecUnit un = load_unit(ws.units + u);
     const int ug = un.gq & 0xFFFF;  // KV head
     const int k0 = un.k0, k1 = un.k1;
     const int p0 = k0 / kBlockSize;
@@ -525,7 +551,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
         const int p = lane + 32 * j;
         int blk = 0;
         if (p < npages) {
-          blk = __ldg(btrow + p);
+          blk = __ldcg(btrow + p);
           if (blk < 0 || (int64_t)blk >= a.num_blocks) {
             atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
             blk = 0;
@@ -733,6 +759,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
       }
     }
   }
+  grid_dep_wait();  // finishing implies the prefill grid before this one has finished
 }
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {

@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   grid_dep_wait();  // the work lists
+  // the plan is complete: the decode grid (this launch's dependent) may start
+  // on the SMs this grid leaves (every CTA without an item exits soon)
+  grid_dep_launch();
   if (ws.hdr->n_pre_entries == 0) return;  // a step without prefill work (every CTA agrees)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
