@@ -19,8 +19,9 @@
  *     launch, so a kernel may begin its set-up while the work before it on
  *     the stream is finishing, but it reads and writes no global memory
  *     until that work has finished.  Within a bf16
- *     attention call the prefill and decode kernels run side by side: the
- *     decode kernel starts on the SMs the prefill kernel leaves.
+ *     attention call that has prefill work, the decode kernel leaves some
+ *     SMs to the prefill kernel, whose items run there beside the decode
+ *     units.
  *   - The caller owns every buffer it passes; the library keeps no pointer to
  *     any of them after the call returns.  The library owns one grow-only
  *     device workspace per device (step plan, split-KV partial results and

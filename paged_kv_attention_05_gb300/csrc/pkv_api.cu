@@ -374,20 +374,22 @@ int run_locked(DeviceState* s, const void* q, int64_t q_row_stride, const void* 
   a.kv_int8 = kv_int8;
   a.k_scale = kv_int8 ? k_scale : 1.f;
   a.v_scale = kv_int8 ? v_scale : 1.f;
-  cudaError_t e;
-  if (!kv_int8) {
-    // Prefill first: its CTAs without an item leave their SMs at once, and
-    // the decode grid, launched as its programmatic dependent, fills them
-    // while the prefill items run (the bf16 decode kernel does not wait for
-    // the prefill grid; see pkv_decode.cu).  An int8 call has no prefill
-    // work: the plan reports such requests.
+  // Decode first.  When the step also has prefill work, the decode grid
+  // leaves some SMs to it at once and the prefill grid (its programmatic
+  // dependent) runs its items there beside the decode units; the prefill
+  // kernel merges the split decode results at its end, once the decode grid
+  // has finished (see pkv_decode.cu and pkv_prefill.cu).  An int8 call has no
+  // prefill work (the plan reports such requests): its merge is a launch of
+  // its own.
+  cudaError_t e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (kv_int8) {
+    e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  } else {
     e = traced(3, st, [&] { return launch_prefill(a, ws, s->sms, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
-  e = traced(2, st, [&] { return launch_decode(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  e = traced(4, st, [&] { return launch_combine(a, ws, s->sms, st); });
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return PKV_OK;
 }
 

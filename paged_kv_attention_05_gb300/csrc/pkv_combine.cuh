@@ -1,5 +1,6 @@
-// The merge of split-KV decode results, run by the combine kernel after the
-// decode kernel.
+// The merge of split-KV decode results, run after the decode kernel: by every
+// warp of the prefill kernel's launch at its end (bf16 calls), by the combine
+// kernel (int8 calls).
 #pragma once
 
 #include "pkv_device.cuh"

@@ -37,8 +37,9 @@
 //     the fragments, so stale or NaN cache slots never reach the product.
 //   * A unit that covers a whole request writes the bf16 output; one split of
 //     several writes (max, sum, unnormalised output) in fp32 to the workspace,
-//     and the merge of the splits (pkv_combine.cuh) runs afterwards, in the
-//     combine kernel below.  Every mbarrier wait is bounded.
+//     and the merge of the splits (pkv_combine.cuh) runs afterwards: at the
+//     end of the prefill kernel's launch for bf16 calls, in the combine
+//     kernel below for int8 calls.  Every mbarrier wait is bounded.
 // The int8-cache variant of the decode kernel is in pkv_decode_i8.cu; it
 // shares the plan, the work units and the merge.
 #include "pkv_combine.cuh"
@@ -93,7 +94,19 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// a work unit written by the plan kernel, read through L2
+// Whether this CTA leaves its SM to the prefill grid, launched after this
+// one as its programmatic dependent: when the step has prefill items, the
+// first min(items, SMs / 2) CTAs of the decode grid exit at once, so that
+// the prefill items run on their SMs beside the decode units on the others
+// (the prefill kernel does not wait for this grid before its items).  Every
+// CTA computes the same from the plan header (read after the plan wait).
+__device__ __forceinline__ bool leaves_sm_to_prefill(const AttnArgs& a, const Workspace& ws) {
+  const int G = a.hq / a.hkv;
+  const int items = ws.hdr->n_pre_entries * (G % 2 == 0 ? a.hq / 2 : a.hq);
+  return items > 0 && (int)blockIdx.x < min(items, (int)gridDim.x / 2);
+}
+
+// a work unit written by the plan kernel
 __device__ __forceinline__ DecUnit load_unit(const DecUnit* p) {
   const int4 w0 = __ldcg(reinterpret_cast<const int4*>(p));
   const int4 w1 = __ldcg(reinterpret_cast<const int4*>(p) + 1);
@@ -138,22 +151,13 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
   }
-  // This grid is the programmatic dependent of the prefill grid, which
-  // triggers it only after its own wait for the plan kernel: the plan is
-  // complete when any CTA of this grid runs, so no wait here (waiting would
-  // hold the decode units back until every prefill item is done).  What the
-  // plan and the kernels before it wrote is read through L2 (ld.global.cg).
-  // Each CTA waits for the prefill grid at its end instead, so that this
-  // grid finishing implies the prefill grid has finished (the merge kernel
-  // after this one, and whatever the stream runs next, rely on that).
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  grid_dep_wait();
   grid_dep_launch();
-  if (__ldcg(&ws.hdr->n_dec_units) == 0) {  // a batch without decode work (every CTA agrees)
-    grid_dep_wait();  // (as at the end: finishing implies the prefill grid has finished)
-    return;
-  }
+  if (leaves_sm_to_prefill(a, ws) || ws.hdr->n_dec_units == 0) return;
   __syncthreads();
 
-  const int n_units = __ldcg(&ws.hdr->n_dec_units);
+  const int n_units = ws.hdr->n_dec_units;
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         const int p = lane + 32 * j;
         int blk = 0;
         if (p < npages) {
-          blk = __ldcg(btrow + p);
+          blk = __ldg(btrow + p);
           if (blk < 0 || (int64_t)blk >= a.num_blocks) {
             atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
             blk = 0;
@@ -426,7 +430,6 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       }
     }
   }
-  grid_dep_wait();  // finishing implies the prefill grid before this one has finished
 }
 
 // Groups above 16 heads: a unit's rows are the G heads of its one query token
@@ -496,22 +499,13 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
             make_uint4(0, 0, 0, 0);
     }
   }
-  // This grid is the programmatic dependent of the prefill grid, which
-  // triggers it only after its own wait for the plan kernel: the plan is
-  // complete when any CTA of this grid runs, so no wait here (waiting would
-  // hold the decode units back until every prefill item is done).  What the
-  // plan and the kernels before it wrote is read through L2 (ld.global.cg).
-  // Each CTA waits for the prefill grid at its end instead, so that this
-  // grid finishing implies the prefill grid has finished (the merge kernel
-  // after this one, and whatever the stream runs next, rely on that).
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  grid_dep_wait();
   grid_dep_launch();
-  if (__ldcg(&ws.hdr->n_dec_units) == 0) {  // a batch without decode work (every CTA agrees)
-    grid_dep_wait();  // (as at the end: finishing implies the prefill grid has finished)
-    return;
-  }
+  if (leaves_sm_to_prefill(a, ws) || ws.hdr->n_dec_units == 0) return;
   __syncthreads();
 
-  const int n_units = __ldcg(&ws.hdr->n_dec_units);
+  const int n_units = ws.hdr->n_dec_units;
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -551,7 +545,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
         const int p = lane + 32 * j;
         int blk = 0;
         if (p < npages) {
-          blk = __ldcg(btrow + p);
+          blk = __ldg(btrow + p);
           if (blk < 0 || (int64_t)blk >= a.num_blocks) {
             atomicOr(ws.err, PKV_DEV_ERR_BLOCK_ID);
             blk = 0;
@@ -759,7 +753,6 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
       }
     }
   }
-  grid_dep_wait();  // finishing implies the prefill grid before this one has finished
 }
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Workspace ws) {

@@ -188,15 +188,16 @@ int decode_i8_warps(int group);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
 // Programmatic dependent launch.  The attention kernels after the cache write
-// (plan, prefill, decode, merge) are launched with programmatic stream
+// (plan, decode, prefill; the merge for int8 calls) are launched with programmatic stream
 // serialisation: a kernel's CTAs may start while the kernel before it in the
 // stream is still running, do their set-up (barriers, shared-memory
 // clearing), and then wait in grid_dep_wait() until that kernel has finished
 // and its writes are visible, before reading anything it produced.  Each such
 // kernel waits before it finishes, so finishing implies that every kernel
-// before it has finished too.  (The bf16 decode kernel, the prefill kernel's
-// dependent, waits only at its end: the prefill grid triggers it after its
-// own wait for the plan, so the decode units run beside the prefill items.)
+// before it has finished too.  (The prefill kernel, the decode kernel's
+// dependent, reads the plan without waiting, since the decode grid triggers
+// it after its own wait for the plan, and waits for the decode grid only
+// before its final merge: its items run beside the decode units.)
 // Launched without the attribute, the wait returns at once.
 template <typename... Params, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,

@@ -160,9 +160,8 @@ extern "C" int pkv_attention_noalloc(const void* q, int64_t q_row_stride, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the kernels of pkv_attention, one after the other on the caller's stream
   if ((e = launch_plan(a, ws, decode_workers(group, 0, sms), st)) != cudaSuccess ||
-      (e = launch_prefill(a, ws, sms, st)) != cudaSuccess ||
       (e = launch_decode(a, ws, sms, st)) != cudaSuccess ||
-      (e = launch_combine(a, ws, sms, st)) != cudaSuccess)
+      (e = launch_prefill(a, ws, sms, st)) != cudaSuccess)  // (merges the splits at its end)
     return noalloc_fail(PKV_ERR_CUDA, "kernel launch failed");
   return PKV_OK;
 }

@@ -44,6 +44,7 @@
 //               through a per-warp staging area (whole 64-byte row pieces).
 // Every mbarrier wait is bounded; on expiry the kernel records
 // PKV_DEV_ERR_TIMEOUT, stops issuing work, frees its TMEM and returns.
+#include "pkv_combine.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -96,6 +97,13 @@ struct Item {
   int g, q0, n, L;
   int ctx, nkv, pad0, pad1;
 };
+
+// a prefill entry written by the plan kernel, read through L2
+__device__ __forceinline__ PreEntry load_entry(const PreEntry* p) {
+  const int4 w0 = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 w1 = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  return PreEntry{w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
@@ -208,11 +216,20 @@ __device__ __forceinline__ void tmem_wait_st() {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
-  grid_dep_wait();  // the work lists
-  // the plan is complete: the decode grid (this launch's dependent) may start
-  // on the SMs this grid leaves (every CTA without an item exits soon)
-  grid_dep_launch();
-  if (ws.hdr->n_pre_entries == 0) return;  // a step without prefill work (every CTA agrees)
+  // This grid is the programmatic dependent of the decode grid, which
+  // triggers it after its own wait for the plan kernel: the plan is complete
+  // when any CTA here runs, so the items start without waiting for the decode
+  // grid (which leaves some SMs to them, see pkv_decode.cu); what the plan and
+  // the kernels before it wrote is read through L2 (ld.global.cg).  The split
+  // decode results are merged at the end, once the decode grid has finished
+  // (so this grid finishing implies that every kernel before it has).
+  const int n_pre = __ldcg(&ws.hdr->n_pre_entries);
+  if (n_pre == 0) {  // a step without prefill work (every CTA agrees)
+    grid_dep_wait();
+    combine_splits(a, ws, blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5),
+                   gridDim.x * (kThreads / 32));
+    return;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)ctl[0];
-  const int n_items = ws.hdr->n_pre_entries * per_entry;
+  const int n_items = n_pre * per_entry;
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
     w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
     const PreEntry none{-1, 0, 0, 0, 0, 0, 0, 0};
-    PreEntry e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
+    PreEntry e_nxt = w_nxt < n_items ? load_entry(ws.pre + w_nxt / per_entry) : none;
     for (uint32_t it_cnt = 0;; ++it_cnt) {
       const int slot = it_cnt & 1;
       const int w = w_nxt;
@@ -301,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next item's cursor and entry (consumed after this item)
       if (lane == 0) w_nxt = atomicAdd(&ws.hdr->pre_counter, 1);
       w_nxt = __shfl_sync(0xffffffffu, w_nxt, 0);
-      e_nxt = w_nxt < n_items ? ws.pre[w_nxt / per_entry] : none;
+      e_nxt = w_nxt < n_items ? load_entry(ws.pre + w_nxt / per_entry) : none;
       const int* btrow = a.bt + (int64_t)it.r * a.bt_width;
       const int row0 = it.q0 + it.qt * kPreTileQ;
       // Q tiles, once the previous item's last S has read them
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // lane p < pages(j) holds the block id of page p of tile j
       auto tile_pages = [&](int j) { return min(8, (it.L - j * kTileK + 15) / 16); };
-      int blk_nxt = lane < tile_pages(0) ? __ldg(btrow + lane) : 0;
+      int blk_nxt = lane < tile_pages(0) ? __ldcg(btrow + lane) : 0;
       for (int j = 0; ok && j < it.nkv; ++j) {
         const uint32_t c = tile_cnt++;
         const int s = c % kStages;
@@ -333,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tail = key0 + kTileK > it.L;
         int blk = blk_nxt;
         if (j + 1 < it.nkv && lane < tile_pages(j + 1))
-          blk_nxt = __ldg(btrow + ((key0 + kTileK) >> 4) + lane);
+          blk_nxt = __ldcg(btrow + ((key0 + kTileK) >> 4) + lane);
         if (c >= (uint32_t)kStages &&
             !mbar_wait_warp(bar(B_KE + s), ((c / kStages) - 1) & 1, abort, ws.err)) {
           ok = false;
@@ -727,6 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
                  "r"(kTmemCols));
   }
+  // the split decode results, once the decode grid has finished
+  grid_dep_wait();
+  combine_splits(a, ws, blockIdx.x * (kThreads / 32) + warp, gridDim.x * (kThreads / 32));
 }
 
 }  // namespace
