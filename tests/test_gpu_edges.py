@@ -79,3 +79,37 @@ def test_first_token_sees_only_itself(hq, hkv):
     G = hq // hkv
     for h in range(hq):
         assert np.array_equal(got[:, h], v[:, h // G]), "head %d" % h
+
+
+def test_steps_back_to_back_without_a_sync():
+    """Four different steps enqueued one after another on one stream with no
+    host synchronisation between them: each step's plan rewrites the work
+    lists at the same workspace addresses, and the prefill grid reads them
+    beside the running decode grid (without waiting for it).  Every step's
+    rows must match its own oracle: nothing read is left over from the step
+    before."""
+    specs = [W.custom([700, 0, 33], [1, 200, 1], 16, 4, seed=1201, pad_tokens=1),
+             W.custom([0, 1500, 9, 0], [300, 1, 1, 17], 16, 4, seed=1202),
+             W.custom([4000] * 6, [1] * 6, 16, 4, seed=1203),
+             W.custom([100, 0, 2048, 5], [129, 64, 1, 1], 16, 4, seed=1204, pad_tokens=3)]
+    steps, refs, dss = [], [], []
+    for sp in specs:
+        step = W.build(sp)
+        kc, vc = step.key_cache.copy(), step.value_cache.copy()
+        assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+        ref, err = oracle.attention(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                    step.block_table, step.num_reqs, step.scale)
+        assert err == 0
+        steps.append(step)
+        refs.append(ref)
+        dss.append(DeviceStep(step))
+    torch.cuda.synchronize()
+    for ds in dss:               # enqueued back to back, one stream, no sync
+        ds.write()
+        ds.attention()
+    assert pkv.pkv_get_error() == 0
+    for i, (step, ref, ds) in enumerate(zip(steps, refs, dss)):
+        got = ds.out_f64()
+        n = int(step.query_start_loc[-1])
+        assert_close(got[:n], ref[:n], "step %d of four" % i)
+        assert np.isnan(got[n:]).all()
