@@ -103,6 +103,11 @@ def test_steps_back_to_back_without_a_sync():
         steps.append(step)
         refs.append(ref)
         dss.append(DeviceStep(step))
+    # room for the largest of the four, so that no call grows the workspace
+    # (growing it synchronises the device)
+    pkv.pkv_reserve_workspace(max(st.num_reqs for st in steps),
+                              max(st.qkv.shape[0] for st in steps),
+                              max(st.block_table.shape[1] for st in steps), 16, 4)
     torch.cuda.synchronize()
     for ds in dss:               # enqueued back to back, one stream, no sync
         ds.write()
