@@ -96,14 +96,22 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 
 // Whether this CTA leaves its SM to the prefill grid, launched after this
 // one as its programmatic dependent: when the step has prefill items, the
-// first min(items, SMs / 2) CTAs of the decode grid exit at once, so that
-// the prefill items run on their SMs beside the decode units on the others
-// (the prefill kernel does not wait for this grid before its items).  Every
+// first P CTAs of the decode grid exit at once, so that the prefill items
+// run on their SMs beside the decode units on the others (the prefill kernel
+// does not wait for this grid before its items).  P is the number of SMs on
+// which the prefill's key-tile steps (items x tiles) fit into the longest
+// item's chain, at most one per item and half of the SMs: fewer would
+// lengthen the prefill, more would sit idle once the items are done.  Every
 // CTA computes the same from the plan header (read after the plan wait).
 __device__ __forceinline__ bool leaves_sm_to_prefill(const AttnArgs& a, const Workspace& ws) {
   const int G = a.hq / a.hkv;
-  const int items = ws.hdr->n_pre_entries * (G % 2 == 0 ? a.hq / 2 : a.hq);
-  return items > 0 && (int)blockIdx.x < min(items, (int)gridDim.x / 2);
+  const int per_entry = G % 2 == 0 ? a.hq / 2 : a.hq;  // items (query head pairs) per entry
+  const int items = ws.hdr->n_pre_entries * per_entry;
+  if (items == 0) return false;
+  const long long steps = (long long)ws.hdr->pre_tiles * per_entry;
+  const int longest = max(ws.hdr->pre_max_tiles, 1);
+  const int p = (int)min((long long)min(items, (int)gridDim.x / 2), (steps + longest - 1) / longest);
+  return (int)blockIdx.x < max(p, 1);
 }
 
 // a work unit written by the plan kernel

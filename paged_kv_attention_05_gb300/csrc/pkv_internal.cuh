@@ -63,7 +63,9 @@ struct PlanHeader {
   int chunk;
   int n_pairs;      // split pairs to merge
   int max_rows;     // most query rows of one split pair (qn * G)
-  int pad[9];
+  int pre_tiles;    // 128-key tiles of all prefill entries (one query head pair each)
+  int pre_max_tiles;  // key tiles of the longest prefill entry
+  int pad[7];
 };
 
 // Device pointers into the per-device workspace.

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // classification for pass 2)
   long long dec_keys = 0;
   int dec_reqs = 0, dec_lmax = 0, dec_rmax = 0;  // rmax: most query rows of a decode
+  int pre_tiles = 0, pre_max = 0;  // key tiles of the prefill entries: sum, longest
   ReqInfo first{0, 0, 0, 0, 0};
   for (int r = tid; r < a.num_reqs; r += nt) {
     ReqInfo ri = classify(a, r);
@@ -152,6 +153,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       dec_reqs += 1;
       dec_lmax = max(dec_lmax, ri.L);
       dec_rmax = max(dec_rmax, ri.n * (a.hq / a.hkv));
+    } else if (ri.kind == 2) {
+      // query tile t (rows up to min(128 (t + 1), n)) reads ctx + its last row
+      // keys; the last tile reads them all
+      const int ctx = ri.L - ri.n;
+      for (int t = 0; t * kPreTileQ < ri.n; ++t)
+        pre_tiles += (ctx + min(kPreTileQ * (t + 1), ri.n) + kPreTileQ - 1) / kPreTileQ;
+      pre_max = max(pre_max, (ri.L + kPreTileQ - 1) / kPreTileQ);
     }
   }
 #pragma unroll
@@ -160,31 +168,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     dec_reqs += __shfl_xor_sync(0xffffffffu, dec_reqs, o);
     dec_lmax = max(dec_lmax, __shfl_xor_sync(0xffffffffu, dec_lmax, o));
     dec_rmax = max(dec_rmax, __shfl_xor_sync(0xffffffffu, dec_rmax, o));
+    pre_tiles += __shfl_xor_sync(0xffffffffu, pre_tiles, o);
+    pre_max = max(pre_max, __shfl_xor_sync(0xffffffffu, pre_max, o));
   }
-  __shared__ int red_n[32], red_l[32], red_r[32];
+  __shared__ int red_n[32], red_l[32], red_r[32], red_t[32], red_m[32];
   if ((tid & 31) == 0) {
     red[tid >> 5] = dec_keys;
     red_n[tid >> 5] = dec_reqs;
     red_l[tid >> 5] = dec_lmax;
     red_r[tid >> 5] = dec_rmax;
+    red_t[tid >> 5] = pre_tiles;
+    red_m[tid >> 5] = pre_max;
   }
   __syncthreads();
   if (tid < 32) {
     long long x = tid < nw ? red[tid] : 0;
     int n = tid < nw ? red_n[tid] : 0, l = tid < nw ? red_l[tid] : 0;
     int rr = tid < nw ? red_r[tid] : 0;
+    int pt = tid < nw ? red_t[tid] : 0, pm = tid < nw ? red_m[tid] : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       x += __shfl_xor_sync(0xffffffffu, x, o);
       n += __shfl_xor_sync(0xffffffffu, n, o);
       l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
       rr = max(rr, __shfl_xor_sync(0xffffffffu, rr, o));
+      pt += __shfl_xor_sync(0xffffffffu, pt, o);
+      pm = max(pm, __shfl_xor_sync(0xffffffffu, pm, o));
     }
     if (tid == 0) {
       red[0] = x;
       red_n[0] = n;
       red_l[0] = l;
       red_r[0] = rr;
+      red_t[0] = pt;
+      red_m[0] = pm;
     }
   }
   __syncthreads();
@@ -401,6 +418,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     ws.hdr->chunk = chunk;
     ws.hdr->n_pairs = fits ? pair_carry : 0;
     ws.hdr->max_rows = s_max_rows;
+    ws.hdr->pre_tiles = red_t[0];
+    ws.hdr->pre_max_tiles = red_m[0];
   }
 }
 
