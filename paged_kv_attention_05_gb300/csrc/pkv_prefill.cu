@@ -84,13 +84,14 @@ enum {
   B_IF = 22,  // [2] item slot published
   B_IE = 24,  // [2] item slot released
   B_XP = 26,  // [4] exchange between the two softmax warps of a row quarter
-  B_LF = 30,  // [2] row sums of tile x written for the epilogue
+  B_LF = 30,  // [2] row sums of tile x written for the epilogue, even items
   kNumBars = 32
 };
 constexpr int kOffItems = kOffBar + kNumBars * 8;  // 2 item slots
 constexpr int kOffXch = kOffItems + 2 * 48;        // [4 quarters][2 slots][2 halves][32] floats
 constexpr int kOffCtl = kOffXch + 4 * 2 * 2 * 32 * 4;  // TMEM address, abort flag
-constexpr int kSmemBytes = kOffCtl + 16 + 1024;    // + alignment slack
+constexpr int kOffBarLF1 = kOffCtl + 16;           // [2] the same for odd items
+constexpr int kSmemBytes = kOffBarLF1 + 16 + 1024;  // + alignment slack
 
 struct Item {
   int r, qt, ha, hb;  // hb < 0: single-tile item
@@ -236,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + kOffBar;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  // row sums of tile x of item it_cnt written
+  auto lf_bar = [&](uint32_t it_cnt, int x) {
+    return (it_cnt & 1) ? sbase + kOffBarLF1 + 8u * (uint32_t)x : bar(B_LF + x);
+  };
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + kOffCtl);
   volatile int* abort = ctl + 1;  // ctl[0] = TMEM base address
   Item* items = reinterpret_cast<Item*>(smem + kOffItems);
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_PF + x), 8);  // one arrival per softmax warp (each writes half of P)
       mbar_init(bar(B_OE + x), 4);  // one arrival per epilogue warp
       mbar_init(bar(B_LF + x), 8);  // one arrival per softmax warp
+      mbar_init(sbase + kOffBarLF1 + 8 * x, 8);
       mbar_init(bar(B_IE + x), 1 + 8 + 4);  // MMA warp, softmax warps, epilogue warps
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_XP + i), 2);
@@ -639,10 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // this warp's partial row sums of the item, for the epilogue warps
+      // (one barrier per item parity: the softmax may finish the next item
+      // before the epilogue has waited for this one, and one barrier would
+      // then have completed two phases, which a parity wait cannot tell
+      // apart from none)
       for (int x = 0; x < nx; ++x) {
         lsum[(((it_cnt & 1) * 2 + x) * 2 + hf) * 128 + row] = l_part[x];
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_LF + x));
+        if (lane == 0) mbar_arrive(lf_bar(it_cnt, x));
       }
     }
   } else {
@@ -674,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < nx && ok; ++x) {
         const uint32_t par = o_cnt[x]++ & 1;
         if (!mbar_wait_warp(bar(B_OF + x), par, abort, ws.err) ||
-            !mbar_wait_warp(bar(B_LF + x), par, abort, ws.err)) {
+            !mbar_wait_warp(lf_bar(it_cnt, x), (it_cnt >> 1) & 1, abort, ws.err)) {
           ok = false;
           break;
         }

@@ -118,3 +118,35 @@ def test_steps_back_to_back_without_a_sync():
         n = int(step.query_start_loc[-1])
         assert_close(got[:n], ref[:n], "step %d of four" % i)
         assert np.isnan(got[n:]).all()
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "mixed_chunked"])
+def test_many_mixed_steps_back_to_back(name):
+    """Twenty thousand steps of a small mixed batch enqueued back to back,
+    the error word read once at the end.  In these steps a prefill CTA often
+    takes two items in a row, the second with a single key tile, while the
+    decode grid keeps HBM busy and the epilogue warps' stores are slow: the
+    softmax warps may then finish the second item before the epilogue warps
+    have waited for the first one's row sums, and each item's signal must
+    still be told apart (a wait that missed it would give up after its time
+    limit and set PKV_DEV_ERR_TIMEOUT).  The last step's rows match the
+    oracle."""
+    step = W.build(W.spec(name))
+    kc, vc = step.key_cache.copy(), step.value_cache.copy()
+    assert oracle.write(step.k, step.v, kc, vc, step.slot_mapping) == 0
+    ref, err = oracle.attention(step.q, kc, vc, step.query_start_loc, step.seq_lens,
+                                step.block_table, step.num_reqs, step.scale)
+    assert err == 0
+    ds = DeviceStep(step)
+    ds.write()
+    ds.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error() == 0
+    for _ in range(20000):
+        ds.write()
+        ds.attention()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error() == 0
+    n = int(step.query_start_loc[-1])
+    got = ds.out_f64()
+    assert_close(got[:n], ref[:n], name + " after 20000 steps")
