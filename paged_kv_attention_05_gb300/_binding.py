@@ -85,11 +85,33 @@ def _check(rc):
         raise PkvError(rc, msg)
 
 
+_torch = None
+_raw_stream = None  # () -> the current device's current stream handle, as an int
+
+
+def _T():
+    """torch, imported on first use (the binding loads without it)."""
+    global _torch, _raw_stream
+    if _torch is None:
+        import torch
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if get_dev is not None and get_raw is not None:
+            _raw_stream = lambda: get_raw(get_dev())  # noqa: E731
+        else:
+            _raw_stream = lambda: torch.cuda.current_stream().cuda_stream  # noqa: E731
+        _torch = torch
+    return _torch
+
+
 def _stream(stream):
-    import torch
+    """The stream handle for a call: torch's current stream when none is given
+    (read through torch's raw getter: a Stream object costs microseconds)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        if _raw_stream is None:
+            _T()
+        return _raw_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _require(t, dtype, name, device=True):
@@ -112,28 +134,45 @@ def _per_row(t):
 
 def _rows3(t, name):
     """Row stride of a [rows, heads, 128] tensor whose per-row block is contiguous."""
-    if t.dim() == 2:
-        if t.stride(1) != 1:
+    st, sh = t.stride(), t.shape
+    if len(st) == 2:
+        if st[1] != 1:
             raise ValueError("%s: last dimension must be contiguous" % name)
-        return t.stride(0)
-    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        return st[0]
+    if len(st) != 3 or st[2] != 1 or st[1] != sh[2]:
         raise ValueError("%s must be [rows, heads, head_size] with contiguous rows" % name)
-    return t.stride(0)
+    return st[0]
+
+
+def _all_on_device(dtype, *ts):
+    """True when every tensor has this dtype and lives on a CUDA device (the
+    common case, tested in one pass; callers fall back to the per-argument
+    checks, which name the culprit, when it is False)."""
+    try:
+        for t in ts:
+            if t.dtype is not dtype or not t.is_cuda:
+                return False
+    except AttributeError:
+        return False
+    return True
 
 
 def pkv_write(k, v, key_cache, value_cache, slot_mapping, n_tokens=None, stream=None):
     """Scatters k/v ([n, Hkv, 128] bf16) into the caches at slot_mapping (int64)."""
-    import torch
-    for t, n in ((k, "k"), (v, "v"), (key_cache, "key_cache"), (value_cache, "value_cache")):
-        _require(t, torch.bfloat16, n)
-    _require(slot_mapping, torch.int64, "slot_mapping")
-    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+    torch = _T()
+    if not (_all_on_device(torch.bfloat16, k, v, key_cache, value_cache) and
+            _all_on_device(torch.int64, slot_mapping)):
+        for t, n in ((k, "k"), (v, "v"), (key_cache, "key_cache"), (value_cache, "value_cache")):
+            _require(t, torch.bfloat16, n)
+        _require(slot_mapping, torch.int64, "slot_mapping")
+    ks = key_cache.shape
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or len(ks) != 4:
         raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
-    if key_cache.shape != value_cache.shape:
+    if ks != value_cache.shape:
         raise ValueError("key_cache and value_cache shapes differ")
     if not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be contiguous")
-    nb, bs, hkv, d = key_cache.shape
+    nb, bs, hkv, d = ks
     n = slot_mapping.shape[0] if n_tokens is None else int(n_tokens)
     if n > slot_mapping.shape[0] or n > k.shape[0] or n > v.shape[0]:
         raise ValueError("n_tokens exceeds the rows of k/v/slot_mapping")
@@ -146,33 +185,42 @@ def pkv_attention(q, key_cache, value_cache, query_start_loc, seq_lens, block_ta
                   scale, out, stream=None):
     """Causal varlen attention of q ([T, Hq, 128] bf16) over the paged cache
     into out ([T, Hq, 128] bf16); see include/pkv.h for the contract."""
-    import torch
-    for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"), (out, "out")):
-        _require(t, torch.bfloat16, n)
-    for t, n in ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
-                 (block_table, "block_table")):
-        _require(t, torch.int32, n)
+    torch = _T()
+    metadata = ((query_start_loc, "query_start_loc"), (seq_lens, "seq_lens"),
+                (block_table, "block_table"))
+    if not (_all_on_device(torch.bfloat16, q, key_cache, value_cache, out) and
+            _all_on_device(torch.int32, query_start_loc, seq_lens, block_table)):
+        for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"),
+                     (out, "out")):
+            _require(t, torch.bfloat16, n)
+        for t, n in metadata:
+            _require(t, torch.int32, n)
+    for t, n in metadata:
         if not t.is_contiguous():
             raise ValueError("%s must be contiguous" % n)
-    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or key_cache.dim() != 4:
+    ks = key_cache.shape
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()) or len(ks) != 4:
         raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, head_size]")
-    if key_cache.shape != value_cache.shape:
+    if ks != value_cache.shape:
         raise ValueError("key_cache and value_cache shapes differ")
-    nb, bs, hkv, d = key_cache.shape
-    if q.dim() != 3:
+    nb, bs, hkv, d = ks
+    qs = q.shape
+    if len(qs) != 3:
         raise ValueError("q must be [rows, num_heads, head_size]")
-    rows, hq, _ = q.shape
+    rows, hq, _ = qs
     if out.shape[0] < rows or _per_row(out) != hq * d:
         raise ValueError("out must hold [rows, num_heads * head_size]")
-    bt_width = block_table.shape[1] if block_table.dim() == 2 else block_table.shape[0]
-    if int(num_reqs) > 0 and (query_start_loc.numel() < int(num_reqs) + 1 or
-                              seq_lens.numel() < int(num_reqs) or
-                              (block_table.dim() == 2 and block_table.shape[0] < int(num_reqs))):
+    bts = block_table.shape
+    bt_width = bts[1] if len(bts) == 2 else bts[0]
+    num_reqs = int(num_reqs)
+    if num_reqs > 0 and (query_start_loc.numel() < num_reqs + 1 or
+                         seq_lens.numel() < num_reqs or
+                         (len(bts) == 2 and bts[0] < num_reqs)):
         raise ValueError("metadata shorter than num_reqs")
     _check(load().pkv_attention(q.data_ptr(), _rows3(q, "q"), rows, hq, key_cache.data_ptr(),
                                 value_cache.data_ptr(), nb, bs, hkv, d,
                                 query_start_loc.data_ptr(), seq_lens.data_ptr(),
-                                block_table.data_ptr(), bt_width, int(num_reqs), float(scale),
+                                block_table.data_ptr(), bt_width, num_reqs, float(scale),
                                 out.data_ptr(), _rows3(out, "out"), _stream(stream)))
 
 
@@ -257,10 +305,13 @@ def pkv_plan(q_rows, num_heads, num_kv_heads, query_start_loc, seq_lens, block_t
 
 def pkv_attention_planned(q, key_cache, value_cache, block_table, scale, out, stream=None):
     """One layer's attention on the current step plan (pkv_plan)."""
-    import torch
-    for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"), (out, "out")):
-        _require(t, torch.bfloat16, n)
-    _require(block_table, torch.int32, "block_table")
+    torch = _T()
+    if not (_all_on_device(torch.bfloat16, q, key_cache, value_cache, out) and
+            _all_on_device(torch.int32, block_table)):
+        for t, n in ((q, "q"), (key_cache, "key_cache"), (value_cache, "value_cache"),
+                     (out, "out")):
+            _require(t, torch.bfloat16, n)
+        _require(block_table, torch.int32, "block_table")
     if not block_table.is_contiguous():
         raise ValueError("block_table must be contiguous")
     nb, bs, hkv, d = _caches(key_cache, value_cache, torch.bfloat16)
