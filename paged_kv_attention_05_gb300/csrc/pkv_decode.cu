@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
+  const uint64_t pol = l2_evict_first();  // K/V pages are read once
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -239,10 +240,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         fence_async_smem();
         const uint32_t st = wbase + s * C::kStageBytes;
         mbar_expect_tx(full_bar(s), C::kStageBytes);
-        tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
-        tma_load_4d(st + kBox, &tm_k, full_bar(s), 64, ug, 0, blk);
-        tma_load_4d(st + 2 * kBox, &tm_v, full_bar(s), 0, ug, 0, blk);
-        tma_load_4d(st + 3 * kBox, &tm_v, full_bar(s), 64, ug, 0, blk);
+        tma_load_4d_hint(st, &tm_k, full_bar(s), 0, ug, 0, blk, pol);
+        tma_load_4d_hint(st + kBox, &tm_k, full_bar(s), 64, ug, 0, blk, pol);
+        tma_load_4d_hint(st + 2 * kBox, &tm_v, full_bar(s), 0, ug, 0, blk, pol);
+        tma_load_4d_hint(st + 3 * kBox, &tm_v, full_bar(s), 64, ug, 0, blk, pol);
       }
     };
     for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
@@ -514,6 +515,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
+  const uint64_t pol = l2_evict_first();  // K/V pages are read once
   const float sl2 = a.scale * kLog2e;
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -581,10 +583,10 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
       if (lane == 0) {
         const uint32_t sa = pbase + st * kPage;
         mbar_expect_tx(full_bar(st), kPage);
-        tma_load_4d(sa, &tm_k, full_bar(st), 0, ug, 0, blk);
-        tma_load_4d(sa + kBox, &tm_k, full_bar(st), 64, ug, 0, blk);
-        tma_load_4d(sa + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk);
-        tma_load_4d(sa + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk);
+        tma_load_4d_hint(sa, &tm_k, full_bar(st), 0, ug, 0, blk, pol);
+        tma_load_4d_hint(sa + kBox, &tm_k, full_bar(st), 64, ug, 0, blk, pol);
+        tma_load_4d_hint(sa + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk, pol);
+        tma_load_4d_hint(sa + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk, pol);
       }
     };
     if (tile == 0) {

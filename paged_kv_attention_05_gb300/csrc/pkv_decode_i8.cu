@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
+  const uint64_t pol = l2_evict_first();  // K/V pages are read once
   const float sl2 = a.scale * kLog2e * a.k_scale;  // folded into the fp16 query
   const float o_scale = a.v_scale;
   const int gid = lane >> 2, tig = lane & 3;
@@ -212,8 +213,8 @@ __global__ void __launch_bounds__(Cfg8<MT>::kThreads, 1)
         fence_async_smem();
         const uint32_t st = wbase + s * kStage8;
         mbar_expect_tx(full_bar(s), kStage8);
-        tma_load_4d(st, &tm_k, full_bar(s), 0, ug, 0, blk);
-        tma_load_4d(st + kBox8, &tm_v, full_bar(s), 0, ug, 0, blk);
+        tma_load_4d_hint(st, &tm_k, full_bar(s), 0, ug, 0, blk, pol);
+        tma_load_4d_hint(st + kBox8, &tm_v, full_bar(s), 0, ug, 0, blk, pol);
       }
     };
     for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
