@@ -189,7 +189,7 @@ int decode_workers(int group, int kv_int8, int sms);
 int decode_i8_warps(int group);
 cudaError_t launch_prefill(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st);
 
-// Programmatic dependent launch.  The attention kernels after the cache write
+// Programmatic dependent launch.  The cache write and the attention kernels
 // (plan, decode, prefill; the merge for int8 calls) are launched with programmatic stream
 // serialisation: a kernel's CTAs may start while the kernel before it in the
 // stream is still running, do their set-up (barriers, shared-memory

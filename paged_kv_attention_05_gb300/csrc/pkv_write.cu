@@ -13,6 +13,12 @@
 // lane, all loads issued before the stores (fully coalesced 512-byte
 // transactions, and enough bytes in flight per SM to cover HBM latency).  The
 // grid is a multiple of the SM count and strides over (token, piece).
+//
+// Both write kernels are launched with programmatic stream serialisation:
+// their CTAs may be scheduled while the kernel before them (typically the
+// previous step's attention, which reads the cache) finishes, and wait for
+// it in grid_dep_wait() before touching any memory; then they let the next
+// kernel (the step plan, which waits for this one in turn) start its set-up.
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -25,6 +31,8 @@ __global__ void __launch_bounds__(256) write_kernel(const uint16_t* __restrict__
                                                     uint16_t* __restrict__ vc, int64_t num_slots,
                                                     int row_vecs, const int64_t* __restrict__ slots,
                                                     int64_t n_tokens, int* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   // row_vecs = 16-byte vectors per token row = num_kv_heads * 128 * 2 / 16
   constexpr int kUnroll = 4;
   constexpr int kPiece = 32 * kUnroll;  // vectors of a row one warp moves
@@ -90,6 +98,8 @@ __global__ void __launch_bounds__(256) write_int8_kernel(
     int64_t v_stride, int8_t* __restrict__ kc, int8_t* __restrict__ vc, int64_t num_slots,
     int row_vecs, const int64_t* __restrict__ slots, int64_t n_tokens, float k_scale,
     float v_scale, int* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   // row_vecs = 16-code vectors per token row = num_kv_heads * 128 / 16
   const int64_t per_token = 2 * (int64_t)row_vecs;
   const int64_t total = n_tokens * per_token;
@@ -129,10 +139,9 @@ cudaError_t launch_write_int8(const uint16_t* k, int64_t k_stride, const uint16_
   const int64_t cap = (int64_t)sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  write_int8_kernel<<<(unsigned)blocks, threads, 0, st>>>(k, k_stride, v, v_stride, kc, vc,
-                                                          num_blocks * kBlockSize, row_vecs,
-                                                          slots, n_tokens, k_scale, v_scale, err);
-  return cudaGetLastError();
+  return launch_dependent(write_int8_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, k,
+                          k_stride, v, v_stride, kc, vc, num_blocks * kBlockSize, row_vecs, slots,
+                          n_tokens, k_scale, v_scale, err);
 }
 
 cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v, int64_t v_stride,
@@ -146,10 +155,9 @@ cudaError_t launch_write(const uint16_t* k, int64_t k_stride, const uint16_t* v,
   const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread CTAs per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  write_kernel<<<(unsigned)blocks, threads, 0, st>>>(k, k_stride, v, v_stride, kc, vc,
-                                                     num_blocks * kBlockSize, row_vecs, slots,
-                                                     n_tokens, err);
-  return cudaGetLastError();
+  return launch_dependent(write_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, k, k_stride,
+                          v, v_stride, kc, vc, num_blocks * kBlockSize, row_vecs, slots, n_tokens,
+                          err);
 }
 
 }  // namespace pkv
