@@ -101,16 +101,24 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 // does not wait for this grid before its items).  P is the number of SMs on
 // which the prefill's key-tile steps (items x tiles) fit into the longest
 // item's chain, at most one per item and half of the SMs: fewer would
-// lengthen the prefill, more would sit idle once the items are done.  Every
-// CTA computes the same from the plan header (read after the plan wait).
-__device__ __forceinline__ bool leaves_sm_to_prefill(const AttnArgs& a, const Workspace& ws) {
+// lengthen the prefill, more would take SMs the decode units need and sit
+// idle once the items are done.  When the decode units fill fewer CTAs than
+// the grid has (units_per_cta at a time each), the spare SMs would idle
+// anyway: P then grows up to one per item (still at most half of the SMs).
+// Every CTA computes the same from the plan header (read after the plan
+// wait).
+__device__ __forceinline__ bool leaves_sm_to_prefill(const AttnArgs& a, const Workspace& ws,
+                                                     int units_per_cta) {
   const int G = a.hq / a.hkv;
   const int per_entry = G % 2 == 0 ? a.hq / 2 : a.hq;  // items (query head pairs) per entry
   const int items = ws.hdr->n_pre_entries * per_entry;
   if (items == 0) return false;
   const long long steps = (long long)ws.hdr->pre_tiles * per_entry;
   const int longest = max(ws.hdr->pre_max_tiles, 1);
-  const int p = (int)min((long long)min(items, (int)gridDim.x / 2), (steps + longest - 1) / longest);
+  const int cap = min(items, (int)gridDim.x / 2);
+  int p = (int)min((long long)cap, (steps + longest - 1) / longest);
+  const int spare = (int)gridDim.x - (ws.hdr->n_dec_units + units_per_cta - 1) / units_per_cta;
+  if (spare > p) p = min(cap, spare);
   return (int)blockIdx.x < max(p, 1);
 }
 
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   // the set-up above overlaps the plan kernel; the work list is read after it
   grid_dep_wait();
   grid_dep_launch();
-  if (leaves_sm_to_prefill(a, ws) || ws.hdr->n_dec_units == 0) return;
+  if (leaves_sm_to_prefill(a, ws, C::kWarps) || ws.hdr->n_dec_units == 0) return;
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
   // the set-up above overlaps the plan kernel; the work list is read after it
   grid_dep_wait();
   grid_dep_launch();
-  if (leaves_sm_to_prefill(a, ws) || ws.hdr->n_dec_units == 0) return;
+  if (leaves_sm_to_prefill(a, ws, C::kPairs) || ws.hdr->n_dec_units == 0) return;
   __syncthreads();
 
   const int n_units = ws.hdr->n_dec_units;

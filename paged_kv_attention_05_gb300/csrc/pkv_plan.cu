@@ -101,7 +101,7 @@ struct ReqInfo {
 
 __device__ ReqInfo classify(const AttnArgs& a, int r) {
   ReqInfo ri{0, 0, 0, 0, 0};
-  const int q0 = a.qsl[r], q1 = a.qsl[r + 1], L = a.seq_lens[r];
+  const int q0 = __ldcg(a.qsl + r), q1 = __ldcg(a.qsl + r + 1), L = __ldcg(a.seq_lens + r);
   int bad = 0;
   if (q0 < 0 || q1 < q0 || (int64_t)q1 > a.q_rows)
     bad = PKV_DEV_ERR_QSL;
@@ -132,10 +132,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   __shared__ int4 smem33[33];
   __shared__ long long red[32];
   const int tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
-  // the metadata may come from the kernel before this one (a device-side
-  // step preparation), and the work lists it overwrites were read by the
-  // previous step's kernels: wait for it, then let the decode grid set up
-  grid_dep_wait();
+  // Let the decode grid set up at once.  The metadata is read before the
+  // wait for the kernel before this one: that kernel let this grid start
+  // either by finishing, or, as this library's cache write, after its own
+  // wait for everything before it (it does not touch the metadata), or, as
+  // another plan kernel (pkv_plan), without writing the metadata.  The wait
+  // comes before the first write to the workspace (which that plan kernel
+  // may still be writing, or the previous step's kernels still reading), and
+  // this grid does not finish before it: a kernel that waits for this one
+  // also finds the cache write done.
   grid_dep_launch();
 
   // pass 1: total decode keys, decode requests and their longest length, to
@@ -348,6 +353,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
       s_off_t[nt] = tot_t;
       s_off_q[nt] = tot_q;
     }
+    if (base == 0) grid_dep_wait();  // the first write to the workspace follows
     __syncthreads();
     // decode units and split pairs: one warp of the grid per request (a
     // request's entries are contiguous), lanes over its entries, so that
@@ -402,6 +408,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     pair_carry += tot_q;
     __syncthreads();  // the chunk's offsets are reused by the next chunk
   }
+  grid_dep_wait();  // (already returned unless the loop above ran no chunk)
   if (blockIdx.x == 0 && tid == 0) {
     // A plan that does not fit the workspace runs nothing: entries past a
     // capacity were not written and partial rows past it have no room, so
