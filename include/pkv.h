@@ -15,13 +15,20 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on `stream` and returns; none
  *     synchronises except pkv_get_error.  Work is stream ordered as usual:
- *     the attention calls launch their kernels with programmatic dependent
- *     launch, so a kernel may begin its set-up while the work before it on
- *     the stream is finishing, but it reads and writes no global memory
- *     until that work has finished.  Within a bf16
- *     attention call that has prefill work, the decode kernel leaves some
- *     SMs to the prefill kernel, whose items run there beside the decode
- *     units.
+ *     every call launches its kernels with programmatic dependent launch,
+ *     so a kernel may begin its set-up while the work before it on the
+ *     stream is finishing, but it writes no global memory, and reads none
+ *     that that work produces, until that work has finished.  One
+ *     refinement: the step plan of pkv_attention, pkv_attention_int8,
+ *     pkv_attention_noalloc and pkv_plan reads query_start_loc and seq_lens
+ *     as soon as its kernel starts, which is after the kernel before it on
+ *     the stream has finished, or, when that kernel is pkv_write's (or
+ *     pkv_write_int8's) or another plan's, after everything before that
+ *     kernel has finished: so enqueue the metadata before the write (as a
+ *     step does), or from a kernel launched without programmatic
+ *     serialisation.  Within a bf16 attention call that has prefill work,
+ *     the decode kernel leaves some SMs to the prefill kernel, whose items
+ *     run there beside the decode units.
  *   - The caller owns every buffer it passes; the library keeps no pointer to
  *     any of them after the call returns.  The library owns one grow-only
  *     device workspace per device (step plan, split-KV partial results and
