@@ -15,7 +15,8 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on `stream` and returns; none
  *     synchronises except pkv_get_error.  Work is stream ordered as usual:
- *     every call launches its kernels with programmatic dependent launch,
+ *     the write and attention calls (not pkv_prepare_step) launch their
+ *     kernels with programmatic dependent launch,
  *     so a kernel may begin its set-up while the work before it on the
  *     stream is finishing, but it writes no global memory, and reads none
  *     that that work produces, until that work has finished.  One
