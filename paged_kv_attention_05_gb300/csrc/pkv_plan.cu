@@ -26,6 +26,7 @@
 // decode share an interface": the phase of a request is told apart only by
 // its query and sequence lengths, which is what this kernel does.
 #include <algorithm>
+#include <climits>
 
 #include "pkv_internal.cuh"
 
@@ -218,11 +219,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // whole 64-key tiles, at most kMaxChunk keys; at least kMinChunk keys, and
   // at least 32 keys per query head of the group, so that a split's partial
   // result (G rows of 130 fp32) stays small next to the K/V bytes it read
-  long long want = (total_keys * a.hkv + (long long)dec_grid * 4 - 1) / ((long long)dec_grid * 4);
+  // (32-bit divisions below: a 64-bit one is a long software sequence, on
+  // this kernel's critical path.  The key total is saturated just past the
+  // largest chunk times the divisor and the capacities at INT_MAX, which
+  // changes no result: past those bounds the clamp to kMaxChunk, or the
+  // smaller per-pair count, decides.)
+  const unsigned den = 4u * (unsigned)dec_grid;  // dec_grid: a few thousand workers at most
+  const long long tk = total_keys * a.hkv;
+  unsigned want = tk > (long long)kMaxChunk * den ? (unsigned)kMaxChunk + 1u
+                                                  : ((unsigned)tk + den - 1u) / den;
   want = (want + kDecTile - 1) / kDecTile * kDecTile;
   const int G = a.hq / a.hkv;
   const int lo_chunk = max(kMinChunk, 32 * G);
-  int chunk = (int)(want < lo_chunk ? lo_chunk : (want > kMaxChunk ? kMaxChunk : want));
+  int chunk = want < (unsigned)lo_chunk ? lo_chunk : (want > (unsigned)kMaxChunk ? kMaxChunk : (int)want);
   // When even the longest request's splits, times the pairs, fit one wave of
   // workers, the step takes one unit's time: give every pair as many splits
   // as the wave has room for (units of at most that many keys), so that the
@@ -231,29 +240,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
   // the workspace also holds the units and partial rows it makes: at most
   // `per` splits a pair, pairs x per units and pairs x per x rmax rows.  (The
   // batch is small then: the extra partial results are small next to the
-  // latency a long unit's chain of pages costs.)
+  // latency a long unit's chain of pages costs.)  In both branches the pairs
+  // are at most the workers.
   if (dec_pairs > 0 && dec_pairs * ((lmax + chunk - 1) / chunk) <= dec_grid) {
-    const long long per_pair = dec_grid / dec_pairs;
-    long long c = (lmax + per_pair - 1) / per_pair;
+    const unsigned pairs = (unsigned)dec_pairs;
+    const unsigned per_pair = (unsigned)dec_grid / pairs;
+    unsigned c = ((unsigned)lmax + per_pair - 1u) / per_pair;
     c = (c + kDecTile - 1) / kDecTile * kDecTile;
-    if (c < kMinChunk) {
-      long long per = per_pair;
-      per = min(per, ws.max_units / dec_pairs);
-      per = min(per, ws.max_part_rows / (dec_pairs * (long long)max(rmax, 1)));
-      long long c2 = per >= 1 ? (lmax + per - 1) / per : kMinChunk;
+    if (c < (unsigned)kMinChunk) {
+      const unsigned mu = (unsigned)min(ws.max_units, (int64_t)INT_MAX);
+      const unsigned mp = (unsigned)min(ws.max_part_rows, (int64_t)INT_MAX);
+      unsigned per = per_pair;
+      per = min(per, mu / pairs);
+      per = min(per, mp / (pairs * (unsigned)max(rmax, 1)));
+      unsigned c2 = per >= 1u ? ((unsigned)lmax + per - 1u) / per : (unsigned)kMinChunk;
       c2 = (c2 + kDecTile - 1) / kDecTile * kDecTile;
-      c = c2 < kMinChunk ? (c2 > c ? c2 : c) : kMinChunk;
+      c = c2 < (unsigned)kMinChunk ? (c2 > c ? c2 : c) : (unsigned)kMinChunk;
     }
-    if (c < chunk) chunk = (int)c;
+    if ((int)c < chunk) chunk = (int)c;
   } else if (dec_pairs > 0 && dec_pairs <= dec_grid) {
     // More splits than one wave of workers, but every pair fits in it with
     // a somewhat longer chunk: one wave of units under twice as long beats
     // two waves (32 MQA requests of 32,769 keys on 912 workers: 1216-key
     // units, 864 of them, instead of 1056 units of 1024 keys)
-    const long long per_pair = dec_grid / dec_pairs;
-    long long c = (lmax + per_pair - 1) / per_pair;
+    const unsigned per_pair = (unsigned)dec_grid / (unsigned)dec_pairs;
+    unsigned c = ((unsigned)lmax + per_pair - 1u) / per_pair;
     c = (c + kDecTile - 1) / kDecTile * kDecTile;
-    if (c <= kMaxChunk && c < 2LL * chunk) chunk = (int)c;
+    if (c <= (unsigned)kMaxChunk && (int)c < 2 * chunk) chunk = (int)c;
   }
 
   // Units are listed roughly longest first, in five classes: every request's
