@@ -24,7 +24,8 @@
 //     token * G + head in group, for the request's qn tokens (qn * G at most
 //     16; longer requests go to prefill).  Groups above 16 heads (up to 32
 //     rows, a single token) run decode_pair_kernel below: a warp pair per
-//     unit, one tile per warp, one page ring per pair.
+//     unit, one tile per warp, one ring of two-page stages per pair, two
+//     pages (32 keys) a step.
 //     Row (token i) sees the keys before position ctx + i + 1, ctx = keys
 //     before the request's first query token (causal mask inside the
 //     request's own tokens).  S = Q.K^T and O += P.V run
@@ -452,20 +453,23 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 // Groups above 16 heads: a unit's rows are the G heads of its one query token
 // (qn * G <= 32 leaves a single token), two 16-row tiles.  A warp pair takes
 // the unit: each warp runs one tile's MMA chain, and the two share the unit's
-// page ring and query rows, so a page is loaded once for both tiles and each
-// warp's chain per page is that of a one-tile unit.  The first warp of the
-// pair takes the unit from the cursor (and hands it over through shared
-// memory), loads the query rows and the pages, and refills a stage only once
-// both warps have released it.
+// page ring, so a page is loaded once for both tiles and each warp's chain
+// per page is that of a one-tile unit.  The first warp of the pair takes the
+// unit from the cursor (and hands it over through shared memory), loads the
+// pages, and refills a stage only once both warps have released it.  A step
+// takes two pages (32 keys): one online-softmax update and one stage
+// hand-over per 32 keys, on a ring of two-page stages.  Each warp reads its
+// query fragments from global memory (L2) once per unit, so that shared
+// memory holds six pairs' rings.
 struct CfgP {
   static constexpr int kPairs = 6;
   static constexpr int kWarps = 2 * kPairs;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kStages = 3;
-  static constexpr int kQHalf = 32 * 128;  // 32 query rows x one 64-dim half
-  static constexpr int kPairBytes = kStages * kPage + 2 * kQHalf;
-  // per pair: full[kStages], empty[kStages], query full, query read, unit[2]
-  static constexpr int kBarsPerPair = 2 * kStages + 4;
+  static constexpr int kStages = 2;        // two-page stages
+  static constexpr int kStage = 2 * kPage;
+  static constexpr int kPairBytes = kStages * kStage;
+  // per pair: full[kStages], empty[kStages], unit[2]
+  static constexpr int kBarsPerPair = 2 * kStages + 2;
   static constexpr int kOffUnit = kPairs * kPairBytes;  // int[kPairs][2]: unit handed over
   static constexpr int kOffBar = kOffUnit + kPairs * 2 * 4;
   static constexpr int kOffCtl = kOffBar + kPairs * kBarsPerPair * 8;
@@ -474,8 +478,7 @@ struct CfgP {
 static_assert(CfgP::kSmem <= 232448, "shared memory per CTA");
 
 __global__ void __launch_bounds__(CfgP::kThreads, 1)
-    decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k,
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
   using C = CfgP;
   extern __shared__ uint8_t smem_raw[];
@@ -486,12 +489,10 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
   const int G = a.hq / a.hkv;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t pbase = sbase + pair * C::kPairBytes;  // the pair's page stages
-  const uint32_t qbuf = pbase + C::kStages * kPage;     // and query rows
   const uint32_t bars = sbase + C::kOffBar + pair * C::kBarsPerPair * 8;
   auto full_bar = [&](int st) { return bars + 8u * st; };
   auto empty_bar = [&](int st) { return bars + 8u * (C::kStages + st); };
-  const uint32_t q_full = bars + 8u * (2 * C::kStages), q_read = q_full + 8u;
-  auto unit_bar = [&](int k) { return bars + 8u * (2 * C::kStages + 2 + k); };
+  auto unit_bar = [&](int k) { return bars + 8u * (2 * C::kStages + k); };
   volatile int* uslot = reinterpret_cast<volatile int*>(smem + C::kOffUnit) + 2 * pair;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::kOffCtl);
 
@@ -501,19 +502,10 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
         mbar_init(full_bar(st), 1);
         mbar_init(empty_bar(st), 2);  // both warps release a stage
       }
-      mbar_init(q_full, 1);
-      mbar_init(q_read, 2);  // both warps hold their query fragments
       mbar_init(unit_bar(0), 1);
       mbar_init(unit_bar(1), 1);
       if (warp == 0) *abort = 0;
       fence_barrier_init();
-    }
-    // query rows past the group's G heads stay zero; their results are dropped
-    for (int i = lane; i < 2 * 32 * 8; i += 32) {
-      const int row = (i >> 3) % 32, half = (i >> 3) / 32, c = i & 7;
-      if (row >= G)
-        *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
-            make_uint4(0, 0, 0, 0);
     }
   }
   // the set-up above overlaps the plan kernel; the work list is read after it
@@ -528,7 +520,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
   const int gid = lane >> 2, tig = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
   const int roff = 16 * tile;  // this warp's rows (heads of the group)
-  uint32_t page_cnt = 0;
+  uint32_t step_cnt = 0;
 
   for (uint32_t unit_cnt = 0;; ++unit_cnt) {
     const int slot = unit_cnt & 1;
@@ -572,53 +564,67 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
         ids[j] = blk;
       }
     }
-    // page p of the unit into stage (page_cnt + p) % kStages, once both warps
-    // have released the stage's previous page
+    // pages 2 * j and 2 * j + 1 (if any) of the unit into stage
+    // (step_cnt + j) % kStages, once both warps have released the stage's
+    // previous pages
+    const int nsteps = (npages + 1) / 2;
     bool ok = true;
-    auto issue_page = [&](int p) {
-      const uint32_t x = page_cnt + p;
+    auto issue_step = [&](int j) {
+      const uint32_t x = step_cnt + j;
       const int st = x % C::kStages;
       if (x >= (uint32_t)C::kStages &&
           !mbar_wait_warp(empty_bar(st), ((x / C::kStages) - 1) & 1, abort, ws.err)) {
         ok = false;
         return;
       }
+      const int p = 2 * j;  // both pages' ids sit in the same register
       int idv = ids[0];
 #pragma unroll
-      for (int j = 1; j < kIdRegs; ++j)
-        if ((p >> 5) == j) idv = ids[j];
-      const int blk = __shfl_sync(0xffffffffu, idv, p & 31);
+      for (int r = 1; r < kIdRegs; ++r)
+        if ((p >> 5) == r) idv = ids[r];
+      const int blk0 = __shfl_sync(0xffffffffu, idv, p & 31);
+      const int blk1 = __shfl_sync(0xffffffffu, idv, (p + 1) & 31);
       if (lane == 0) {
-        const uint32_t sa = pbase + st * kPage;
-        mbar_expect_tx(full_bar(st), kPage);
-        tma_load_4d_hint(sa, &tm_k, full_bar(st), 0, ug, 0, blk, pol);
-        tma_load_4d_hint(sa + kBox, &tm_k, full_bar(st), 64, ug, 0, blk, pol);
-        tma_load_4d_hint(sa + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk, pol);
-        tma_load_4d_hint(sa + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk, pol);
+        const bool two = p + 1 < npages;
+        const uint32_t sa = pbase + st * C::kStage;
+        mbar_expect_tx(full_bar(st), two ? 2 * kPage : kPage);
+        tma_load_4d_hint(sa, &tm_k, full_bar(st), 0, ug, 0, blk0, pol);
+        tma_load_4d_hint(sa + kBox, &tm_k, full_bar(st), 64, ug, 0, blk0, pol);
+        tma_load_4d_hint(sa + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk0, pol);
+        tma_load_4d_hint(sa + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk0, pol);
+        if (two) {
+          const uint32_t sb = sa + kPage;
+          tma_load_4d_hint(sb, &tm_k, full_bar(st), 0, ug, 0, blk1, pol);
+          tma_load_4d_hint(sb + kBox, &tm_k, full_bar(st), 64, ug, 0, blk1, pol);
+          tma_load_4d_hint(sb + 2 * kBox, &tm_v, full_bar(st), 0, ug, 0, blk1, pol);
+          tma_load_4d_hint(sb + 3 * kBox, &tm_v, full_bar(st), 64, ug, 0, blk1, pol);
+        }
       }
     };
     if (tile == 0) {
-      // the query rows, once both warps hold the previous unit's fragments
-      if (unit_cnt > 0 && !mbar_wait_warp(q_read, (unit_cnt - 1) & 1, abort, ws.err)) break;
-      if (lane == 0) {
-        mbar_expect_tx(q_full, 2 * G * 128);
-        tma_load_3d(qbuf, &tm_q, q_full, 0, ug * G, un.q0);
-        tma_load_3d(qbuf + C::kQHalf, &tm_q, q_full, 64, ug * G, un.q0);
-      }
-      for (int p = 0; p < C::kStages && p < npages && ok; ++p) issue_page(p);
+      for (int j = 0; j < C::kStages && j < nsteps && ok; ++j) issue_step(j);
       if (!ok) break;
     }
     // every row sees keys < ctx + 1, clipped to the unit
     const int vis = min(k1, un.ctx + 1);
-    if (!mbar_wait_warp(q_full, unit_cnt & 1, abort, ws.err)) break;
+    // the A fragments of the warp's 16 query rows (heads roff + gid and
+    // roff + gid + 8 of the group; k-step k: dimensions 16k + 2tig, + 1 in
+    // registers 0 / 1 and 16k + 8 + 2tig, + 1 in 2 / 3); rows past the
+    // group's G heads are zero and their results dropped
     uint32_t qa[8][4];
+    {
+      const int ha = roff + gid, hb = ha + 8;
+      const uint16_t* qrow = a.q + (int64_t)un.q0 * a.q_stride + (int64_t)ug * G * kHeadSize;
+      const uint32_t* qra = reinterpret_cast<const uint32_t*>(qrow + (int64_t)ha * kHeadSize);
+      const uint32_t* qrb = reinterpret_cast<const uint32_t*>(qrow + (int64_t)hb * kHeadSize);
 #pragma unroll
-    for (int kstep = 0; kstep < 8; ++kstep)
-      ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf +
-                  sw128(roff + rr + ((mi & 1) << 3), (kstep & 3) * 2 + (mi >> 1)),
-              qa[kstep][0], qa[kstep][1], qa[kstep][2], qa[kstep][3]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_read);
+      for (int kstep = 0; kstep < 8; ++kstep) {
+        qa[kstep][0] = ha < G ? __ldg(qra + 8 * kstep + tig) : 0u;
+        qa[kstep][1] = hb < G ? __ldg(qrb + 8 * kstep + tig) : 0u;
+        qa[kstep][2] = ha < G ? __ldg(qra + 8 * kstep + 4 + tig) : 0u;
+        qa[kstep][3] = hb < G ? __ldg(qrb + 8 * kstep + 4 + tig) : 0u;
+      }
+    }
 
     float o[16][4];
 #pragma unroll
@@ -627,39 +633,47 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
       for (int e = 0; e < 4; ++e) o[dn][e] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-    for (int p = 0; p < npages; ++p) {
-      const uint32_t x = page_cnt + p;
+    for (int j = 0; j < nsteps; ++j) {
+      const uint32_t x = step_cnt + j;
       const int st = x % C::kStages;
       if (!mbar_wait_warp(full_bar(st), (x / C::kStages) & 1, abort, ws.err)) {
         ok = false;
         break;
       }
+      const int p = 2 * j;
+      const bool two = p + 1 < npages;
       const int pos0 = k0 + p * kBlockSize;
-      const int valid = k1 - pos0;  // keys of this page inside the unit
-      const uint32_t sa = pbase + st * kPage;
+      // keys of each page inside the unit (a missing second page: none, its
+      // keys masked and its V zeroed; the first page's data stands in)
+      const int valid[2] = {k1 - pos0, k1 - pos0 - kBlockSize};
+      const uint32_t sa[2] = {pbase + st * C::kStage, pbase + st * C::kStage + (two ? kPage : 0)};
 
-      // S = Q K^T for the page's 16 keys (two n-tiles of 8)
-      float sacc[2][4];
+      // S = Q K^T for the step's 32 keys (n-tiles 2 * page + 0, 1 of 8 keys)
+      float sacc[4][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
 #pragma unroll
       for (int kstep = 0; kstep < 8; ++kstep) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sa + (kstep >> 2) * kBox + sw128(rr + ((mi >> 1) << 3), (kstep & 3) * 2 + (mi & 1)),
-                b0, b1, b2, b3);
-        mma_bf16(sacc[0], qa[kstep], b0, b1);
-        mma_bf16(sacc[1], qa[kstep], b2, b3);
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sa[pg] + (kstep >> 2) * kBox +
+                      sw128(rr + ((mi >> 1) << 3), (kstep & 3) * 2 + (mi & 1)),
+                  b0, b1, b2, b3);
+          mma_bf16(sacc[2 * pg], qa[kstep], b0, b1);
+          mma_bf16(sacc[2 * pg + 1], qa[kstep], b2, b3);
+        }
       }
 
       // online softmax in the log2 domain (as in decode_kernel)
-      uint32_t pa[4];
+      uint32_t pa[2][4];
       {
-        float xs[2][4];
+        float xs[4][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = nt * 8 + tig * 2 + (e & 1);
@@ -692,7 +706,7 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
         const float c0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
         const float c1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
           xs[nt][0] = fast_exp2(xs[nt][0] - c0);
           xs[nt][1] = fast_exp2(xs[nt][1] - c0);
           xs[nt][2] = fast_exp2(xs[nt][2] - c1);
@@ -700,37 +714,44 @@ __global__ void __launch_bounds__(CfgP::kThreads, 1)
           l_run[0] += xs[nt][0] + xs[nt][1];
           l_run[1] += xs[nt][2] + xs[nt][3];
         }
-        pa[0] = pack_bf16(xs[0][0], xs[0][1]);
-        pa[1] = pack_bf16(xs[0][2], xs[0][3]);
-        pa[2] = pack_bf16(xs[1][0], xs[1][1]);
-        pa[3] = pack_bf16(xs[1][2], xs[1][3]);
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+          pa[pg][0] = pack_bf16(xs[2 * pg][0], xs[2 * pg][1]);
+          pa[pg][1] = pack_bf16(xs[2 * pg][2], xs[2 * pg][3]);
+          pa[pg][2] = pack_bf16(xs[2 * pg + 1][0], xs[2 * pg + 1][1]);
+          pa[pg][3] = pack_bf16(xs[2 * pg + 1][2], xs[2 * pg + 1][3]);
+        }
       }
 
-      // O += P V (V rows read transposed); V of keys past the unit zeroed
+      // O += P V (V rows read transposed), one k-step of 16 keys per page;
+      // V of keys past the unit zeroed
 #pragma unroll
-      for (int dn = 0; dn < 16; dn += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sa + (2 + (dn >> 3)) * kBox + sw128(rr + ((mi & 1) << 3), (dn & 7) + (mi >> 1)),
-                  b0, b1, b2, b3);
-        if (valid < 16) {
-          b0 = mask_pair(b0, 2 * tig, valid);
-          b2 = mask_pair(b2, 2 * tig, valid);
-          b1 = mask_pair(b1, 8 + 2 * tig, valid);
-          b3 = mask_pair(b3, 8 + 2 * tig, valid);
+      for (int pg = 0; pg < 2; ++pg)
+#pragma unroll
+        for (int dn = 0; dn < 16; dn += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sa[pg] + (2 + (dn >> 3)) * kBox +
+                        sw128(rr + ((mi & 1) << 3), (dn & 7) + (mi >> 1)),
+                    b0, b1, b2, b3);
+          if (valid[pg] < 16) {
+            b0 = mask_pair(b0, 2 * tig, valid[pg]);
+            b2 = mask_pair(b2, 2 * tig, valid[pg]);
+            b1 = mask_pair(b1, 8 + 2 * tig, valid[pg]);
+            b3 = mask_pair(b3, 8 + 2 * tig, valid[pg]);
+          }
+          mma_bf16(o[dn], pa[pg], b0, b1);
+          mma_bf16(o[dn + 1], pa[pg], b2, b3);
         }
-        mma_bf16(o[dn], pa, b0, b1);
-        mma_bf16(o[dn + 1], pa, b2, b3);
-      }
       // this warp is done with the stage; the loading warp refills it
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(st));
-      if (tile == 0 && p + C::kStages < npages) {
-        issue_page(p + C::kStages);
+      if (tile == 0 && j + C::kStages < nsteps) {
+        issue_step(j + C::kStages);
         if (!ok) break;
       }
     }
     if (!ok) break;
-    page_cnt += npages;
+    step_cnt += nsteps;
 
     // finish: row sums across the quad, then output or split partials
     float l0 = l_run[0], l1 = l_run[1];
@@ -797,14 +818,12 @@ cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStrea
 cudaError_t launch_pair(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   static std::atomic<bool> attr[kMaxAttrDevices];
   if (cudaError_t e = smem_attr_once(decode_pair_kernel, CfgP::kSmem, attr)) return e;
-  const int G = a.hq / a.hkv;
-  CUtensorMap tq, tk, tv;
-  if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) ||
-      !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
+  CUtensorMap tk, tv;  // (query rows: plain loads, 16-byte aligned by the API's checks)
+  if (!make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
   return launch_dependent(decode_pair_kernel, dim3(sms), dim3(CfgP::kThreads), CfgP::kSmem, st,
-                          tq, tk, tv, a, ws);
+                          tk, tv, a, ws);
 }
 
 }  // namespace

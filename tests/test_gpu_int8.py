@@ -74,7 +74,7 @@ def test_int8_write_codes_clamp_and_nan():
 
 @pytest.mark.parametrize("hq,hkv,qn", [(8, 8, 1), (32, 8, 1), (32, 1, 1), (64, 2, 1),
                                        (48, 2, 1), (20, 1, 1), (8, 8, 4), (16, 4, 2),
-                                       (12, 4, 5), (8, 1, 2)])
+                                       (12, 4, 5), (8, 1, 2), (17, 1, 1), (56, 2, 1)])
 def test_int8_decode(hq, hkv, qn):
     ctx = [0, 1, 15, 16, 63, 200, 1023, 2100, 5000]
     step = W.build(W.custom(ctx, [qn] * len(ctx), hq, hkv, seed=hq * 7 + hkv + qn))
