@@ -263,7 +263,10 @@ int pkv_write_int8(const void* k, int64_t k_row_stride, const void* v, int64_t v
  * fp16 integers, the query is multiplied by scale * log2(e) * k_scale and
  * rounded to fp16 (so |q| * scale * k_scale * 1.4427 must stay below 65504,
  * the fp16 range; a larger product gives inf), the probabilities are fp16,
- * accumulation is fp32, and v_scale is applied to the output.
+ * accumulation is fp32, and v_scale is applied to the output.  The codes
+ * enter the products as code + 1152 (exact in fp16): the constant this adds
+ * to a row's scores leaves its softmax unchanged, and the one it adds to the
+ * output sums is subtracted at the end, both in fp32.
  *
  * Requests on the decode path only: a request whose query_len * (num_heads /
  * num_kv_heads) is at most 16 (32 when the group is larger than 16) —

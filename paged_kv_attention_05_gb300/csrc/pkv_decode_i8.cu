@@ -17,8 +17,17 @@
 // the operand registers of fp16 mma.sync m16n8k16 — no widened copy of the
 // page is written back — because every code -127..127 is an fp16 integer:
 // the byte, offset by 128, becomes the low mantissa byte of the fp16 number
-// 1024 + byte (one byte permute for two codes), and one packed fp16 subtract
-// of 1152 leaves the code exactly.  Two reorderings make each thread's codes
+// 1024 + byte (one byte permute for two codes), so the MMAs see code + 1152.
+// The offset leaves the sums exactly:
+//   * a score becomes s + 1152 * sum_d q_d, the same constant for every key
+//     of a row, which neither the online softmax (differences of scores and
+//     maxima) nor the merge of the splits (differences of the maxima of one
+//     row) sees — the maximum a split writes carries the constant;
+//   * the output sum becomes O + 1152 * L with L = sum_k p_k over the same
+//     fp16 probabilities, which one more MMA per page and tile gives (P times
+//     a column of ones, fp32 accumulation) and which is also the row sum the
+//     output is divided by.
+// Two reorderings make each thread's codes
 // contiguous in shared memory, so that a page takes eight 16-byte loads per
 // thread and no ldmatrix:
 //   * S = Q.K^T sums over the 128 dimensions in any order: k-step ks of the
@@ -47,7 +56,7 @@ constexpr int kBox8 = kBlockSize * 128;          // 16 slots x 128 codes (2 KB)
 constexpr int kStage8 = 2 * kBox8;               // K box | V box
 constexpr int kIdRegs8 = kMaxChunk / kBlockSize / 32;
 constexpr uint32_t kSignFlip = 0x80808080u;      // int8 -> offset binary (code + 128)
-constexpr uint32_t kFp16Bias = 0x64806480u;      // fp16 pair (1152, 1152) = 1024 + 128
+constexpr uint32_t kOnesF16x2 = 0x3C003C00u;     // fp16 pair (1, 1)
 
 // groups of up to 16 heads: one 16-row query tile per warp, 12 warps of 3
 // page stages (160 registers)
@@ -82,14 +91,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two codes as an fp16 pair: u holds offset-binary bytes (code + 128); sel
-// picks two of them (0x4140: bytes 0, 1; 0x4342: bytes 2, 3) into the low
-// mantissa bytes of 0x6400 (fp16 1024), and 1152 is subtracted (exact).
-__device__ __forceinline__ uint32_t codes_f16x2(uint32_t u, uint32_t sel) {
-  const uint32_t h = __byte_perm(u, 0x64646464u, sel);
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(h), "r"(kFp16Bias));
-  return r;
+// Two codes plus 1152 as an fp16 pair: u holds offset-binary bytes (code +
+// 128); sel picks two of them (0x4140: bytes 0, 1; 0x4342: bytes 2, 3) into
+// the low mantissa bytes of 0x6400 (fp16 1024), which gives 1024 + 128 +
+// code (1025..1279, exact).  The kernels take the offset out of their sums.
+__device__ __forceinline__ uint32_t codes_plus_bias_f16x2(uint32_t u, uint32_t sel) {
+  return __byte_perm(u, 0x64646464u, sel);
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -234,12 +241,14 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
       }
     }
 
-    float o[16][4];
+    // o: the output sums (+ 1152 * L); lsum: L of rows gid (elements 0, 1)
+    // and gid + 8 (2, 3)
+    float o[16][4], lsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[dn][e] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float m_run[2] = {-INFINITY, -INFINITY};
 
     bool ok = true;
     for (int p = 0; p < npages; ++p) {
@@ -272,8 +281,10 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t u0 = (ks < 4 ? word_of(ka0, ks) : word_of(kb0, ks - 4)) ^ kSignFlip;
         const uint32_t u1 = (ks < 4 ? word_of(ka1, ks) : word_of(kb1, ks - 4)) ^ kSignFlip;
-        const uint32_t b00 = codes_f16x2(u0, 0x4140), b01 = codes_f16x2(u0, 0x4342);
-        const uint32_t b10 = codes_f16x2(u1, 0x4140), b11 = codes_f16x2(u1, 0x4342);
+        const uint32_t b00 = codes_plus_bias_f16x2(u0, 0x4140);
+        const uint32_t b01 = codes_plus_bias_f16x2(u0, 0x4342);
+        const uint32_t b10 = codes_plus_bias_f16x2(u1, 0x4140);
+        const uint32_t b11 = codes_plus_bias_f16x2(u1, 0x4342);
         mma_f16(sacc[0], qa[ks], b00, b01);
         mma_f16(sacc[1], qa[ks], b10, b11);
       }
@@ -311,8 +322,10 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
           const float al1 = up1 ? fast_exp2(m_run[1] - n1) : 1.f;
           m_run[0] = n0;
           m_run[1] = n1;
-          l_run[0] *= al0;
-          l_run[1] *= al1;
+          lsum[0] *= al0;
+          lsum[1] *= al0;
+          lsum[2] *= al1;
+          lsum[3] *= al1;
 #pragma unroll
           for (int dn = 0; dn < 16; ++dn) {
             o[dn][0] *= al0;
@@ -330,8 +343,6 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
           xs[nt][1] = fast_exp2(xs[nt][1] - c0);
           xs[nt][2] = fast_exp2(xs[nt][2] - c1);
           xs[nt][3] = fast_exp2(xs[nt][3] - c1);
-          l_run[0] += xs[nt][0] + xs[nt][1];
-          l_run[1] += xs[nt][2] + xs[nt][3];
         }
         pa[0] = pack_f16(xs[0][0], xs[0][1]);
         pa[1] = pack_f16(xs[0][2], xs[0][3]);
@@ -342,7 +353,8 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
       // O += P V: code word i of the four key rows (dimensions 16 * gid +
       // 4 * i .. + 3) gives n-tiles dn = 4 * i .. + 3; the byte pairs (key
       // 2 * tig, key 2 * tig + 1) and (key 2 * tig + 8, + 9) of a dimension
-      // are interleaved first
+      // are interleaved first.  L += P times a column of ones.
+      mma_f16(lsum, pa, kOnesF16x2, kOnesF16x2);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t wa = word_of(vA, i), wb = word_of(vB, i);
@@ -355,7 +367,8 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const uint32_t ab = e < 2 ? ab_lo : ab_hi, cd = e < 2 ? cd_lo : cd_hi;
           const uint32_t sel = (e & 1) ? 0x4342 : 0x4140;
-          const uint32_t b0 = codes_f16x2(ab, sel), b1 = codes_f16x2(cd, sel);
+          const uint32_t b0 = codes_plus_bias_f16x2(ab, sel);
+          const uint32_t b1 = codes_plus_bias_f16x2(cd, sel);
           mma_f16(o[4 * i + e], pa, b0, b1);
         }
       }
@@ -363,21 +376,17 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
     if (!ok) break;
     page_cnt += npages;
 
-    // finish: row sums across the quad; the thread holds output dimensions
-    // 32 * tig .. + 31 of rows gid and gid + 8 (dimension 32 * tig + j in
-    // o[j][0 / 2] for j < 16, o[j - 16][1 / 3] above)
-    float l0 = l_run[0], l1 = l_run[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    // finish: output = (O + 1152 L) / L - 1152; the thread holds output
+    // dimensions 32 * tig .. + 31 of rows gid and gid + 8 (dimension
+    // 32 * tig + j in o[j][0 / 2] for j < 16, o[j - 16][1 / 3] above)
+    const float l0 = lsum[0], l1 = lsum[2];
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
       const int rw = gid + 8 * hrow;  // row: token * G + head in group
       if (rw >= nrows) continue;
       const int e0 = 2 * hrow;  // o[][e0]: first 16 dimensions, o[][e0 + 1]: the rest
       if (un.nsplit == 1) {
-        const float inv = o_scale / (hrow ? l1 : l0);
+        const float inv = 1.f / (hrow ? l1 : l0);
         uint16_t* orow = a.out + (int64_t)(un.q0 + rw / G) * a.out_stride +
                          (int64_t)(ug * G + rw % G) * kHeadSize + 32 * tig;
 #pragma unroll
@@ -388,20 +397,22 @@ __global__ void __launch_bounds__(Cfg8::kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int j = q4 * 8 + 2 * k;
-              w[k] = pack_bf16(o[j][e0 + h2] * inv, o[j + 1][e0 + h2] * inv);
+              w[k] = pack_bf16((o[j][e0 + h2] * inv - 1152.f) * o_scale,
+                               (o[j + 1][e0 + h2] * inv - 1152.f) * o_scale);
             }
             *reinterpret_cast<uint4*>(orow + h2 * 16 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
       } else {
+        const float off = 1152.f * (hrow ? l1 : l0);
         float* prow = ws.part_o + ((int64_t)un.part + rw) * kHeadSize + 32 * tig;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int j = q4 * 4;
-            *reinterpret_cast<float4*>(prow + h2 * 16 + j) =
-                make_float4(o[j][e0 + h2] * o_scale, o[j + 1][e0 + h2] * o_scale,
-                            o[j + 2][e0 + h2] * o_scale, o[j + 3][e0 + h2] * o_scale);
+            *reinterpret_cast<float4*>(prow + h2 * 16 + j) = make_float4(
+                (o[j][e0 + h2] - off) * o_scale, (o[j + 1][e0 + h2] - off) * o_scale,
+                (o[j + 2][e0 + h2] - off) * o_scale, (o[j + 3][e0 + h2] - off) * o_scale);
           }
         if (tig == 0)
           *reinterpret_cast<float2*>(ws.part_ml + ((int64_t)un.part + rw) * 2) =
@@ -600,16 +611,19 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
       __syncwarp();
     }
 
-    float o[2][16][4];
-    float m_run[2][2], l_run[2][2];
+    // o: the output sums (+ 1152 * L); lsum: L of rows gid (elements 0, 1)
+    // and gid + 8 (2, 3)
+    float o[2][16][4], lsum[2][4];
+    float m_run[2][2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
       for (int dn = 0; dn < 16; ++dn)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[mt][dn][e] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lsum[mt][e] = 0.f;
       m_run[mt][0] = m_run[mt][1] = -INFINITY;
-      l_run[mt][0] = l_run[mt][1] = 0.f;
     }
 
     bool ok = true;
@@ -661,8 +675,10 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
           for (int pg = 0; pg < 2; ++pg) {
             const uint32_t u0 = word_of(kc[pg][0], k4) ^ kSignFlip;
             const uint32_t u1 = word_of(kc[pg][1], k4) ^ kSignFlip;
-            const uint32_t b00 = codes_f16x2(u0, 0x4140), b01 = codes_f16x2(u0, 0x4342);
-            const uint32_t b10 = codes_f16x2(u1, 0x4140), b11 = codes_f16x2(u1, 0x4342);
+            const uint32_t b00 = codes_plus_bias_f16x2(u0, 0x4140);
+            const uint32_t b01 = codes_plus_bias_f16x2(u0, 0x4342);
+            const uint32_t b10 = codes_plus_bias_f16x2(u1, 0x4140);
+            const uint32_t b11 = codes_plus_bias_f16x2(u1, 0x4342);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
               mma_f16(sacc[mt][2 * pg], qf[mt], b00, b01);
@@ -714,8 +730,10 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
           const float al1 = up1 ? fast_exp2(m_run[mt][1] - n1) : 1.f;
           m_run[mt][0] = n0;
           m_run[mt][1] = n1;
-          l_run[mt][0] *= al0;
-          l_run[mt][1] *= al1;
+          lsum[mt][0] *= al0;
+          lsum[mt][1] *= al0;
+          lsum[mt][2] *= al1;
+          lsum[mt][3] *= al1;
 #pragma unroll
           for (int dn = 0; dn < 16; ++dn) {
             o[mt][dn][0] *= al0;
@@ -733,8 +751,6 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
           xs[nt][1] = fast_exp2(xs[nt][1] - c0);
           xs[nt][2] = fast_exp2(xs[nt][2] - c1);
           xs[nt][3] = fast_exp2(xs[nt][3] - c1);
-          l_run[mt][0] += xs[nt][0] + xs[nt][1];
-          l_run[mt][1] += xs[nt][2] + xs[nt][3];
         }
 #pragma unroll
         for (int pg = 0; pg < 2; ++pg) {
@@ -748,9 +764,12 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
       // O += P V, one k-step of 16 keys per page: code word i of the four
       // key rows (dimensions 16 * gid + 4 * i .. + 3) gives n-tiles
       // dn = 4 * i .. + 3; the byte pairs (key 2 * tig, key 2 * tig + 1) and
-      // (key 2 * tig + 8, + 9) of a dimension are interleaved first
+      // (key 2 * tig + 8, + 9) of a dimension are interleaved first.  L +=
+      // P times a column of ones.
 #pragma unroll
-      for (int pg = 0; pg < 2; ++pg)
+      for (int pg = 0; pg < 2; ++pg) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) mma_f16(lsum[mt], pa[mt][pg], kOnesF16x2, kOnesF16x2);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t wa = word_of(vc[pg][0], i), wb = word_of(vc[pg][1], i);
@@ -763,33 +782,32 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             const uint32_t ab = e < 2 ? ab_lo : ab_hi, cd = e < 2 ? cd_lo : cd_hi;
             const uint32_t sel = (e & 1) ? 0x4342 : 0x4140;
-            const uint32_t b0 = codes_f16x2(ab, sel), b1 = codes_f16x2(cd, sel);
+            const uint32_t b0 = codes_plus_bias_f16x2(ab, sel);
+            const uint32_t b1 = codes_plus_bias_f16x2(cd, sel);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) mma_f16(o[mt][4 * i + e], pa[mt][pg], b0, b1);
           }
         }
+      }
     }
     if (!ok) break;
     pair_cnt += nsteps;
 
-    // finish: row sums across the quad; the thread holds output dimensions
-    // 32 * tig .. + 31 of rows ra and rb (dimension 32 * tig + j in
-    // o[j][0 / 2] for j < 16, o[j - 16][1 / 3] above)
+    // finish: output = (O + 1152 L) / L - 1152; the thread holds output
+    // dimensions 32 * tig .. + 31 of rows ra and rb (dimension 32 * tig + j
+    // in o[j][0 / 2] for j < 16, o[j - 16][1 / 3] above)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      float l0 = l_run[mt][0], l1 = l_run[mt][1];
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      const float l0 = lsum[mt][0], l1 = lsum[mt][2];
       const int ra = mt * 16 + gid, rb = ra + 8;  // rows: token * G + head in group
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
         const int rw = hrow ? rb : ra;
         if (rw >= nrows) continue;
         const int e0 = 2 * hrow;  // o[][e0]: first 16 dimensions, o[][e0 + 1]: the rest
+        const float l = hrow ? l1 : l0;
         if (un.nsplit == 1) {
-          const float inv = o_scale / (hrow ? l1 : l0);
+          const float inv = 1.f / l;
           uint16_t* orow = a.out + (int64_t)(un.q0 + rw / G) * a.out_stride +
                            (int64_t)(ug * G + rw % G) * kHeadSize + 32 * tig;
 #pragma unroll
@@ -800,20 +818,22 @@ __global__ void __launch_bounds__(CfgX2::kThreads, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const int j = q4 * 8 + 2 * k;
-                w[k] = pack_bf16(o[mt][j][e0 + h2] * inv, o[mt][j + 1][e0 + h2] * inv);
+                w[k] = pack_bf16((o[mt][j][e0 + h2] * inv - 1152.f) * o_scale,
+                                 (o[mt][j + 1][e0 + h2] * inv - 1152.f) * o_scale);
               }
               *reinterpret_cast<uint4*>(orow + h2 * 16 + q4 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         } else {
+          const float off = 1152.f * l;
           float* prow = ws.part_o + ((int64_t)un.part + rw) * kHeadSize + 32 * tig;
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int j = q4 * 4;
-              *reinterpret_cast<float4*>(prow + h2 * 16 + j) =
-                  make_float4(o[mt][j][e0 + h2] * o_scale, o[mt][j + 1][e0 + h2] * o_scale,
-                              o[mt][j + 2][e0 + h2] * o_scale, o[mt][j + 3][e0 + h2] * o_scale);
+              *reinterpret_cast<float4*>(prow + h2 * 16 + j) = make_float4(
+                  (o[mt][j][e0 + h2] - off) * o_scale, (o[mt][j + 1][e0 + h2] - off) * o_scale,
+                  (o[mt][j + 2][e0 + h2] - off) * o_scale, (o[mt][j + 3][e0 + h2] - off) * o_scale);
             }
           if (tig == 0)
             *reinterpret_cast<float2*>(ws.part_ml + ((int64_t)un.part + rw) * 2) =
