@@ -82,6 +82,21 @@ def test_int8_decode(hq, hkv, qn):
     _check_all(step, got, ref, "int8 decode hq=%d hkv=%d qn=%d" % (hq, hkv, qn))
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (8, 2)])
+def test_int8_decode_queries_with_large_offset_and_spread(hq, hkv):
+    """Queries 3 + 4 * N(0, 1): every score of a row carries a large common
+    part and the softmax is sharp.  The kernels feed the codes to the MMAs as
+    code + 1152, which adds 1152 * sum(q) to each score of a row and 1152 * L
+    to the output sums before both are taken out; this checks that nothing of
+    it shows at the tolerance, with and without splits."""
+    ctx = [0, 17, 300, 2100, 5000, 9000]
+    step = W.build(W.custom(ctx, [1] * len(ctx), hq, hkv, seed=4747 + hq))
+    q = W.bf16_to_f32(step.q)
+    step.q[...] = W.bf16_bits((3.0 + 4.0 * q).astype(np.float32))
+    ds, got, ref = run_int8(step, "int8 shifted queries")
+    _check_all(step, got, ref, "int8 decode, shifted queries hq=%d hkv=%d" % (hq, hkv))
+
+
 def test_int8_long_requests_split_and_merge():
     step = W.build(W.custom([9000, 3, 16384], [1, 1, 1], 32, 8, seed=43))
     ds, got, ref = run_int8(step, "int8 split")
