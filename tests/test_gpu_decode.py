@@ -49,6 +49,18 @@ def test_decode_groups_above_16(hq, hkv):
     run_and_check(step, "decode hq=%d hkv=%d" % (hq, hkv))
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (24, 1)])
+def test_decode_groups_above_16_several_units_per_worker(hq, hkv):
+    """About 2,400 short requests and two long split ones: with one unit per
+    request, every warp pair takes two or three units in turn, so the unit
+    hand-over through the pair's mailbox, the page ring's phases carried
+    from unit to unit and the query fragments loaded per unit all run."""
+    rng = np.random.default_rng(2024 + hq)
+    ctx = [int(c) for c in rng.integers(16, 300, size=2400)] + [5000, 9000]
+    step = W.build(W.custom(ctx, [1] * len(ctx), hq, hkv, seed=hq * 13 + 5))
+    run_and_check(step, "decode, several units per worker, hq=%d hkv=%d" % (hq, hkv))
+
+
 def test_decode_long_requests_split_and_merge():
     ctx = [5000, 9000, 3, 4097]
     step = W.build(W.custom(ctx, [1] * 4, 32, 8, seed=77))

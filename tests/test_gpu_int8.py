@@ -97,6 +97,19 @@ def test_int8_decode_queries_with_large_offset_and_spread(hq, hkv):
     _check_all(step, got, ref, "int8 decode, shifted queries hq=%d hkv=%d" % (hq, hkv))
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (24, 1)])
+def test_int8_decode_several_units_per_worker(hq, hkv):
+    """About 2,400 short requests and two long split ones over int8 codes:
+    every warp of the two-tile kernel takes two or three units in turn, so
+    the query buffer is refilled by TMA after the previous unit's fragments
+    were read from it and the page ring's phases carry over."""
+    rng = np.random.default_rng(4048 + hq)
+    ctx = [int(c) for c in rng.integers(16, 300, size=2400)] + [5000, 9000]
+    step = W.build(W.custom(ctx, [1] * len(ctx), hq, hkv, seed=hq * 17 + 3))
+    ds, got, ref = run_int8(step, "int8 several units per worker")
+    _check_all(step, got, ref, "int8 decode, several units per worker, hq=%d hkv=%d" % (hq, hkv))
+
+
 def test_int8_long_requests_split_and_merge():
     step = W.build(W.custom([9000, 3, 16384], [1, 1, 1], 32, 8, seed=43))
     ds, got, ref = run_int8(step, "int8 split")
