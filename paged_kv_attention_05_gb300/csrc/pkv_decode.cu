@@ -56,15 +56,14 @@ constexpr int kBox = kBlockSize * 128;     // one TMA box: 16 slots x 64 dims (2
 constexpr int kPage = 4 * kBox;            // K lo | K hi | V lo | V hi
 constexpr int kIdRegs = kMaxChunk / kBlockSize / 32;  // block ids per lane per unit
 
-// MT 16-row query tiles per warp (1: decode_kernel<1> serves every group of
-// up to 16 heads; larger groups take the warp pairs of decode_pair_kernel)
-template <int MT>
+// decode_kernel: one 16-row query tile per warp (groups of up to 16 heads;
+// larger groups take the warp pairs of decode_pair_kernel)
 struct Cfg {
   static constexpr int kWarps = 8;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kStages = MT == 1 ? 3 : 2;
+  static constexpr int kStages = 3;
   static constexpr int kStageBytes = kPage;
-  static constexpr int kQHalf = MT * 16 * 128;        // query rows x one 64-dim half
+  static constexpr int kQHalf = 16 * 128;             // query rows x one 64-dim half
   static constexpr int kWarpBytes = kStages * kStageBytes + 2 * kQHalf;
   static constexpr int kBarsPerWarp = kStages + 1;     // page stages, query
   static constexpr int kOffBar = kWarps * kWarpBytes;
@@ -137,11 +136,10 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int tok_lo, int valid)
   return v & (lo | hi);
 }
 
-template <int MT>
-__global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, AttnArgs a, Workspace ws) {
-  using C = Cfg<MT>;
+  using C = Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
@@ -162,8 +160,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   }
   // rows past a unit's qn * G query rows hold zeros or an earlier unit's
   // queries; their results are dropped
-  for (int i = lane; i < 2 * MT * 16 * 8; i += 32) {
-    const int row = (i >> 3) % (MT * 16), half = (i >> 3) / (MT * 16), c = i & 7;
+  for (int i = lane; i < 2 * 16 * 8; i += 32) {
+    const int row = (i >> 3) % 16, half = (i >> 3) / 16, c = i & 7;
     if (row >= G)
       *reinterpret_cast<uint4*>(smem + (qbuf - sbase) + half * C::kQHalf + row * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
@@ -223,17 +221,15 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         tma_load_3d(qbuf + C::kQHalf + i * G * 128, &tm_q, q_bar, 64, ug * G, q0 + i);
       }
     }
-    // last visible key + 1 of the two rows this thread holds in each tile:
-    // row (token i, head) sees keys < ctx + i + 1, clipped to the unit
-    int vis[MT][2];
+    // last visible key + 1 of the two rows this thread holds: row (token i,
+    // head) sees keys < ctx + i + 1, clipped to the unit
+    int vis[2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int hrow = 0; hrow < 2; ++hrow) {
-        const int row = mt * 16 + (lane >> 2) + hrow * 8;
-        const int ti = row < nrows ? row / G : qn - 1;
-        vis[mt][hrow] = min(k1, un.ctx + ti + 1);
-      }
+    for (int hrow = 0; hrow < 2; ++hrow) {
+      const int row = (lane >> 2) + hrow * 8;
+      const int ti = row < nrows ? row / G : qn - 1;
+      vis[hrow] = min(k1, un.ctx + ti + 1);
+    }
 
     // page p of the unit into stage (page_cnt + p) % kStages; the stage's
     // previous page was consumed by this warp already (program order)
@@ -258,27 +254,20 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     for (int p = 0; p < C::kStages && p < npages; ++p) issue_page(p);
     if (!mbar_wait_warp(q_bar, unit_cnt & 1, abort, ws.err)) break;
 
-    // query fragments: registers for one tile, re-read from shared memory for two
-    uint32_t qa[MT == 1 ? 8 : 1][4];
-    if (MT == 1) {
+    // the query fragments, in registers for the whole unit
+    uint32_t qa[8][4];
 #pragma unroll
-      for (int kstep = 0; kstep < (MT == 1 ? 8 : 1); ++kstep)
-        ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf + sw128(rr + ((mi & 1) << 3),
-                                                         (kstep & 3) * 2 + (mi >> 1)),
-                qa[kstep][0], qa[kstep][1], qa[kstep][2], qa[kstep][3]);
-    }
+    for (int kstep = 0; kstep < 8; ++kstep)
+      ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf + sw128(rr + ((mi & 1) << 3),
+                                                       (kstep & 3) * 2 + (mi >> 1)),
+              qa[kstep][0], qa[kstep][1], qa[kstep][2], qa[kstep][3]);
 
-    float o[MT][16][4];
-    float m_run[MT][2], l_run[MT][2];
+    float o[16][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int dn = 0; dn < 16; ++dn)
 #pragma unroll
-      for (int dn = 0; dn < 16; ++dn)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[mt][dn][e] = 0.f;
-      m_run[mt][0] = m_run[mt][1] = -INFINITY;
-      l_run[mt][0] = l_run[mt][1] = 0.f;
-    }
+      for (int e = 0; e < 4; ++e) o[dn][e] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     bool ok = true;
     for (int p = 0; p < npages; ++p) {
@@ -293,39 +282,24 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       const uint32_t st = wbase + s * C::kStageBytes;
 
       // S = Q K^T for the page's 16 keys (two n-tiles of 8)
-      float sacc[MT][2][4];
+      float sacc[2][4];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
 #pragma unroll
       for (int kstep = 0; kstep < 8; ++kstep) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(st + (kstep >> 2) * kBox + sw128(rr + ((mi >> 1) << 3), (kstep & 3) * 2 + (mi & 1)),
                 b0, b1, b2, b3);
-        if (MT == 1) {
-          mma_bf16(sacc[0][0], qa[MT == 1 ? kstep : 0], b0, b1);
-          mma_bf16(sacc[0][1], qa[MT == 1 ? kstep : 0], b2, b3);
-        } else {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            uint32_t qf[4];
-            ldsm_x4(qbuf + (kstep >> 2) * C::kQHalf +
-                        sw128(mt * 16 + rr + ((mi & 1) << 3), (kstep & 3) * 2 + (mi >> 1)),
-                    qf[0], qf[1], qf[2], qf[3]);
-            mma_bf16(sacc[mt][0], qf, b0, b1);
-            mma_bf16(sacc[mt][1], qf, b2, b3);
-          }
-        }
+        mma_bf16(sacc[0], qa[kstep], b0, b1);
+        mma_bf16(sacc[1], qa[kstep], b2, b3);
       }
 
       // online softmax in the log2 domain, keys >= k1 masked; the output is
       // rescaled only when a row's maximum grows by more than 2^8
-      uint32_t pa[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
+      uint32_t pa[4];
+      {
         float xs[2][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -333,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int tok = nt * 8 + tig * 2 + (e & 1);
-            xs[nt][e] = pos0 + tok < vis[mt][e >> 1] ? sacc[mt][nt][e] * sl2 : -INFINITY;
+            xs[nt][e] = pos0 + tok < vis[e >> 1] ? sacc[nt][e] * sl2 : -INFINITY;
           }
           mx0 = fmaxf(mx0, fmaxf(xs[nt][0], xs[nt][1]));
           mx1 = fmaxf(mx1, fmaxf(xs[nt][2], xs[nt][3]));
@@ -342,40 +316,40 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const bool up0 = mx0 > m_run[mt][0] + 8.f, up1 = mx1 > m_run[mt][1] + 8.f;
+        const bool up0 = mx0 > m_run[0] + 8.f, up1 = mx1 > m_run[1] + 8.f;
         if (__any_sync(0xffffffffu, up0 || up1)) {
-          const float n0 = up0 ? mx0 : m_run[mt][0], n1 = up1 ? mx1 : m_run[mt][1];
+          const float n0 = up0 ? mx0 : m_run[0], n1 = up1 ? mx1 : m_run[1];
           // (a row that did not grow keeps factor 1: its maximum may still be -inf)
-          const float al0 = up0 ? fast_exp2(m_run[mt][0] - n0) : 1.f;
-          const float al1 = up1 ? fast_exp2(m_run[mt][1] - n1) : 1.f;
-          m_run[mt][0] = n0;
-          m_run[mt][1] = n1;
-          l_run[mt][0] *= al0;
-          l_run[mt][1] *= al1;
+          const float al0 = up0 ? fast_exp2(m_run[0] - n0) : 1.f;
+          const float al1 = up1 ? fast_exp2(m_run[1] - n1) : 1.f;
+          m_run[0] = n0;
+          m_run[1] = n1;
+          l_run[0] *= al0;
+          l_run[1] *= al1;
 #pragma unroll
           for (int dn = 0; dn < 16; ++dn) {
-            o[mt][dn][0] *= al0;
-            o[mt][dn][1] *= al0;
-            o[mt][dn][2] *= al1;
-            o[mt][dn][3] *= al1;
+            o[dn][0] *= al0;
+            o[dn][1] *= al0;
+            o[dn][2] *= al1;
+            o[dn][3] *= al1;
           }
         }
         // a row with no visible key yet keeps m = -inf: use 0 as its reference
-        const float c0 = m_run[mt][0] == -INFINITY ? 0.f : m_run[mt][0];
-        const float c1 = m_run[mt][1] == -INFINITY ? 0.f : m_run[mt][1];
+        const float c0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float c1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           xs[nt][0] = fast_exp2(xs[nt][0] - c0);
           xs[nt][1] = fast_exp2(xs[nt][1] - c0);
           xs[nt][2] = fast_exp2(xs[nt][2] - c1);
           xs[nt][3] = fast_exp2(xs[nt][3] - c1);
-          l_run[mt][0] += xs[nt][0] + xs[nt][1];
-          l_run[mt][1] += xs[nt][2] + xs[nt][3];
+          l_run[0] += xs[nt][0] + xs[nt][1];
+          l_run[1] += xs[nt][2] + xs[nt][3];
         }
-        pa[mt][0] = pack_bf16(xs[0][0], xs[0][1]);
-        pa[mt][1] = pack_bf16(xs[0][2], xs[0][3]);
-        pa[mt][2] = pack_bf16(xs[1][0], xs[1][1]);
-        pa[mt][3] = pack_bf16(xs[1][2], xs[1][3]);
+        pa[0] = pack_bf16(xs[0][0], xs[0][1]);
+        pa[1] = pack_bf16(xs[0][2], xs[0][3]);
+        pa[2] = pack_bf16(xs[1][0], xs[1][1]);
+        pa[3] = pack_bf16(xs[1][2], xs[1][3]);
       }
 
       // O += P V (V rows read transposed); V of keys past the unit zeroed
@@ -390,11 +364,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           b1 = mask_pair(b1, 8 + 2 * tig, valid);
           b3 = mask_pair(b3, 8 + 2 * tig, valid);
         }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16(o[mt][dn], pa[mt], b0, b1);
-          mma_bf16(o[mt][dn + 1], pa[mt], b2, b3);
-        }
+        mma_bf16(o[dn], pa, b0, b1);
+        mma_bf16(o[dn + 1], pa, b2, b3);
       }
       __syncwarp();
       if (p + C::kStages < npages) issue_page(p + C::kStages);
@@ -403,48 +374,45 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     page_cnt += npages;
 
     // finish: row sums across the quad, then output or split partials
+    float l0 = l_run[0], l1 = l_run[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int ra = gid, rb = ra + 8;  // rows: token * G + head in group
+    if (un.nsplit == 1) {
+      const int q0 = un.q0;
+      // row -> out[q0 + row / G][g * G + row % G]
+      uint16_t* oa = a.out + (int64_t)(q0 + ra / G) * a.out_stride +
+                     (int64_t)(ug * G + ra % G) * kHeadSize;
+      uint16_t* ob = a.out + (int64_t)(q0 + rb / G) * a.out_stride +
+                     (int64_t)(ug * G + rb % G) * kHeadSize;
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      float l0 = l_run[mt][0], l1 = l_run[mt][1];
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      const int ra = mt * 16 + gid, rb = ra + 8;  // rows: token * G + head in group
-      if (un.nsplit == 1) {
-        const int q0 = un.q0;
-        // row -> out[q0 + row / G][g * G + row % G]
-        uint16_t* oa = a.out + (int64_t)(q0 + ra / G) * a.out_stride +
-                       (int64_t)(ug * G + ra % G) * kHeadSize;
-        uint16_t* ob = a.out + (int64_t)(q0 + rb / G) * a.out_stride +
-                       (int64_t)(ug * G + rb % G) * kHeadSize;
-        const float i0 = 1.f / l0, i1 = 1.f / l1;
+      for (int dn = 0; dn < 16; ++dn) {
+        const int col = dn * 8 + tig * 2;
+        if (ra < nrows)
+          *reinterpret_cast<uint32_t*>(oa + col) = pack_bf16(o[dn][0] * i0, o[dn][1] * i0);
+        if (rb < nrows)
+          *reinterpret_cast<uint32_t*>(ob + col) = pack_bf16(o[dn][2] * i1, o[dn][3] * i1);
+      }
+    } else {
+      const int64_t pra = (int64_t)un.part + ra, prb = (int64_t)un.part + rb;
 #pragma unroll
-        for (int dn = 0; dn < 16; ++dn) {
-          const int col = dn * 8 + tig * 2;
-          if (ra < nrows)
-            *reinterpret_cast<uint32_t*>(oa + col) = pack_bf16(o[mt][dn][0] * i0, o[mt][dn][1] * i0);
-          if (rb < nrows)
-            *reinterpret_cast<uint32_t*>(ob + col) = pack_bf16(o[mt][dn][2] * i1, o[mt][dn][3] * i1);
-        }
-      } else {
-        const int64_t pra = (int64_t)un.part + ra, prb = (int64_t)un.part + rb;
-#pragma unroll
-        for (int dn = 0; dn < 16; ++dn) {
-          const int col = dn * 8 + tig * 2;
-          if (ra < nrows)
-            *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
-                make_float2(o[mt][dn][0], o[mt][dn][1]);
-          if (rb < nrows)
-            *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
-                make_float2(o[mt][dn][2], o[mt][dn][3]);
-        }
-        if (tig == 0) {
-          if (ra < nrows)
-            *reinterpret_cast<float2*>(ws.part_ml + pra * 2) = make_float2(m_run[mt][0], l0);
-          if (rb < nrows)
-            *reinterpret_cast<float2*>(ws.part_ml + prb * 2) = make_float2(m_run[mt][1], l1);
-        }
+      for (int dn = 0; dn < 16; ++dn) {
+        const int col = dn * 8 + tig * 2;
+        if (ra < nrows)
+          *reinterpret_cast<float2*>(ws.part_o + pra * kHeadSize + col) =
+              make_float2(o[dn][0], o[dn][1]);
+        if (rb < nrows)
+          *reinterpret_cast<float2*>(ws.part_o + prb * kHeadSize + col) =
+              make_float2(o[dn][2], o[dn][3]);
+      }
+      if (tig == 0) {
+        if (ra < nrows)
+          *reinterpret_cast<float2*>(ws.part_ml + pra * 2) = make_float2(m_run[0], l0);
+        if (rb < nrows)
+          *reinterpret_cast<float2*>(ws.part_ml + prb * 2) = make_float2(m_run[1], l1);
       }
     }
   }
@@ -800,18 +768,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttnArgs a, Wo
   combine_splits(a, ws, blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), gridDim.x * kWarpsPerBlock);
 }
 
-template <int MT>
-cudaError_t launch_mt(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
-  using C = Cfg<MT>;
+cudaError_t launch_one_tile(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
+  using C = Cfg;
   static std::atomic<bool> attr[kMaxAttrDevices];
-  if (cudaError_t e = smem_attr_once(decode_kernel<MT>, C::kSmem, attr)) return e;
+  if (cudaError_t e = smem_attr_once(decode_kernel, C::kSmem, attr)) return e;
   const int G = a.hq / a.hkv;
   CUtensorMap tq, tk, tv;
   if (!make_rows_map(&tq, a.q, a.q_rows, a.hq, a.q_stride, G, 1) ||
       !make_cache_map(&tk, a.kc, a.num_blocks, a.hkv) ||
       !make_cache_map(&tv, a.vc, a.num_blocks, a.hkv))
     return cudaErrorInvalidValue;
-  return launch_dependent(decode_kernel<MT>, dim3(sms), dim3(C::kThreads), C::kSmem, st, tq, tk,
+  return launch_dependent(decode_kernel, dim3(sms), dim3(C::kThreads), C::kSmem, st, tq, tk,
                           tv, a, ws);
 }
 
@@ -829,13 +796,13 @@ cudaError_t launch_pair(const AttnArgs& a, const Workspace& ws, int sms, cudaStr
 }  // namespace
 
 int decode_workers(int group, int kv_int8, int sms) {
-  return sms * (kv_int8 ? decode_i8_warps(group) : (group <= 16 ? Cfg<1>::kWarps : CfgP::kPairs));
+  return sms * (kv_int8 ? decode_i8_warps(group) : (group <= 16 ? Cfg::kWarps : CfgP::kPairs));
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
   const int G = a.hq / a.hkv;
   if (a.kv_int8) return launch_decode_i8(a, ws, sms, st);
-  return G <= 16 ? launch_mt<1>(a, ws, sms, st) : launch_pair(a, ws, sms, st);
+  return G <= 16 ? launch_one_tile(a, ws, sms, st) : launch_pair(a, ws, sms, st);
 }
 
 cudaError_t launch_combine(const AttnArgs& a, const Workspace& ws, int sms, cudaStream_t st) {
