@@ -35,52 +35,57 @@ namespace {
 
 constexpr int kPlanThreads = 1024;  // the most threads of a plan CTA
 
-// Exclusive block-wide prefix sums of four ints per thread (any whole number
-// of warps up to 32), the four scans sharing their barriers.
-__device__ int4 block_exclusive_scan4(int4 x, int4* total, int4* smem33) {
+// Exclusive block-wide prefix sums of eight ints per thread (two int4; any
+// whole number of warps up to 32), the eight scans sharing their barriers;
+// *tx / *ty receive the block totals.
+__device__ void block_exclusive_scan8(int4 x, int4 y, int4* ox, int4* oy, int4* tx, int4* ty,
+                                      int4* sx, int4* sy) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int4 incl = x;
+  auto add4 = [](int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+  auto sub4 = [](int4 a, int4 b) { return make_int4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); };
+  auto shfl_up4 = [](int4 v, int o) {
+    return make_int4(__shfl_up_sync(0xffffffffu, v.x, o), __shfl_up_sync(0xffffffffu, v.y, o),
+                     __shfl_up_sync(0xffffffffu, v.z, o), __shfl_up_sync(0xffffffffu, v.w, o));
+  };
+  int4 ix = x, iy = y;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y0 = __shfl_up_sync(0xffffffffu, incl.x, o);
-    const int y1 = __shfl_up_sync(0xffffffffu, incl.y, o);
-    const int y2 = __shfl_up_sync(0xffffffffu, incl.z, o);
-    const int y3 = __shfl_up_sync(0xffffffffu, incl.w, o);
+    const int4 px = shfl_up4(ix, o), py = shfl_up4(iy, o);
     if (lane >= o) {
-      incl.x += y0;
-      incl.y += y1;
-      incl.z += y2;
-      incl.w += y3;
+      ix = add4(ix, px);
+      iy = add4(iy, py);
     }
   }
-  if (lane == 31) smem33[warp] = incl;
+  if (lane == 31) {
+    sx[warp] = ix;
+    sy[warp] = iy;
+  }
   __syncthreads();
   if (warp == 0) {
-    const int4 w = lane < nw ? smem33[lane] : make_int4(0, 0, 0, 0);
-    int4 wi = w;
+    const int4 z = make_int4(0, 0, 0, 0);
+    const int4 wx = lane < nw ? sx[lane] : z, wy = lane < nw ? sy[lane] : z;
+    int4 jx = wx, jy = wy;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y0 = __shfl_up_sync(0xffffffffu, wi.x, o);
-      const int y1 = __shfl_up_sync(0xffffffffu, wi.y, o);
-      const int y2 = __shfl_up_sync(0xffffffffu, wi.z, o);
-      const int y3 = __shfl_up_sync(0xffffffffu, wi.w, o);
+      const int4 px = shfl_up4(jx, o), py = shfl_up4(jy, o);
       if (lane >= o) {
-        wi.x += y0;
-        wi.y += y1;
-        wi.z += y2;
-        wi.w += y3;
+        jx = add4(jx, px);
+        jy = add4(jy, py);
       }
     }
-    smem33[lane] = make_int4(wi.x - w.x, wi.y - w.y, wi.z - w.z, wi.w - w.w);  // exclusive
-    if (lane == 31) smem33[32] = wi;
+    sx[lane] = sub4(jx, wx);  // exclusive
+    sy[lane] = sub4(jy, wy);
+    if (lane == 31) {
+      sx[32] = jx;
+      sy[32] = jy;
+    }
   }
   __syncthreads();
-  const int4 wo = smem33[warp];
-  const int4 res = make_int4(wo.x + incl.x - x.x, wo.y + incl.y - x.y, wo.z + incl.z - x.z,
-                             wo.w + incl.w - x.w);
-  *total = smem33[32];
+  *ox = add4(sx[warp], sub4(ix, x));
+  *oy = add4(sy[warp], sub4(iy, y));
+  *tx = sx[32];
+  *ty = sy[32];
   __syncthreads();
-  return res;
 }
 
 // Last index i in [0, n) with off[i] <= x: the request that owns entry x
@@ -130,7 +135,7 @@ __device__ ReqInfo classify(const AttnArgs& a, int r) {
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspace ws,
                                                             int dec_grid) {
-  __shared__ int4 smem33[33];
+  __shared__ int4 smem33[33], smem33b[33];
   __shared__ long long red[32];
   const int tid = threadIdx.x, nt = blockDim.x, nw = nt >> 5;
   // Let the decode grid set up at once.  The metadata is read before the
@@ -339,19 +344,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     } else if (ri.kind == 2) {
       tiles = (ri.n + kPreTileQ - 1) / kPreTileQ;
     }
-    int4 tot;
-    const int4 off = block_exclusive_scan4(make_int4(units, parts, tiles, pairs), &tot, smem33);
+    // the per-request offsets, and those inside the classes: full chunks and
+    // the last piece's class 1..3; a request's units are its full chunks and
+    // its last piece (class 1..4), so class 4's offsets are what remains
+    const int lu = units - fulls;  // a.hkv or 0
+    int4 off, off2, tot, tot2;
+    block_exclusive_scan8(make_int4(units, parts, tiles, pairs),
+                          make_int4(fulls, lcls == 1 ? lu : 0, lcls == 2 ? lu : 0, lcls == 3 ? lu : 0),
+                          &off, &off2, &tot, &tot2, smem33, smem33b);
     const int off_u = off.x, off_p = off.y, off_t = off.z, off_q = off.w;
     const int tot_u = tot.x, tot_p = tot.y, tot_t = tot.z, tot_q = tot.w;
-    // offsets inside the classes: full chunks, and the last piece's class
-    const int lu = units - fulls;  // a.hkv or 0
-    int4 tot2, tot3;
-    const int4 off2 = block_exclusive_scan4(
-        make_int4(fulls, lcls == 1 ? lu : 0, lcls == 2 ? lu : 0, lcls == 3 ? lu : 0), &tot2, smem33);
-    const int4 off3 = block_exclusive_scan4(make_int4(lcls == 4 ? lu : 0, 0, 0, 0), &tot3, smem33);
+    const int off4 = off_u - (off2.x + off2.y + off2.z + off2.w);
+    const int tot4 = tot_u - (tot2.x + tot2.y + tot2.z + tot2.w);
     s_off_f[tid] = cls_base[0] + cls_carry[0] + off2.x;
     {
-      const int ofs = lcls == 1 ? off2.y : (lcls == 2 ? off2.z : (lcls == 3 ? off2.w : off3.x));
+      const int ofs = lcls == 1 ? off2.y : (lcls == 2 ? off2.z : (lcls == 3 ? off2.w : off4));
       s_off_l[tid] = lcls == 0 ? 0 : cls_base[lcls] + cls_carry[lcls] + ofs;
     }
     s_off_u[tid] = off_u;
@@ -415,7 +422,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnArgs a, Workspac
     cls_carry[1] += tot2.y;
     cls_carry[2] += tot2.z;
     cls_carry[3] += tot2.w;
-    cls_carry[4] += tot3.x;
+    cls_carry[4] += tot4;
     part_carry += tot_p;
     pre_carry += tot_t;
     pair_carry += tot_q;
