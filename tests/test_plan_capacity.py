@@ -33,7 +33,8 @@ def plan_counts(ctx, q_len, hq, hkv, workers, caps):
     kernel chooses it (about four units per decode worker, whole 64-key
     tiles, between max(256, 32 G) and 2048 keys; shorter where every pair's
     splits fit one wave of workers and the workspace holds them; longer, by
-    less than twice, where that makes one wave instead of more), then the
+    less than twice, where that makes one wave instead of more; in the first
+    case a chunk of 256 keys or more is cut at whole 16-key pages), then the
     units, split pairs, partial rows and prefill tiles of that chunk."""
     G = hq // hkv
     decs, pres = [], []
@@ -53,9 +54,11 @@ def plan_counts(ctx, q_len, hq, hkv, workers, caps):
         chunk = min(max(want, lo), 2048)
         if pairs * -(-lmax // chunk) <= workers:
             per_pair = workers // pairs
-            c = -(-lmax // per_pair)
-            c = -(-c // 64) * 64
-            if c < 256:
+            c1 = -(-lmax // per_pair)
+            c = -(-c1 // 64) * 64
+            if c >= 256:
+                c = max(-(-c1 // 16) * 16, 256)
+            else:
                 per = min(per_pair, caps["decode_units"] // pairs,
                           caps["partial_rows"] // (pairs * max(rmax, 1)))
                 c2 = -(-lmax // per) if per >= 1 else 256
